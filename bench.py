@@ -1,0 +1,501 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one decode step of a continuous-batching layer on the decode-batch
+workload (64 sequences, Llama-3.1-8B attention shape: 32 q / 8 kv heads,
+d128, bf16, block size 16, cache lengths uniform in 1024..16384): the 64 new
+tokens' K/V are written into the paged cache by slot mapping, then paged
+decode attention runs over the updated cache.  The headline value is the
+step's algorithmic HBM bytes per second (attended K/V + Q + O of the decode,
+plus the written rows read and stored), i.e. paged-decode HBM GB/s.
+
+Also measured in the same run (``also``): the long-context decode workload
+(8 x 131072 tokens, 64 q / 8 kv heads) with a bf16 and an FP8-E4M3 cache, and
+the causal varlen prefill workload (TFLOP/s) when the library provides it.
+
+``--impl reference`` times the CPU oracle (fp64 NumPy) on bounded samples of
+the same workload, as the reference arm.
+
+Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
+``torch.distributed.run`` every rank runs its own replica (no collective on
+the data path) and rank 0 prints one JSON line.
+"""
+
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn HBM GB/s (% of peak) & tokens/s; varlen prefill TFLOP/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 126 * 2 ** 20
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def profile_traffic(kernel_key):
+    """Per-launch DRAM bytes from a committed ncu summary, or None if the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+    try:
+        rows = {}
+        with open(path) as f:
+            for line in f:
+                line = line.strip()
+                if not line or line.startswith("#"):
+                    continue
+                key, src, digest, nbytes = line.split()[:4]
+                rows[key] = (src, digest, float(nbytes))
+        if kernel_key not in rows:
+            return None
+        src, digest, nbytes = rows[kernel_key]
+        with open(os.path.join(ROOT, src), "rb") as f:
+            now = hashlib.sha256(f.read()).hexdigest()[:16]
+        return nbytes if now == digest else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.lines = []
+        try:
+            props = torch.cuda.get_device_properties(device)
+            uuid = str(getattr(props, "uuid", "") or "")
+            sel = ["-i", "GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid] if uuid else []
+            self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms",
+                        "200"] + sel
+        except Exception:
+            self.cmd = None
+
+    def start(self):
+        if not self.cmd:
+            return
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.6)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+
+def decode_bytes(wl):
+    """Algorithmic HBM bytes of one decode call: attended K/V + Q + O."""
+    elt = 1 if wl.cache_dtype == "fp8_e4m3" else 2
+    lens = wl.lens_before + 1
+    kv = int(lens.sum()) * wl.num_kv_heads * wl.head_dim * elt * 2
+    qo = 2 * wl.batch * wl.num_heads * wl.head_dim * 2
+    return kv + qo
+
+
+def write_bytes(wl):
+    """Algorithmic bytes of the KV write: new rows read (bf16) + stored (cache dtype), K and V."""
+    elt = 1 if wl.cache_dtype == "fp8_e4m3" else 2
+    row = wl.num_kv_heads * wl.head_dim
+    return wl.batch * row * (2 + elt) * 2
+
+
+class DecodeStep:
+    def __init__(self, pkv, wl):
+        self.pkv, self.wl = pkv, wl
+        shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+        self.kc4 = wl.k_cache.view(shape4)
+        self.vc4 = wl.v_cache.view(shape4)
+        self.out = torch.empty_like(wl.q)
+        need = pkv.lib().pkv_paged_attn_decode_workspace(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim,
+                                                         wl.max_seqlen)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=wl.q.device)
+        self.launches = 2 + (1 if need > 0 else 0)
+
+    def write(self, k_new=None, v_new=None, slots=None):
+        wl = self.wl
+        self.pkv.kv_cache_write(wl.k_new if k_new is None else k_new, wl.v_new if v_new is None else v_new,
+                                wl.k_cache, wl.v_cache, wl.slot_mapping if slots is None else slots,
+                                k_inv_scale=wl.k_inv_scale, v_inv_scale=wl.v_inv_scale)
+
+    def decode(self, q=None, seqlens=None, table=None, out=None):
+        wl = self.wl
+        self.pkv.paged_attn_decode(wl.q if q is None else q, self.kc4, self.vc4,
+                                   wl.cache_seqlens if seqlens is None else seqlens,
+                                   wl.block_table if table is None else table, wl.scale,
+                                   max_seqlen_k=wl.max_seqlen, k_scale=wl.k_scale, v_scale=wl.v_scale,
+                                   out=self.out if out is None else out, workspace_buf=self.ws)
+
+
+def time_decode_steps(step, steps, warmup):
+    """Device-timed loop of write+decode; returns (ms per step, mean decode-call ms)."""
+    for _ in range(warmup):
+        step.write()
+        step.decode()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        step.write()
+        ev[i][0].record()
+        step.decode()
+        ev[i][1].record()
+    end.record()
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    dec = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return total / steps, dec
+
+
+def time_e2e(step, steps, warmup):
+    """Per step: H2D of the step's inputs from pinned memory, write + decode, D2H of the output."""
+    wl = step.wl
+    host = {name: getattr(wl, name).cpu().pin_memory() for name in
+            ("q", "k_new", "v_new", "slot_mapping", "cache_seqlens", "block_table")}
+    dev = {name: torch.empty_like(getattr(wl, name)) for name in host}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for name, t in host.items():
+            dev[name].copy_(t, non_blocking=True)
+        step.write(dev["k_new"], dev["v_new"], dev["slot_mapping"])
+        step.decode(dev["q"], dev["cache_seqlens"], dev["block_table"])
+        out_host.copy_(step.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def sampled_oracle_decode(wl, seqs):
+    """Copy the sampled sequences' blocks to the host and run the oracle on them."""
+    import oracle as O
+    table = wl.block_table.cpu().numpy()
+    lens = wl.cache_seqlens.cpu().numpy()
+    blocks = sorted({int(x) for s in seqs for x in table[s][:-(-int(lens[s]) // wl.block_size)]})
+    remap = {b: i for i, b in enumerate(blocks)}
+    idx = torch.tensor(blocks, device=wl.q.device)
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+
+    def host_bits(t):
+        t = t.view(shape4)[idx].reshape(-1, wl.num_kv_heads, wl.head_dim).cpu()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    kc, vc = host_bits(wl.k_cache), host_bits(wl.v_cache)
+    tsub = np.full_like(table, -1)
+    for s in seqs:
+        n = -(-int(lens[s]) // wl.block_size)
+        tsub[s, :n] = [remap[int(x)] for x in table[s][:n]]
+    q = wl.q.cpu().view(torch.int16).numpy().view(np.uint16)
+    return O, q, kc, vc, lens, tsub
+
+
+def oracle_decode_rate(wl, budget_s, max_seqs=64, truncate=None):
+    """Oracle throughput (algorithmic bytes/s) on whole (or truncated) sampled sequences."""
+    order = list(np.random.default_rng(0).permutation(wl.batch))[:max_seqs]
+    O, q, kc, vc, lens, tsub = sampled_oracle_decode(wl, order[:max(1, min(len(order), 8))])
+    elt = 1 if wl.cache_dtype == "fp8_e4m3" else 2
+    done_bytes, done_tok, nseq = 0, 0, 0
+    t0 = time.perf_counter()
+    for s in order[:8]:
+        L = int(lens[s]) if truncate is None else min(int(lens[s]), truncate)
+        l2 = lens.copy()
+        l2[s] = L
+        O.paged_attn_decode(q, kc, vc, l2, tsub, wl.block_size, wl.scale, wl.cache_dtype, wl.k_scale,
+                            wl.v_scale, seqs=[s])
+        done_bytes += L * wl.num_kv_heads * wl.head_dim * elt * 2 + 2 * wl.num_heads * wl.head_dim * 2
+        done_tok += L
+        nseq += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done_bytes / dt, nseq, done_tok, dt
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+
+def run_pkv(args, rank, world, device):
+    from paged_kv_cache_200_gb300 import build as B
+    from paged_kv_cache_200_gb300 import pkv
+    from paged_kv_cache_200_gb300 import workloads as W
+
+    if rank == 0 or not os.path.exists(B.LIB_PATH):
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pkv.lib()
+    pk = peaks()
+
+    wl = W.decode_batch(device=device)
+    step = DecodeStep(pkv, wl)
+    nbytes = decode_bytes(wl) + write_bytes(wl)
+
+    # CPU baseline (rank 0 only): the oracle on a bounded sample of the same workload
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, nseq, ntok, dt = oracle_decode_rate(wl, budget_s=args.cpu_budget)
+        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nseq} whole sequences of the decode batch ({ntok} cached tokens, all 32 heads), "
+                         f"fp64 NumPy, single thread, {dt:.1f} s"}
+
+    clocks = ClockSampler(device)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ms, dec_ms = time_decode_steps(step, args.steps, args.warmup)
+    clk = clocks.stop()
+    t = torch.tensor([ms], device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+    ms_max = float(t.item())
+
+    e2e_ms, h2d, d2h = time_e2e(step, max(1, min(args.steps, args.e2e_steps)), 3)
+    te = torch.tensor([e2e_ms], device=device)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+
+    also = {}
+    if not args.no_extra:
+        also.update(extra_workloads(pkv, W, device, pk, args))
+
+    dec_bytes = decode_bytes(wl)
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = profile_traffic("paged_decode_split_bf16_d128")
+    result = {
+        "metric": METRIC,
+        "value": world * nbytes / (ms_max * 1e-3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q, seeded lengths and permuted block pool)",
+        "config": {
+            "workload": "decode_batch64: 64 seqs, cached lengths U[1024,16384] + 1 new token each, 32 q / 8 kv "
+                        "heads, head_dim 128, bf16 cache, block_size 16, permuted pool; step = KV write of the 64 "
+                        "new tokens + paged decode attention",
+            "batch": wl.batch,
+            "attended_tokens": int((wl.lens_before + 1).sum()),
+            "bytes_per_step": nbytes,
+            "l2": "inputs larger than L2 (%.2f GB of K/V read per step)" % (dec_bytes / 1e9),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "tokens_per_s": world * wl.batch / (ms_max * 1e-3),
+        "roofline": {
+            "kernel": "paged_attn_decode (split-KV kernel + combine, one call)",
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": pk["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"],
+            "traffic": traffic,
+            "algorithmic_bytes": dec_bytes,
+            "launch_ms": dec_ms,
+            "peak_source": pk["source"],
+        },
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": step.launches * args.steps,
+        "clocks": clk,
+        "also": also,
+    }
+    if cpu is not None:
+        result["cpu_baseline"] = cpu
+    return result
+
+
+def extra_workloads(pkv, W, device, pk, args):
+    out = {}
+    for dt in ("bf16", "fp8_e4m3"):
+        wl = W.long_decode(device=device, cache_dtype=dt)
+        step = DecodeStep(pkv, wl)
+        steps = max(10, min(200, args.steps // 10))
+        ms, dec_ms = time_decode_steps(step, steps, 3)
+        b = decode_bytes(wl)
+        ach = b / (dec_ms * 1e-3) / 1e9
+        out[f"long_decode_{dt}"] = {
+            "workload": "8 seqs x 131072 cached tokens (+1), 64 q / 8 kv heads, d128, block 32, " + dt + " cache",
+            "decode_ms": dec_ms, "step_ms": ms, "GB_per_s": ach, "frac_of_hbm_peak": ach / pk["hbm_gbs"],
+            "tokens_per_s": wl.batch / (ms * 1e-3), "steps": steps}
+        del step, wl
+        torch.cuda.empty_cache()
+    if hasattr(pkv, "paged_attn_varlen") and hasattr(pkv.lib(), "pkv_paged_attn_varlen"):
+        out.update(prefill_workload(pkv, W, device, pk, args))
+    return out
+
+
+def prefill_workload(pkv, W, device, pk, args):
+    import prefill_bench  # noqa: F401  (provided with the varlen kernel)
+    return prefill_bench.measure(pkv, W, device, pk, args)
+
+
+def run_reference(args):
+    """The CPU oracle on bounded samples of the decode-batch workload (rank 0 only)."""
+    from paged_kv_cache_200_gb300 import workloads as W
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = W.decode_batch(device=device)
+    budget = 150.0
+    # calibrate: oracle time for a 1024-token sample
+    O, q, kc, vc, lens, tsub = sampled_oracle_decode(wl, list(range(wl.batch)))
+    order = list(np.random.default_rng(0).permutation(wl.batch))
+    t0 = time.perf_counter()
+    l2 = lens.copy()
+    l2[order[0]] = 1024
+    O.paged_attn_decode(q, kc, vc, l2, tsub, wl.block_size, wl.scale, seqs=[order[0]])
+    t1024 = time.perf_counter() - t0
+    per_step = budget / (args.steps + args.warmup)
+    n = int(max(16, min(int(lens.max()), 1024 * per_step / max(t1024, 1e-6))))
+    elt = 2
+
+    def one(i):
+        s = order[i % len(order)]
+        L = min(int(lens[s]), n)
+        l3 = lens.copy()
+        l3[s] = L
+        O.paged_attn_decode(q, kc, vc, l3, tsub, wl.block_size, wl.scale, seqs=[s])
+        return L * wl.num_kv_heads * wl.head_dim * elt * 2 + 2 * wl.num_heads * wl.head_dim * 2
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        nbytes += one(args.warmup + i)
+    dt = time.perf_counter() - t0
+    val = nbytes / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_batch64 (same as the main arm), bounded samples: one sequence per step "
+                               f"truncated to {n} cached tokens, all 32 heads"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"one sequence per step, up to {n} cached tokens, fp64 NumPy, single thread"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    res = run_pkv(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

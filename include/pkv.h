@@ -1,0 +1,154 @@
+/*
+ * pkv.h -- C ABI of libpkv, paged KV-cache attention for one NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, in the order a serving layer calls them for one step:
+ *
+ *   pkv_kv_cache_write      scatter each new token's K/V row into the paged cache
+ *   pkv_paged_attn_decode   one query token per sequence over its paged cache
+ *   pkv_paged_attn_varlen   causal GQA attention over packed variable-length
+ *                           sequences, K/V packed or read from the paged cache
+ *
+ * Sources (web pages, by title and section):
+ *   [KVM]  "効率的な KV キャッシュ管理と Attention 計算" (itan.pw): "Triton カーネルによる
+ *          KV キャッシュ書き込み" (the write), "Python 層からのカーネル呼び出し" (its shape
+ *          and stride checks), "Attention モジュールの実装" (write first, then varlen
+ *          attention for prefill or paged attention for decode).
+ *   [PA]   "ページド・アテンション" (transformers docs): "Varlen パス" (cu_seq_lens,
+ *          max lengths) and "デコードパス" (block_table, cache_seqlens).
+ *   [CH15] "KV cache / batching / paged attention" (1s.xyz, chapter 15): FP8 KV
+ *          halves the cache ("KVキャッシュはどれくらいメモリを食う？"), GQA, PagedAttention,
+ *          prefix caching / chunked prefill, FlashAttention (tiling is exact).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *   where a comment says "host".  The library allocates no memory; scratch
+ *   space ("workspace") is passed in and sized by the matching *_workspace call.
+ * - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *   NULL = the legacy default stream).  No call synchronises the device or
+ *   reads device data on the host, so calls can be captured in a CUDA graph.
+ * - Head layout: q/k/v rows are [heads, head_dim] contiguous, head_dim innermost.
+ *   A cache is [num_blocks, block_size, num_kv_heads, head_dim] contiguous,
+ *   i.e. a flat array of num_slots = num_blocks*block_size rows of
+ *   num_kv_heads*head_dim elements; slot = block*block_size + offset.
+ * - GQA: query head h reads kv head h / (num_heads / num_kv_heads).
+ * - Supported: head_dim 64 or 128; num_heads a multiple of num_kv_heads with
+ *   num_heads/num_kv_heads <= 8 for decode; block_size a multiple of 16 for
+ *   the paged attention calls (any >= 1 for the write).
+ * - Return value: a pkv_status.  Host-visible argument problems return
+ *   PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED / PKV_ERR_WORKSPACE before any
+ *   launch; a failed launch returns PKV_ERR_CUDA.
+ * - Device metadata (slots, block ids, lengths) is never trusted blindly:
+ *   a slot >= num_slots, a block id outside [0, num_blocks) or a length that
+ *   does not fit the block table is skipped (never dereferenced) and, when
+ *   `err_flag` is non-NULL, sets bits of *err_flag (an int32 in device memory,
+ *   OR-ed atomically; PKV_DEVERR_* below).  Clear it before the call to read it.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride */
+  PKV_ERR_UNSUPPORTED = 2, /* dtype, head_dim, group size or block size not built */
+  PKV_ERR_WORKSPACE = 3,   /* workspace pointer NULL or smaller than required */
+  PKV_ERR_CUDA = 4         /* a kernel launch or a driver call failed */
+} pkv_status;
+
+typedef enum {
+  PKV_BF16 = 0,     /* bfloat16 */
+  PKV_FP8_E4M3 = 2  /* OCP FP8 E4M3 (cache only), per-tensor scale */
+} pkv_dtype;
+
+/* bits of *err_flag */
+#define PKV_DEVERR_SLOT 1        /* a slot_mapping entry >= num_slots (row skipped) */
+#define PKV_DEVERR_BLOCK 2       /* a block_table entry outside [0, num_blocks) was needed */
+#define PKV_DEVERR_LENGTH 4      /* a length is negative or needs more than max_blocks_per_seq blocks */
+#define PKV_DEVERR_TIMEOUT 8     /* a bounded wait inside a kernel gave up (the tile was abandoned) */
+
+/* Human-readable name of a pkv_status. */
+PKV_API const char* pkv_status_string(int status);
+
+/* Library ABI version (increases when a signature changes). */
+PKV_API int pkv_abi_version(void);
+
+/*
+ * KV-cache write ([KVM] "Triton カーネルによる KV キャッシュ書き込み"; checks from
+ * "Python 層からのカーネル呼び出し").
+ *
+ * For every token t in [0, num_tokens) with s = slot_mapping[t]:
+ *   k_cache row s := k row t,  v_cache row s := v row t   (a row is num_kv_heads*head_dim elements)
+ * s < 0 marks a padding token: nothing is written.  s >= num_slots is skipped
+ * and flagged (PKV_DEVERR_SLOT).  Two tokens with the same slot race (the
+ * caller must not pass duplicates).
+ *
+ * k, v:          bf16, token t's row starts at element t*k_row_stride (resp.
+ *                v_row_stride) and holds [num_kv_heads, head_dim] contiguous
+ *                elements; the row strides are free (K and V may be views of a
+ *                fused QKV projection) but must be multiples of 8 elements and
+ *                the pointers 16-byte aligned.
+ * k_cache, v_cache: [num_slots, num_kv_heads, head_dim] of cache_dtype, 16-byte aligned.
+ * cache_dtype:   PKV_BF16 (bits copied) or PKV_FP8_E4M3: each element is stored as
+ *                e4m3_rne_satfinite(float(x) * inv_scale), one fp32 multiply
+ *                and one round-to-nearest-even saturating conversion.
+ * k_inv_scale, v_inv_scale: 1/scale of each FP8 cache (ignored for PKV_BF16).
+ * num_kv_heads*head_dim must be a multiple of 8.
+ */
+PKV_API int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                       int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                       void* k_cache, void* v_cache, int32_t cache_dtype, int64_t num_slots,
+                       const int32_t* slot_mapping, float k_inv_scale, float v_inv_scale,
+                       int32_t* err_flag, void* stream);
+
+/*
+ * Workspace bytes pkv_paged_attn_decode needs for these sizes on the current
+ * device (0 is a valid answer).  max_seqlen_k is a host upper bound of
+ * cache_seqlens.  Returns 0 for invalid sizes as well; the call itself then
+ * reports the error.
+ */
+PKV_API size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t max_seqlen_k);
+
+/*
+ * Paged decode attention ([PA] "デコードパス"; [KVM] "Attention モジュールの実装",
+ * decode branch).  Each sequence b has one query token q[b] ([batch, num_heads,
+ * head_dim] bf16) and attends to its first cache_seqlens[b] cached positions
+ * (the count AFTER this step's token was written): position p of sequence b is
+ * slot block_table[b*max_blocks_per_seq + p/block_size]*block_size + p%block_size.
+ *
+ *   out[b,h,:] = sum_p softmax_p(scale * <q[b,h], k_p>) * v_p       (bf16, RNE)
+ *   lse[b,h]   = log sum_p exp(scale * <q[b,h], k_p>)               (fp32, natural log; nullable)
+ * with k_p, v_p taken from kv head h/(num_heads/num_kv_heads).  A sequence
+ * with cache_seqlens[b] == 0 outputs zeros and lse = -inf.
+ *
+ * cache_dtype PKV_BF16, or PKV_FP8_E4M3 where the cached code c stands for
+ * float(c)*k_scale (resp. v_scale).  Long sequences are split across CTAs and
+ * merged by log-sum-exp; workspace holds the partial results.
+ * max_seqlen_k: host upper bound of cache_seqlens (it sizes the split).
+ */
+PKV_API int pkv_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, int32_t cache_dtype,
+                          const int32_t* cache_seqlens, const int32_t* block_table,
+                          int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, int32_t max_seqlen_k, float scale, float k_scale,
+                          float v_scale, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,534 @@
+// Paged decode attention: split-KV kernel + log-sum-exp combine kernel.
+//
+// Source: "ページド・アテンション" (transformers docs), section "デコードパス": one
+// query token per sequence; its keys are the first cache_seqlens[b] positions,
+// found through row b of block_table (shape (batch, max_blocks_per_seq));
+// blocks need not be contiguous.  "効率的な KV キャッシュ管理と Attention 計算"
+// (itan.pw), "Attention モジュールの実装": the decode branch attends after the
+// new token was written.  "KV cache / batching / paged attention" (1s.xyz ch. 15),
+// "FlashAttention：注意計算そのものを速く": tiling with a running max and sum
+// gives exactly ordinary attention.
+//
+// Design (GB300):
+// * Grid (split, kv_head, seq).  A CTA owns one kv head of one sequence over a
+//   contiguous range of positions, and serves every query head of that GQA
+//   group, so each K/V page row is read from HBM once per group.
+// * 4 warps; each warp streams its own 16-token groups (positions
+//   16*(warp + 4*i)) through a private cp.async ring of shared-memory stages
+//   (16-byte copies, zero-filled beyond the sequence end, XOR-swizzled rows).
+// * Scores on tensor cores with the operands swapped: S^T[16 tok x 8 heads] =
+//   K[16 x D] * Q^T[D x 8] (mma.sync m16n8k16), so a group of up to 8 heads
+//   fills the N=8 side and no token row is padding.  P is transposed in
+//   registers (movmatrix) into the B operand of O^T[D x 8] += V^T * P^T.
+// * Online softmax in the log2 domain, fp32; masked positions get -inf
+//   (never multiply-by-zero, so stale or NaN cache rows cannot leak in).
+// * FP8 E4M3 cache: codes are widened to bf16 in registers with a bit move that
+//   is exact up to a 2^-120 factor (see pkv_device.cuh); k_scale * 2^120 is
+//   folded into the logit scale and v_scale * 2^120 into the output.
+// * Per-CTA partials (O/l, log2-sum-exp) go to the caller's workspace; a
+//   second kernel merges the splits of each (seq, head).  A sequence that fits
+//   one split is written directly by the split kernel.
+#include <cmath>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kDecWarps = 4;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kGroupTok = 16;       // positions per warp step
+constexpr int kMaxGroup = 8;        // query heads per kv head handled by one CTA
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kFp8Bias = 1.329227995784916e36f;  // 2^120
+
+struct DecodeParams {
+  const uint16_t* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* seqlens;
+  const int32_t* block_table;
+  int32_t max_blocks;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t split_tokens;
+  int32_t max_splits;
+  float scale_log2;
+  float v_mul;
+  uint16_t* out;
+  float* lse;
+  float* ws_o;
+  float* ws_lse;
+  int32_t* err;
+};
+
+// Attended length of sequence b, clamped to what the block table and the
+// workspace can hold (violations are flagged by the caller thread).
+__device__ __forceinline__ int attended_length(const DecodeParams& p, int b, bool report) {
+  int len = __ldg(p.seqlens + b);
+  const int64_t cap_bt = (int64_t)p.max_blocks * p.block_size;
+  const int64_t cap_ws = (int64_t)p.max_splits * p.split_tokens;
+  bool bad = false;
+  if (len < 0) { len = 0; bad = true; }
+  if ((int64_t)len > cap_bt) { len = (int)cap_bt; bad = true; }
+  if ((int64_t)len > cap_ws) { len = (int)cap_ws; bad = true; }
+  if (bad && report) flag_error(p.err, PKV_DEVERR_LENGTH);
+  return len;
+}
+
+template <int kChunks>
+__device__ __forceinline__ int swz(int row, int chunk) {
+  if constexpr (kChunks >= 8) {
+    return chunk ^ (row & 7);
+  } else {
+    return chunk ^ ((row >> 1) & 3);
+  }
+}
+
+template <int D, bool kFp8, int kStages>
+__global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(const DecodeParams p) {
+  constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one position, one kv head
+  constexpr int kChunks = kRowBytes / 16;
+  constexpr int kTileBytes = kGroupTok * kRowBytes;
+  constexpr int kWarpStageBytes = 2 * kTileBytes;
+  constexpr int kDT = D / 16;
+  constexpr int kItems = kGroupTok * kChunks / 32;  // 16-byte copies per lane per tensor
+  static_assert(kItems >= 1, "tile too small");
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+
+  const int len = attended_length(p, b, split == 0 && kvh == 0 && threadIdx.x == 0);
+  const int n_splits = (len + p.split_tokens - 1) / p.split_tokens;
+  if (split >= (n_splits > 0 ? n_splits : 1)) return;
+  const int t_begin = split * p.split_tokens;
+  const int t_end = min(t_begin + p.split_tokens, len);
+  const int n_groups = t_end > t_begin ? (t_end - t_begin + kGroupTok - 1) / kGroupTok : 0;
+  const int my_groups = n_groups > warp ? (n_groups - warp + kDecWarps - 1) / kDecWarps : 0;
+
+  const int64_t slot_bytes = (int64_t)p.num_kv_heads * kRowBytes;
+  const uint8_t* kbase = p.k_cache + (int64_t)kvh * kRowBytes;
+  const uint8_t* vbase = p.v_cache + (int64_t)kvh * kRowBytes;
+  const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
+  uint8_t* wsm = smem + warp * kStages * kWarpStageBytes;
+
+  // ---- Q as the B operand (n = head lane/4 of this group, k = head dim) ----
+  uint32_t qf[kDT][2];
+  {
+    const int h = lane >> 2;
+    const int j = lane & 3;
+    const bool hv = h < p.group;
+    const uint16_t* qrow = p.q + ((int64_t)b * p.num_heads + (int64_t)kvh * p.group + (hv ? h : 0)) * D;
+#pragma unroll
+    for (int kk = 0; kk < kDT; ++kk) {
+      if constexpr (!kFp8) {
+        qf[kk][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * j) : 0u;
+        qf[kk][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * j) : 0u;
+      } else {
+        // FP8 K fragments carry head dims 4j..4j+3 of each 16-wide slice in
+        // k-slots {2j,2j+1,2j+8,2j+9}; Q uses the same permutation.
+        const uint2 w = hv ? *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * j) : make_uint2(0u, 0u);
+        qf[kk][0] = w.x;
+        qf[kk][1] = w.y;
+      }
+    }
+  }
+
+  auto block_of = [&](int pos0, bool report) -> int {
+    const int blk = __ldg(bt + pos0 / p.block_size);
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (report) flag_error(p.err, PKV_DEVERR_BLOCK);
+      return -1;
+    }
+    return blk;
+  };
+
+  auto issue = [&](int i) {
+    if (i < my_groups) {
+      const int g = warp + i * kDecWarps;
+      const int pos0 = t_begin + g * kGroupTok;
+      const int blk = block_of(pos0, lane == 0);
+      const int64_t slot0 = (int64_t)blk * p.block_size + pos0 % p.block_size;
+      uint8_t* st = wsm + (i % kStages) * kWarpStageBytes;
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {
+        const int item = lane + 32 * u;
+        const int row = item / kChunks;
+        const int ch = item % kChunks;
+        const bool valid = blk >= 0 && pos0 + row < t_end;
+        const int64_t off = valid ? (slot0 + row) * slot_bytes + ch * 16 : 0;
+        const uint32_t dst = smem_u32(st + row * kRowBytes + swz<kChunks>(row, ch) * 16);
+        cp_async_16(dst, kbase + off, valid ? 16u : 0u);
+        cp_async_16(dst + kTileBytes, vbase + off, valid ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float o[kDT][4];
+#pragma unroll
+  for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) issue(i);
+
+  for (int i = 0; i < my_groups; ++i) {
+    cp_async_wait<kStages - 2>();
+    __syncwarp();
+    const int g = warp + i * kDecWarps;
+    const int pos0 = t_begin + g * kGroupTok;
+    const bool blk_ok = block_of(pos0, false) >= 0;
+    const uint8_t* st = wsm + (i % kStages) * kWarpStageBytes;
+    const uint32_t ks = smem_u32(st);
+    const uint32_t vs = ks + kTileBytes;
+
+    // ---- S^T = K Q^T (16 positions x 8 heads) ----
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int csel = lane >> 4;
+      if constexpr (!kFp8) {
+#pragma unroll
+        for (int kk = 0; kk < kDT; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(ks + row * kRowBytes + swz<kChunks>(row, 2 * kk + csel) * 16, a0, a1, a2, a3);
+          mma_bf16_16816(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        }
+      } else {
+#pragma unroll
+        for (int pp = 0; pp < kDT / 2; ++pp) {
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4(ks + row * kRowBytes + swz<kChunks>(row, 2 * pp + csel) * 16, r0, r1, r2, r3);
+          const uint32_t lo0 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x1404u));
+          const uint32_t hi0 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x3424u));
+          const uint32_t lo1 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x1404u));
+          const uint32_t hi1 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x3424u));
+          mma_bf16_16816(s, lo0, lo1, hi0, hi1, qf[2 * pp][0], qf[2 * pp][1]);
+          const uint32_t lo2 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x1404u));
+          const uint32_t hi2 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x3424u));
+          const uint32_t lo3 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x1404u));
+          const uint32_t hi3 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x3424u));
+          mma_bf16_16816(s, lo2, lo3, hi2, hi3, qf[2 * pp + 1][0], qf[2 * pp + 1][1]);
+        }
+      }
+    }
+
+    // ---- online softmax (log2 domain); this thread: positions lane/4 (+8), heads 2j, 2j+1 ----
+    const int tok0 = pos0 + (lane >> 2);
+    const bool v0 = blk_ok && tok0 < t_end;
+    const bool v1 = blk_ok && tok0 + 8 < t_end;
+    const float x0 = v0 ? s[0] * p.scale_log2 : -INFINITY;
+    const float x1 = v0 ? s[1] * p.scale_log2 : -INFINITY;
+    const float x2 = v1 ? s[2] * p.scale_log2 : -INFINITY;
+    const float x3 = v1 ? s[3] * p.scale_log2 : -INFINITY;
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const bool live0 = mn0 != -INFINITY, live1 = mn1 != -INFINITY;
+    const float al0 = live0 ? fast_exp2(m0 - mn0) : 1.f;
+    const float al1 = live1 ? fast_exp2(m1 - mn1) : 1.f;
+    const float p0 = live0 ? fast_exp2(x0 - mn0) : 0.f;
+    const float p1 = live1 ? fast_exp2(x1 - mn1) : 0.f;
+    const float p2 = live0 ? fast_exp2(x2 - mn0) : 0.f;
+    const float p3 = live1 ? fast_exp2(x3 - mn1) : 0.f;
+    m0 = mn0;
+    m1 = mn1;
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+#pragma unroll
+    for (int t = 0; t < kDT; ++t) {
+      o[t][0] *= al0;
+      o[t][1] *= al1;
+      o[t][2] *= al0;
+      o[t][3] *= al1;
+    }
+    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // positions 0..7 as B (k = pos, n = head)
+    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // positions 8..15
+
+    // ---- O^T += V^T P^T ----
+    {
+      const int row = (lane & 7) + (lane >> 4) * 8;
+      const int csel = (lane >> 3) & 1;
+      if constexpr (!kFp8) {
+#pragma unroll
+        for (int t = 0; t < kDT; ++t) {
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4_trans(vs + row * kRowBytes + swz<kChunks>(row, 2 * t + csel) * 16, a0, a1, a2, a3);
+          mma_bf16_16816(o[t], a0, a1, a2, a3, pb0, pb1);
+        }
+      } else {
+#pragma unroll
+        for (int pp = 0; pp < kDT / 2; ++pp) {
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4_trans(vs + row * kRowBytes + swz<kChunks>(row, 2 * pp + csel) * 16, r0, r1, r2, r3);
+          // r: bytes (pos 2j, dim 2u), (2j, 2u+1), (2j+1, 2u), (2j+1, 2u+1); split even / odd dims
+          mma_bf16_16816(o[2 * pp], e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x2404u)),
+                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x2404u)),
+                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x2404u)),
+                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x2404u)), pb0, pb1);
+          mma_bf16_16816(o[2 * pp + 1], e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x3414u)),
+                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x3414u)),
+                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x3414u)),
+                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x3414u)), pb0, pb1);
+        }
+      }
+    }
+    __syncwarp();
+    issue(i + kStages - 1);
+  }
+
+  // ---- merge the four warps of the CTA ----
+  cp_async_wait<0>();
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  __syncthreads();
+  float* m_s = reinterpret_cast<float*>(smem);           // [warps][8]
+  float* l_s = m_s + kDecWarps * kMaxGroup;               // [warps][8]
+  float* o_s = l_s + kDecWarps * kMaxGroup;               // [warps][8][D]
+  {
+    const int j = lane & 3;
+    if (lane < 4) {
+      m_s[warp * kMaxGroup + 2 * j] = m0;
+      m_s[warp * kMaxGroup + 2 * j + 1] = m1;
+      l_s[warp * kMaxGroup + 2 * j] = l0;
+      l_s[warp * kMaxGroup + 2 * j + 1] = l1;
+    }
+    float* ow = o_s + warp * kMaxGroup * D;
+    const int r = lane >> 2;
+#pragma unroll
+    for (int t = 0; t < kDT; ++t) {
+      int d0, d1;
+      if constexpr (!kFp8) {
+        d0 = 16 * t + r;
+        d1 = d0 + 8;
+      } else {
+        d0 = 32 * (t >> 1) + 2 * r + (t & 1);
+        d1 = d0 + 16;
+      }
+      ow[(2 * j) * D + d0] = o[t][0];
+      ow[(2 * j + 1) * D + d0] = o[t][1];
+      ow[(2 * j) * D + d1] = o[t][2];
+      ow[(2 * j + 1) * D + d1] = o[t][3];
+    }
+  }
+  __syncthreads();
+  const bool single = n_splits <= 1;
+  for (int idx = threadIdx.x; idx < p.group * D; idx += kDecThreads) {
+    const int h = idx / D;
+    const int d = idx % D;
+    float ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) ms = fmaxf(ms, m_s[w * kMaxGroup + h]);
+    float L = 0.f, acc = 0.f;
+    if (ms != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = m_s[w * kMaxGroup + h];
+        const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - ms);
+        L += l_s[w * kMaxGroup + h] * f;
+        acc += o_s[(w * kMaxGroup + h) * D + d] * f;
+      }
+    }
+    const bool any = L > 0.f;
+    const float val = any ? acc * p.v_mul / L : 0.f;
+    const float lse2 = any ? ms + log2f(L) : -INFINITY;
+    const int64_t bh = (int64_t)b * p.num_heads + (int64_t)kvh * p.group + h;
+    if (single) {
+      p.out[bh * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+      if (p.lse != nullptr && d == 0) p.lse[bh] = any ? lse2 * kLn2 : -INFINITY;
+    } else {
+      p.ws_o[(bh * p.max_splits + split) * D + d] = val;
+      if (d == 0) p.ws_lse[bh * p.max_splits + split] = lse2;
+    }
+  }
+}
+
+// One warp per (sequence, query head): merge the splits by log-sum-exp.
+template <int D>
+__global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p, int batch) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t bh = (int64_t)blockIdx.x * 4 + warp;
+  if (bh >= (int64_t)batch * p.num_heads) return;
+  const int b = (int)(bh / p.num_heads);
+  const int len = attended_length(p, b, false);
+  const int n = (len + p.split_tokens - 1) / p.split_tokens;
+  if (n <= 1) return;
+  const float* ls = p.ws_lse + bh * p.max_splits;
+  float mx = -INFINITY;
+  for (int s = lane; s < n; s += 32) mx = fmaxf(mx, ls[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float sum = 0.f;
+  if (mx != -INFINITY)
+    for (int s = lane; s < n; s += 32) sum += fast_exp2(ls[s] - mx);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const bool any = mx != -INFINITY && sum > 0.f;
+  const float lse2 = any ? mx + log2f(sum) : -INFINITY;
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  if (any) {
+    const float* os = p.ws_o + bh * p.max_splits * D + lane * kPer;
+    for (int s = 0; s < n; ++s) {
+      const float w = fast_exp2(ls[s] - lse2);
+      if constexpr (kPer == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(os + (int64_t)s * D);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(os + (int64_t)s * D);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+  }
+  uint16_t* orow = p.out + bh * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) orow[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
+  if (p.lse != nullptr && lane == 0) p.lse[bh] = any ? lse2 * kLn2 : -INFINITY;
+}
+
+struct SplitPlan {
+  int split_tokens;
+  int max_splits;
+  size_t workspace;
+};
+
+// Positions per CTA: enough CTAs to fill the GPU several times over at the
+// longest sequence, in multiples of 64 positions (4 warps x 16), at least 512.
+SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seqlen_k) {
+  SplitPlan pl{64, 1, 0};
+  if (batch <= 0 || max_seqlen_k <= 0) return pl;
+  const int64_t units = (int64_t)batch * num_kv_heads;
+  const int64_t target = (int64_t)device_sm_count() * 2 * 16;
+  int64_t c = ((int64_t)max_seqlen_k * units + target - 1) / target;
+  c = ((c + 63) / 64) * 64;
+  if (c < 512) c = 512;
+  const int64_t whole = ((int64_t)max_seqlen_k + 63) / 64 * 64;
+  if (c > whole) c = whole;
+  pl.split_tokens = (int)c;
+  pl.max_splits = (int)((max_seqlen_k + c - 1) / c);
+  if (pl.max_splits > 1) {
+    const size_t rows = (size_t)batch * num_heads * pl.max_splits;
+    pl.workspace = rows * head_dim * sizeof(float) + ((rows * sizeof(float) + 255) / 256) * 256;
+  }
+  return pl;
+}
+
+template <int D, bool kFp8>
+int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, cudaStream_t st) {
+  constexpr int kStages = kFp8 ? 6 : 3;
+  constexpr int kRowBytes = D * (kFp8 ? 1 : 2);
+  constexpr int kSmemPipe = kDecWarps * kStages * 2 * kGroupTok * kRowBytes;
+  constexpr int kSmemMerge = (2 * kDecWarps * kMaxGroup + kDecWarps * kMaxGroup * D) * (int)sizeof(float);
+  constexpr int kSmem = kSmemPipe > kSmemMerge ? kSmemPipe : kSmemMerge;
+  auto kern = paged_decode_split_kernel<D, kFp8, kStages>;
+  static bool attr_set[64] = {false};  // per instantiation and device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= 64) dev = 63;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  dim3 grid(pl.max_splits, p.num_kv_heads, batch);
+  kern<<<grid, kDecThreads, kSmem, st>>>(p);
+  if (pl.max_splits > 1) {
+    const int64_t rows = (int64_t)batch * p.num_heads;
+    paged_decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p, batch);
+  }
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                                  int32_t head_dim, int32_t max_seqlen_k) {
+  if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seqlen_k <= 0) return 0;
+  return pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k).workspace;
+}
+
+extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, int32_t cache_dtype,
+                                     const int32_t* cache_seqlens, const int32_t* block_table,
+                                     int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                     int32_t num_blocks, int32_t max_seqlen_k, float scale, float k_scale,
+                                     float v_scale, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  using namespace pkv;
+  if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+      max_seqlen_k < 0 || block_size <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (num_heads / num_kv_heads > kMaxGroup) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (cache_dtype == PKV_FP8_E4M3 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
+                                      !std::isfinite(v_scale)))
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !cache_seqlens || !block_table || !out) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(q) & 7u) ||
+      (reinterpret_cast<uintptr_t>(out) & 7u))
+    return PKV_ERR_INVALID_ARG;
+  const int mlen = max_seqlen_k > 0 ? max_seqlen_k : 1;
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, mlen);
+  if (pl.workspace > 0 && (workspace == nullptr || workspace_bytes < pl.workspace ||
+                           (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return PKV_ERR_WORKSPACE;
+
+  DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.seqlens = cache_seqlens;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.split_tokens = pl.split_tokens;
+  p.max_splits = pl.max_splits;
+  const bool fp8 = cache_dtype == PKV_FP8_E4M3;
+  p.scale_log2 = scale * kLog2e * (fp8 ? k_scale * kFp8Bias : 1.f);
+  p.v_mul = fp8 ? v_scale * kFp8Bias : 1.f;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  if (pl.max_splits > 1) {
+    const size_t rows = (size_t)batch * num_heads * pl.max_splits;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + rows * head_dim * sizeof(float));
+  }
+  p.err = err_flag;
+  cudaStream_t st = as_stream(stream);
+  if (head_dim == 128) return fp8 ? launch_decode<128, true>(p, batch, pl, st) : launch_decode<128, false>(p, batch, pl, st);
+  return fp8 ? launch_decode<64, true>(p, batch, pl, st) : launch_decode<64, false>(p, batch, pl, st);
+}

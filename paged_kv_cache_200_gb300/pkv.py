@@ -1,0 +1,210 @@
+"""Thin ctypes binding of ``libpkv.so`` (declared in ``include/pkv.h``).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  Torch tensors supply device pointers, the current CUDA stream and
+workspace memory.  There is no CPU fallback: if the library is missing the
+first call raises.
+
+Functions mirror the C entry points:
+
+* ``kv_cache_write(k, v, k_cache, v_cache, slot_mapping, ...)``
+* ``paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale, ...)``
+* ``paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q, max_len_k, ...)``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpkv.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "pkv.h")
+
+PKV_BF16 = 0
+PKV_FP8_E4M3 = 2
+
+DEVERR_SLOT = 1
+DEVERR_BLOCK = 2
+DEVERR_LENGTH = 4
+DEVERR_TIMEOUT = 8
+
+_c_void_p = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_abi_version": (ctypes.c_int, []),
+    "pkv_kv_cache_write": (ctypes.c_int, [
+        _c_void_p, _i64, _c_void_p, _i64, _i32, _i32, _i32, _c_void_p, _c_void_p, _i32, _i64,
+        _c_void_p, _f32, _f32, _c_void_p, _c_void_p]),
+    "pkv_paged_attn_decode_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "pkv_paged_attn_decode": (ctypes.c_int, [
+        _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
+        _i32, _i32, _i32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "pkv_paged_attn_varlen_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pkv_paged_attn_varlen": (ctypes.c_int, [
+        _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
+        _c_void_p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _f32, _f32, _c_void_p, _c_void_p,
+        _c_void_p, _sz, _c_void_p, _c_void_p]),
+}
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    """A libpkv call returned a non-zero status."""
+
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions ``include/pkv.h`` declares."""
+    with open(header) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", text)))
+
+
+def lib(path: str = LIB_PATH):
+    """Load the library (once) and declare argument types."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with paged_kv_cache_200_gb300.build.build()")
+        handle = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            if hasattr(handle, name):
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise PkvError(status, lib().pkv_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cache_dtype(cache: torch.Tensor) -> int:
+    if cache.dtype == torch.bfloat16:
+        return PKV_BF16
+    if cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        return PKV_FP8_E4M3
+    raise TypeError(f"unsupported cache dtype {cache.dtype}")
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+
+
+_workspaces = {}
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A cached per-device scratch buffer of at least ``nbytes`` (grows, never shrinks)."""
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+        _workspaces[key] = buf
+    return buf
+
+
+# ---------------------------------------------------------------------------
+# KV-cache write
+# ---------------------------------------------------------------------------
+
+
+def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, k_inv_scale: float = 1.0, v_inv_scale: float = 1.0,
+                   err_flag=None, stream=None):
+    """Scatter each token's K/V row into the caches at ``slot_mapping[t]`` (negative = skip).
+
+    ``k``, ``v``: ``[T, Hkv, D]`` bf16 with the inner two dims contiguous (any
+    row stride).  Caches: ``[..., Hkv, D]`` contiguous, bf16 or uint8 E4M3
+    codes; FP8 stores ``e4m3(x * inv_scale)``.
+    """
+    _require_cuda(k, v, k_cache, v_cache, slot_mapping)
+    T, Hkv, D = k.shape
+    if v.shape != k.shape or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("k and v must be bf16 tensors of the same shape [T, Hkv, D]")
+    if k.stride(-1) != 1 or v.stride(-1) != 1 or k.stride(1) != D or v.stride(1) != D:
+        raise ValueError("k/v inner dims [Hkv, D] must be contiguous")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    if k_cache.shape[-2:] != (Hkv, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must end in [Hkv, D] and match each other")
+    if slot_mapping.dtype != torch.int32 or slot_mapping.numel() != T:
+        raise ValueError("slot_mapping must be int32 with one entry per token")
+    num_slots = k_cache.numel() // (Hkv * D)
+    st = lib().pkv_kv_cache_write(_ptr(k), k.stride(0), _ptr(v), v.stride(0), T, Hkv, D, _ptr(k_cache),
+                                  _ptr(v_cache), _cache_dtype(k_cache), num_slots, _ptr(slot_mapping),
+                                  float(k_inv_scale), float(v_inv_scale), _ptr(err_flag), _stream(stream))
+    _check(st)
+
+
+# ---------------------------------------------------------------------------
+# paged decode attention
+# ---------------------------------------------------------------------------
+
+
+def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale: float, max_seqlen_k: int = None,
+                      k_scale: float = 1.0, v_scale: float = 1.0, out=None, lse=None, return_lse=False,
+                      err_flag=None, workspace_buf=None, stream=None):
+    """Decode attention over a paged cache; returns ``out [B, Hq, D]`` (and ``lse [B, Hq]``).
+
+    ``k_cache``/``v_cache``: ``[num_blocks, block_size, Hkv, D]``.
+    ``cache_seqlens``: int32 ``[B]`` tokens to attend; ``block_table``: int32
+    ``[B, max_blocks_per_seq]``.  ``max_seqlen_k`` is a host upper bound of the
+    lengths (default: the block table's capacity; no device sync is made).
+    """
+    _require_cuda(q, k_cache, v_cache, cache_seqlens, block_table)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bf16 [B, Hq, D]")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.is_contiguous()):
+        raise ValueError("caches and block_table must be contiguous")
+    if cache_seqlens.dtype != torch.int32 or block_table.dtype != torch.int32:
+        raise ValueError("cache_seqlens and block_table must be int32")
+    MB = block_table.shape[1]
+    if max_seqlen_k is None:
+        max_seqlen_k = MB * bs
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    L = lib()
+    need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
+    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device) if need else None)
+    st = L.pkv_paged_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _cache_dtype(k_cache),
+                                 _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB,
+                                 int(max_seqlen_k), float(scale), float(k_scale), float(v_scale), _ptr(out),
+                                 _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(err_flag),
+                                 _stream(stream))
+    _check(st)
+    return (out, lse) if (return_lse or lse is not None) else out

@@ -1,0 +1,55 @@
+"""The C-ABI library builds, loads, and exports every function include/pkv.h declares.
+
+No kernel runs here: only calls that the library rejects on the host before
+touching the GPU are made.
+"""
+
+import ctypes
+import shutil
+
+import pytest
+
+from _helpers import built_library
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not __import__("os").path.exists(
+    "/usr/local/cuda/bin/nvcc"), reason="nvcc not available")
+
+
+def test_every_declared_symbol_is_exported():
+    pkv = built_library()
+    names = pkv.declared_functions()
+    assert "pkv_kv_cache_write" in names and "pkv_paged_attn_decode" in names
+    lib = pkv.lib()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding declares a signature for every exported entry point
+    assert set(names) <= set(pkv._SIGNATURES), set(names) - set(pkv._SIGNATURES)
+
+
+def test_status_strings_and_version():
+    pkv = built_library()
+    lib = pkv.lib()
+    assert lib.pkv_abi_version() >= 1
+    for code in range(5):
+        assert lib.pkv_status_string(code).startswith(b"PKV_")
+
+
+def test_host_side_argument_validation():
+    pkv = built_library()
+    lib = pkv.lib()
+    nul = ctypes.c_void_p(0)
+    # negative token count / bad head dims are rejected before any launch
+    assert lib.pkv_kv_cache_write(nul, 128, nul, 128, -1, 1, 128, nul, nul, 0, 16, nul, 1.0, 1.0, nul, nul) == 1
+    assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 4, 1, 128, nul, nul, 7, 16, nul, 1.0, 1.0, nul, nul) == 2
+    assert lib.pkv_kv_cache_write(nul, 12, nul, 12, 4, 1, 12, nul, nul, 0, 16, nul, 1.0, 1.0, nul, nul) == 2
+    # zero tokens: nothing to do
+    assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 0, 1, 128, nul, nul, 0, 16, nul, 1.0, 1.0, nul, nul) == 0
+    # null pointers with work to do
+    assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 4, 1, 128, nul, nul, 0, 16, nul, 1.0, 1.0, nul, nul) == 1
+    # decode: head_dim 96 unsupported, group of 16 unsupported, block size 8 unsupported
+    args = lambda H, Hkv, D, bs: (nul, nul, nul, 0, nul, nul, 4, 1, H, Hkv, D, bs, 8, 64, 0.1, 1.0, 1.0,
+                                  nul, nul, nul, 0, nul, nul)
+    assert lib.pkv_paged_attn_decode(*args(8, 2, 96, 16)) == 2
+    assert lib.pkv_paged_attn_decode(*args(32, 2, 128, 16)) == 2
+    assert lib.pkv_paged_attn_decode(*args(8, 2, 128, 8)) == 2
+    assert lib.pkv_paged_attn_decode(*args(8, 3, 128, 16)) == 1
