@@ -264,18 +264,17 @@ def sampled_oracle_decode(wl, seqs):
     return O, q, kc, vc, lens, tsub
 
 
-def oracle_decode_rate(wl, budget_s, max_seqs=64, truncate=None):
-    """Oracle throughput (algorithmic bytes/s) on whole (or truncated) sampled sequences."""
-    order = list(np.random.default_rng(0).permutation(wl.batch))[:max_seqs]
-    O, q, kc, vc, lens, tsub = sampled_oracle_decode(wl, order[:max(1, min(len(order), 8))])
+def oracle_decode_rate(wl, budget_s, max_seqs=64):
+    """Oracle throughput (algorithmic bytes/s): whole sampled sequences, cycled until the budget is spent."""
+    order = [int(s) for s in np.random.default_rng(0).permutation(wl.batch)[:max_seqs]]
+    O, q, kc, vc, lens, tsub = sampled_oracle_decode(wl, order)
     elt = 1 if wl.cache_dtype == "fp8_e4m3" else 2
     done_bytes, done_tok, nseq = 0, 0, 0
     t0 = time.perf_counter()
-    for s in order[:8]:
-        L = int(lens[s]) if truncate is None else min(int(lens[s]), truncate)
-        l2 = lens.copy()
-        l2[s] = L
-        O.paged_attn_decode(q, kc, vc, l2, tsub, wl.block_size, wl.scale, wl.cache_dtype, wl.k_scale,
+    while True:
+        s = order[nseq % len(order)]
+        L = int(lens[s])
+        O.paged_attn_decode(q, kc, vc, lens, tsub, wl.block_size, wl.scale, wl.cache_dtype, wl.k_scale,
                             wl.v_scale, seqs=[s])
         done_bytes += L * wl.num_kv_heads * wl.head_dim * elt * 2 + 2 * wl.num_heads * wl.head_dim * 2
         done_tok += L
@@ -312,8 +311,8 @@ def run_pkv(args, rank, world, device):
     if rank == 0 and not args.no_cpu_baseline:
         rate, nseq, ntok, dt = oracle_decode_rate(wl, budget_s=args.cpu_budget)
         cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nseq} whole sequences of the decode batch ({ntok} cached tokens, all 32 heads), "
-                         f"fp64 NumPy, single thread, {dt:.1f} s"}
+               "sample": f"{nseq} whole-sequence decodes drawn from the decode batch ({ntok} cached tokens, "
+                         f"all 32 heads), fp64 NumPy, single thread, {dt:.1f} s"}
 
     clocks = ClockSampler(device)
     if world > 1:
@@ -459,6 +458,25 @@ def run_reference(args):
     }
 
 
+def ncu_case(args):
+    """A small case for ncu captures: a few write+decode steps, no timing, no JSON."""
+    from paged_kv_cache_200_gb300 import build as B
+    from paged_kv_cache_200_gb300 import pkv
+    from paged_kv_cache_200_gb300 import workloads as W
+    B.build()
+    rng = np.random.default_rng(77)
+    dt = "fp8_e4m3" if args.ncu_case == "decode_fp8" else "bf16"
+    # 64 sequences of 1K..4K cached tokens: ~0.65 GB of bf16 K/V, larger than L2
+    wl = W.make_decode(rng.integers(1024, 4096, 64, endpoint=True), 32, 8, 128, 16, seed=77, device="cuda",
+                       cache_dtype=dt)
+    step = DecodeStep(pkv, wl)
+    for _ in range(4):
+        step.write()
+        step.decode()
+    torch.cuda.synchronize()
+    log("ncu case done:", args.ncu_case, "decode bytes", decode_bytes(wl))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -469,7 +487,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8"], default=None,
+                    help="run a small case for an ncu capture and exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        ncu_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
 
