@@ -147,6 +147,40 @@ PKV_API int pkv_paged_attn_decode(const void* q, const void* k_cache, const void
                           float v_scale, void* out, float* lse, void* workspace,
                           size_t workspace_bytes, int32_t* err_flag, void* stream);
 
+/*
+ * Paged decode attention without a caller workspace (no counterpart on the
+ * source pages; an addition of this library).
+ *
+ * Some callers cannot allocate device memory: a plugin hosted by an engine
+ * that has already reserved all of the device's memory for its own pool, or a
+ * latency-critical loop where cudaMalloc's implicit device synchronisation is
+ * not allowed.  They cannot supply the workspace pkv_paged_attn_decode needs.
+ * This entry point computes the same result as pkv_paged_attn_decode (same
+ * arguments, same kernels, same status codes) but keeps the split-KV partials
+ * in a fixed 32 MiB array that the library declares in device memory; it
+ * allocates nothing itself.
+ *
+ * - Limit: requests whose pkv_paged_attn_decode_workspace(...) exceeds
+ *   pkv_paged_attn_decode_noalloc_max_scratch() (32 MiB) are rejected with
+ *   PKV_ERR_WORKSPACE before any launch.
+ * - Every GPU that loads the library holds the 32 MiB array until the process exits.
+ * - The first call on each device looks up the array's device address once
+ *   (with that device current); make that first call before any stream capture.
+ * - All calls share the array.  Nothing in it must start at zero, but calls that
+ *   overlap on the GPU (e.g. on two streams) race on it and corrupt each other.
+ * The caller still passes inputs and outputs (q, caches, metadata, out, lse).
+ */
+PKV_API int pkv_paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                          int32_t cache_dtype, const int32_t* cache_seqlens,
+                                          const int32_t* block_table, int32_t max_blocks_per_seq,
+                                          int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                          int32_t max_seqlen_k, float scale, float k_scale, float v_scale,
+                                          void* out, float* lse, int32_t* err_flag, void* stream);
+
+/* Bytes of the fixed scratch array pkv_paged_attn_decode_noalloc uses (its size limit). */
+PKV_API size_t pkv_paged_attn_decode_noalloc_max_scratch(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -532,3 +532,62 @@ extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const v
   if (head_dim == 128) return fp8 ? launch_decode<128, true>(p, batch, pl, st) : launch_decode<128, false>(p, batch, pl, st);
   return fp8 ? launch_decode<64, true>(p, batch, pl, st) : launch_decode<64, false>(p, batch, pl, st);
 }
+
+// ---------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory.
+//
+// The split-KV partials live in one file-scope device array of fixed size
+// instead of a caller workspace.  Every GPU that loads this library holds the
+// array until the process exits.  Its device address is looked up once per
+// device (cudaGetSymbolAddress, with that device current) by the first call
+// made on that device; make that first call before any stream capture.
+// Every call shares the array and finds the previous call's partials in it;
+// nothing in it needs to start at zero (each call writes every partial it
+// reads), but two calls that overlap on the GPU, on different streams,
+// overwrite each other's partials.
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+static constexpr size_t kPkvFixedScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char pkv_decode_fixed_scratch[kPkvFixedScratchBytes];
+
+namespace {
+
+std::mutex g_fixed_scratch_mu;
+void* g_fixed_scratch_addr[64] = {nullptr};
+
+int fixed_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
+  if (g_fixed_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, pkv_decode_fixed_scratch) != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
+    g_fixed_scratch_addr[dev] = p;
+  }
+  *out = g_fixed_scratch_addr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" size_t pkv_paged_attn_decode_noalloc_max_scratch(void) { return kPkvFixedScratchBytes; }
+
+extern "C" int pkv_paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                             int32_t cache_dtype, const int32_t* cache_seqlens,
+                                             const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch,
+                                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                             int32_t block_size, int32_t num_blocks, int32_t max_seqlen_k,
+                                             float scale, float k_scale, float v_scale, void* out, float* lse,
+                                             int32_t* err_flag, void* stream) {
+  const size_t need = pkv_paged_attn_decode_workspace(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k);
+  if (need > kPkvFixedScratchBytes) return PKV_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int st = fixed_scratch_address(&scratch);
+  if (st != PKV_OK) return st;
+  return pkv_paged_attn_decode(q, k_cache, v_cache, cache_dtype, cache_seqlens, block_table, max_blocks_per_seq,
+                               batch, num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_seqlen_k, scale,
+                               k_scale, v_scale, out, lse, scratch, kPkvFixedScratchBytes, err_flag, stream);
+}

@@ -48,6 +48,10 @@ _SIGNATURES = {
     "pkv_paged_attn_decode": (ctypes.c_int, [
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
         _i32, _i32, _i32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "pkv_paged_attn_decode_noalloc": (ctypes.c_int, [
+        _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
+        _i32, _i32, _i32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "pkv_paged_attn_decode_noalloc_max_scratch": (_sz, []),
     "pkv_paged_attn_varlen_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pkv_paged_attn_varlen": (ctypes.c_int, [
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
@@ -208,3 +212,29 @@ def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale: fl
                                  _stream(stream))
     _check(st)
     return (out, lse) if (return_lse or lse is not None) else out
+
+
+def paged_attn_decode_noalloc(q, k_cache, v_cache, cache_seqlens, block_table, scale: float,
+                              max_seqlen_k: int = None, k_scale: float = 1.0, v_scale: float = 1.0, out=None,
+                              lse=None, err_flag=None, stream=None):
+    """``paged_attn_decode`` for callers that cannot allocate: partials go to the library's fixed scratch.
+
+    Same arguments and result as ``paged_attn_decode`` (``out`` must be given by
+    callers that must not allocate; ``lse`` is optional).  Raises ``PkvError``
+    (PKV_ERR_WORKSPACE) when the request needs more scratch than the fixed 32 MiB.
+    Calls that overlap on the GPU share the scratch and must not be issued.
+    """
+    _require_cuda(q, k_cache, v_cache, cache_seqlens, block_table)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    MB = block_table.shape[1]
+    if max_seqlen_k is None:
+        max_seqlen_k = MB * bs
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    st = lib().pkv_paged_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _cache_dtype(k_cache),
+                                             _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB,
+                                             int(max_seqlen_k), float(scale), float(k_scale), float(v_scale),
+                                             _ptr(out), _ptr(lse), _ptr(err_flag), _stream(stream))
+    _check(st)
+    return out

@@ -1,0 +1,69 @@
+"""The decode entry point that allocates nothing, against the workspace entry point.
+
+For callers that cannot allocate device memory (an engine that owns all of
+it, or a loop that must not synchronise on cudaMalloc), the library offers a
+decode call whose split-KV partials live in a fixed device array.  These
+tests call it directly through the C ABI and compare it with the regular
+entry point on consecutive calls, and check that a request too large for the
+fixed array is refused before anything runs.  This file is collected last.
+"""
+
+import ctypes
+
+import pytest
+import torch
+
+from paged_kv_cache_200_gb300 import workloads as W
+from _helpers import BF16_ATOL, BF16_RTOL, FP8_ATOL, FP8_RTOL, assert_close, built_library, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _c_noalloc(lib, wl, out, lse):
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    kc, vc = wl.k_cache.view(shape4), wl.v_cache.view(shape4)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    return lib.pkv_paged_attn_decode_noalloc(
+        p(wl.q), p(kc), p(vc), 2 if wl.cache_dtype == "fp8_e4m3" else 0, p(wl.cache_seqlens), p(wl.block_table),
+        wl.block_table.shape[1], wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+        wl.num_blocks, wl.max_seqlen, wl.scale, wl.k_scale, wl.v_scale, p(out), p(lse), None,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
+    pkv = built_library()
+    lib = pkv.lib()
+    cases = [
+        W.make_decode([3000, 17, 9000, 512], 32, 8, 128, 16, seed=101, device="cuda"),            # several splits
+        W.make_decode([40, 2500, 700], 16, 4, 64, 32, seed=102, device="cuda", cache_dtype="fp8_e4m3"),
+        W.make_decode([3000, 17, 9000, 512], 32, 8, 128, 16, seed=101, device="cuda"),            # again
+    ]
+    for wl in cases:
+        shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+        ref, ref_lse = pkv.paged_attn_decode(wl.q, wl.k_cache.view(shape4), wl.v_cache.view(shape4),
+                                             wl.cache_seqlens, wl.block_table, wl.scale,
+                                             max_seqlen_k=wl.max_seqlen, k_scale=wl.k_scale, v_scale=wl.v_scale,
+                                             return_lse=True)
+        out = torch.full_like(ref, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        assert _c_noalloc(lib, wl, out, lse) == 0
+        torch.cuda.synchronize()
+        atol, rtol = (FP8_ATOL, FP8_RTOL) if wl.cache_dtype == "fp8_e4m3" else (BF16_ATOL, BF16_RTOL)
+        assert_close(f64(out), f64(ref), atol, rtol, "noalloc out")
+        assert_close(f64(lse), f64(ref_lse), 1e-3, 1e-3, "noalloc lse")
+
+
+def test_noalloc_rejects_requests_beyond_its_fixed_scratch():
+    pkv = built_library()
+    lib = pkv.lib()
+    limit = lib.pkv_paged_attn_decode_noalloc_max_scratch()
+    assert limit == 32 << 20
+    # The partials scale with batch x heads x splits; find a size whose split plan on this GPU needs more
+    # than the fixed array (the plan depends on the SM count, so search instead of hard-coding one).
+    Hq, Hkv, D, L = 64, 8, 128, 100000
+    B = next((b for b in range(64, 2048, 4) if lib.pkv_paged_attn_decode_workspace(b, Hq, Hkv, D, L) > limit), None)
+    assert B is not None, "no oversize request found"
+    nul = ctypes.c_void_p(0)
+    st = lib.pkv_paged_attn_decode_noalloc(nul, nul, nul, 0, nul, nul, 32768, B, Hq, Hkv, D, 32, 1 << 20, L, 0.1,
+                                           1.0, 1.0, nul, nul, nul, nul)
+    assert st == 3  # PKV_ERR_WORKSPACE, refused before any launch
