@@ -407,9 +407,91 @@ def extra_workloads(pkv, W, device, pk, args):
     return out
 
 
+def causal_pairs(q_lens, k_lens):
+    """Visible (query, key) pairs under bottom-right causal alignment."""
+    tot = 0
+    for lq, lk in zip(q_lens, k_lens):
+        lq, lk = int(lq), int(lk)
+        i = np.arange(lq, dtype=np.int64)
+        tot += int(np.clip(i + lk - lq + 1, 0, lk).sum())
+    return tot
+
+
+def time_calls(fn, iters, warmup=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
 def prefill_workload(pkv, W, device, pk, args):
-    import prefill_bench  # noqa: F401  (provided with the varlen kernel)
-    return prefill_bench.measure(pkv, W, device, pk, args)
+    """The varlen prefill workload (packed and paged) and the mixed chunked-prefill batch."""
+    res = {}
+    iters = max(10, min(100, args.steps // 20))
+    wl = W.varlen_prefill(device=device)
+    flops = 4 * wl.head_dim * wl.num_heads * causal_pairs(wl.q_lens, wl.k_lens)
+    out = torch.empty_like(wl.q)
+    ms = time_calls(lambda: pkv.paged_attn_varlen(wl.q, wl.k, wl.v, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.max_len_q,
+                                                  wl.max_len_k, scale=wl.scale, out=out), iters)
+    tf = flops / (ms * 1e-3) / 1e12
+    res["varlen_prefill_packed"] = {
+        "workload": "8 seqs, q_len = k_len in U[128,2048] (" + ",".join(str(int(x)) for x in wl.q_lens) +
+                    "), 32 q / 8 kv heads, d128, causal, packed K/V",
+        "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "causal_flops": flops,
+        "iters": iters}
+    del wl, out
+    wp = W.varlen_prefill(device=device, paged=True)
+    shape4 = (wp.num_blocks, wp.block_size, wp.num_kv_heads, wp.head_dim)
+    kc4, vc4 = wp.k_cache.view(shape4), wp.v_cache.view(shape4)
+    need = pkv.lib().pkv_paged_attn_varlen_workspace(wp.batch, wp.total_q, wp.num_heads, wp.num_kv_heads,
+                                                      wp.head_dim, wp.max_len_q, wp.max_len_k, 1)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(wp.q)
+
+    def paged_step():
+        pkv.kv_cache_write(wp.k_new, wp.v_new, wp.k_cache, wp.v_cache, wp.slot_mapping)
+        pkv.paged_attn_varlen(wp.q, kc4, vc4, wp.cu_seqlens_q, wp.cu_seqlens_k, wp.max_len_q, wp.max_len_k,
+                              block_table=wp.block_table, scale=wp.scale, out=out, workspace_buf=ws)
+
+    ms = time_calls(paged_step, iters)
+    tf = flops / (ms * 1e-3) / 1e12
+    res["varlen_prefill_paged"] = {
+        "workload": "same sequences written by slot mapping into a 16-token-block permuted pool, then causal "
+                    "varlen attention reading K/V through the block table (step = write + attention)",
+        "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "iters": iters}
+    del wp, kc4, vc4, out, ws
+    torch.cuda.empty_cache()
+
+    wm = W.mixed_chunked(device=device)
+    shape4 = (wm.num_blocks, wm.block_size, wm.num_kv_heads, wm.head_dim)
+    kc4, vc4 = wm.k_cache.view(shape4), wm.v_cache.view(shape4)
+    need = pkv.lib().pkv_paged_attn_varlen_workspace(wm.batch, wm.total_q, wm.num_heads, wm.num_kv_heads,
+                                                      wm.head_dim, wm.max_len_q, wm.max_len_k, 1)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(wm.q)
+
+    def mixed_step():
+        pkv.kv_cache_write(wm.k_new, wm.v_new, wm.k_cache, wm.v_cache, wm.slot_mapping)
+        pkv.paged_attn_varlen(wm.q, kc4, vc4, wm.cu_seqlens_q, wm.cu_seqlens_k, wm.max_len_q, wm.max_len_k,
+                              block_table=wm.block_table, scale=wm.scale, out=out, workspace_buf=ws)
+
+    ms = time_calls(mixed_step, iters)
+    pre = wm.q_lens > 1
+    mflops = 4 * wm.head_dim * wm.num_heads * causal_pairs(wm.q_lens[pre], wm.k_lens[pre])
+    dec_bytes = int(wm.k_lens[~pre].sum()) * wm.num_kv_heads * wm.head_dim * 2 * 2
+    t_roof = max(mflops / (pk["bf16_tflops"] * 1e12), dec_bytes / (pk["hbm_gbs"] * 1e9))
+    res["mixed_chunked"] = {
+        "workload": "4 x 512-query chunks over 0/2K/4K/8K prefixes (2K prefix shares the 4K chunk's blocks) + 60 "
+                    "decode rows of 513..8193 keys, one varlen call after the write; 32 q / 8 kv, d128, bs16",
+        "ms": ms, "prefill_flops": mflops, "decode_kv_bytes": dec_bytes, "roofline_ms": t_roof * 1e3,
+        "frac_of_roofline": t_roof * 1e3 / ms, "tokens_per_s": wm.total_q / (ms * 1e-3), "iters": iters}
+    return res
 
 
 def run_reference(args):
@@ -464,6 +546,15 @@ def ncu_case(args):
     from paged_kv_cache_200_gb300 import pkv
     from paged_kv_cache_200_gb300 import workloads as W
     B.build()
+    if args.ncu_case == "prefill":
+        # the varlen prefill workload itself (8 seqs of 128..2048 tokens, packed): ~0.2 GB of inputs
+        wl = W.varlen_prefill(device="cuda")
+        for _ in range(4):
+            pkv.paged_attn_varlen(wl.q, wl.k, wl.v, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.max_len_q, wl.max_len_k,
+                                  scale=wl.scale)
+        torch.cuda.synchronize()
+        log("ncu case done: prefill")
+        return
     rng = np.random.default_rng(77)
     dt = "fp8_e4m3" if args.ncu_case == "decode_fp8" else "bf16"
     # 64 sequences of 1K..4K cached tokens: ~0.65 GB of bf16 K/V, larger than L2
@@ -487,7 +578,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "prefill"], default=None,
                     help="run a small case for an ncu capture and exit")
     args = ap.parse_args()
     if args.ncu_case:

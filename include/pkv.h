@@ -148,6 +148,52 @@ PKV_API int pkv_paged_attn_decode(const void* q, const void* k_cache, const void
                           size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /*
+ * Workspace bytes pkv_paged_attn_varlen needs for these sizes on the current
+ * device (0 is a valid answer).  `paged` is non-zero when a block table will be
+ * passed.  Returns 0 for invalid sizes as well.
+ */
+PKV_API size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, int32_t num_heads,
+                                               int32_t num_kv_heads, int32_t head_dim, int32_t max_len_q,
+                                               int32_t max_len_k, int32_t paged);
+
+/*
+ * Variable-length causal attention ([PA] "Varlen パス"; [KVM] "Attention モジュールの実装",
+ * prefill branch; [CH15] prefix caching and chunked prefill).
+ *
+ * Sequence b has Lq_b = cu_seqlens_q[b+1]-cu_seqlens_q[b] queries, packed as
+ * rows cu_seqlens_q[b].. of q ([total_q, num_heads, head_dim] bf16), and
+ * Lk_b = cu_seqlens_k[b+1]-cu_seqlens_k[b] keys:
+ *   - block_table == NULL: k, v are packed [total_k, num_kv_heads, head_dim] bf16
+ *     and key j of sequence b is row cu_seqlens_k[b]+j;
+ *   - otherwise k, v are the paged caches [num_blocks*block_size, num_kv_heads,
+ *     head_dim] bf16 and key j is slot block_table[b*max_blocks_per_seq + j/block_size]
+ *     *block_size + j%block_size (prefix reuse: the keys of a shared prefix are
+ *     the same blocks in several rows of the table).
+ * Causal alignment is bottom-right: query i of sequence b sees key j iff
+ * j <= i + Lk_b - Lq_b (the queries are the last Lq_b of the Lk_b positions).
+ *   out[row, h, :] = softmax_j(scale * <q[row,h], k_j>) . v_j      (bf16, RNE)
+ *   lse[h, row]    = log sum_j exp(scale * <q[row,h], k_j>)        (fp32; nullable)
+ * with kv head h/(num_heads/num_kv_heads).  A query that sees no key outputs
+ * zeros and lse = -inf.
+ *
+ * max_len_q, max_len_k: host upper bounds of the lengths (grid sizing).
+ * total_k: rows of the packed k/v (ignored in paged mode).
+ * Supported: head_dim 64 or 128, bf16 K/V (kv_dtype PKV_BF16; k_scale and
+ * v_scale are reserved), causal != 0; paged block_size a multiple of 16 that
+ * divides 128 or is a multiple of 128.  All of q, k, v, out 16-byte aligned.
+ * In paged mode sequences with exactly one query are computed by the decode
+ * kernels (split-KV over the GQA group) instead of a 128-row tile.
+ */
+PKV_API int pkv_paged_attn_varlen(const void* q, const void* k, const void* v, int32_t kv_dtype,
+                                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                                  int32_t total_q, int32_t total_k, int32_t max_len_q, int32_t max_len_k,
+                                  const int32_t* block_table, int32_t max_blocks_per_seq, int32_t block_size,
+                                  int32_t num_blocks, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  float scale, int32_t causal, float k_scale, float v_scale, void* out,
+                                  float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                  void* stream);
+
+/*
  * Paged decode attention without a caller workspace (no counterpart on the
  * source pages; an addition of this library).
  *

@@ -65,12 +65,31 @@ struct DecodeParams {
   float* ws_o;
   float* ws_lse;
   int32_t* err;
+  // Varlen routing (all null for a plain decode call): CTA z serves sequence
+  // items[z] when z < *item_count; its q/out row is cu_q[b] and its length
+  // cu_k[b+1]-cu_k[b].  lse[b, h] lives at lse[h*lse_head_stride + row*lse_row_stride].
+  const int32_t* items;
+  const int32_t* item_count;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int64_t lse_head_stride;
+  int64_t lse_row_stride;
 };
+
+// Sequence served by grid index z (or -1), its q/out row and its length source.
+__device__ __forceinline__ int item_sequence(const DecodeParams& p, int z) {
+  if (p.items == nullptr) return z;
+  if (z >= __ldg(p.item_count)) return -1;
+  return __ldg(p.items + z);
+}
+__device__ __forceinline__ int64_t item_row(const DecodeParams& p, int b) {
+  return p.cu_q != nullptr ? (int64_t)__ldg(p.cu_q + b) : (int64_t)b;
+}
 
 // Attended length of sequence b, clamped to what the block table and the
 // workspace can hold (violations are flagged by the caller thread).
 __device__ __forceinline__ int attended_length(const DecodeParams& p, int b, bool report) {
-  int len = __ldg(p.seqlens + b);
+  int len = p.cu_k != nullptr ? __ldg(p.cu_k + b + 1) - __ldg(p.cu_k + b) : __ldg(p.seqlens + b);
   const int64_t cap_bt = (int64_t)p.max_blocks * p.block_size;
   const int64_t cap_ws = (int64_t)p.max_splits * p.split_tokens;
   bool bad = false;
@@ -105,7 +124,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(cons
   const int lane = threadIdx.x & 31;
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
+  const int z = blockIdx.z;
+  const int b = item_sequence(p, z);
+  if (b < 0) return;
+  const int64_t qrow_idx = item_row(p, b);
 
   const int len = attended_length(p, b, split == 0 && kvh == 0 && threadIdx.x == 0);
   const int n_splits = (len + p.split_tokens - 1) / p.split_tokens;
@@ -127,7 +149,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(cons
     const int h = lane >> 2;
     const int j = lane & 3;
     const bool hv = h < p.group;
-    const uint16_t* qrow = p.q + ((int64_t)b * p.num_heads + (int64_t)kvh * p.group + (hv ? h : 0)) * D;
+    const uint16_t* qrow = p.q + (qrow_idx * p.num_heads + (int64_t)kvh * p.group + (hv ? h : 0)) * D;
 #pragma unroll
     for (int kk = 0; kk < kDT; ++kk) {
       if constexpr (!kFp8) {
@@ -349,10 +371,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(cons
     const bool any = L > 0.f;
     const float val = any ? acc * p.v_mul / L : 0.f;
     const float lse2 = any ? ms + log2f(L) : -INFINITY;
-    const int64_t bh = (int64_t)b * p.num_heads + (int64_t)kvh * p.group + h;
+    const int hq = kvh * p.group + h;
+    const int64_t bh = (int64_t)z * p.num_heads + hq;  // partials are indexed by grid item
     if (single) {
-      p.out[bh * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-      if (p.lse != nullptr && d == 0) p.lse[bh] = any ? lse2 * kLn2 : -INFINITY;
+      p.out[(qrow_idx * p.num_heads + hq) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+      if (p.lse != nullptr && d == 0)
+        p.lse[hq * p.lse_head_stride + qrow_idx * p.lse_row_stride] = any ? lse2 * kLn2 : -INFINITY;
     } else {
       p.ws_o[(bh * p.max_splits + split) * D + d] = val;
       if (d == 0) p.ws_lse[bh * p.max_splits + split] = lse2;
@@ -367,7 +391,11 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   const int lane = threadIdx.x & 31;
   const int64_t bh = (int64_t)blockIdx.x * 4 + warp;
   if (bh >= (int64_t)batch * p.num_heads) return;
-  const int b = (int)(bh / p.num_heads);
+  const int z = (int)(bh / p.num_heads);
+  const int hq = (int)(bh % p.num_heads);
+  const int b = item_sequence(p, z);
+  if (b < 0) return;
+  const int64_t row = item_row(p, b);
   const int len = attended_length(p, b, false);
   const int n = (len + p.split_tokens - 1) / p.split_tokens;
   if (n <= 1) return;
@@ -404,10 +432,11 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
       }
     }
   }
-  uint16_t* orow = p.out + bh * D + lane * kPer;
+  uint16_t* orow = p.out + (row * p.num_heads + hq) * D + lane * kPer;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) orow[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
-  if (p.lse != nullptr && lane == 0) p.lse[bh] = any ? lse2 * kLn2 : -INFINITY;
+  if (p.lse != nullptr && lane == 0)
+    p.lse[hq * p.lse_head_stride + row * p.lse_row_stride] = any ? lse2 * kLn2 : -INFINITY;
 }
 
 struct SplitPlan {
@@ -528,10 +557,65 @@ extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const v
     p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + rows * head_dim * sizeof(float));
   }
   p.err = err_flag;
+  p.lse_head_stride = 1;
+  p.lse_row_stride = num_heads;
   cudaStream_t st = as_stream(stream);
   if (head_dim == 128) return fp8 ? launch_decode<128, true>(p, batch, pl, st) : launch_decode<128, false>(p, batch, pl, st);
   return fp8 ? launch_decode<64, true>(p, batch, pl, st) : launch_decode<64, false>(p, batch, pl, st);
 }
+
+namespace pkv {
+
+size_t varlen_decode_workspace(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k) {
+  if (batch <= 0 || max_len_k <= 0) return 0;
+  return plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k).workspace;
+}
+
+// Decode kernels over the single-query sequences of a paged varlen batch
+// (items[0..*item_count) on the device, at most `batch` of them).
+int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* items,
+                         const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,
+                         const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                         int32_t max_len_k, int64_t total_q, float scale, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, int32_t* err_flag, cudaStream_t st) {
+  if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1);
+  if (pl.workspace > workspace_bytes) return PKV_ERR_WORKSPACE;
+  DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_table = block_table;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.split_tokens = pl.split_tokens;
+  p.max_splits = pl.max_splits;
+  p.scale_log2 = scale * kLog2e;
+  p.v_mul = 1.f;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  if (pl.max_splits > 1) {
+    const size_t rows = (size_t)batch * num_heads * pl.max_splits;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + rows * head_dim * sizeof(float));
+  }
+  p.err = err_flag;
+  p.items = items;
+  p.item_count = item_count;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.lse_head_stride = total_q;
+  p.lse_row_stride = 1;
+  if (head_dim == 128) return launch_decode<128, false>(p, batch, pl, st);
+  return launch_decode<64, false>(p, batch, pl, st);
+}
+
+}  // namespace pkv
 
 // ---------------------------------------------------------------------------
 // Decode for callers that cannot allocate device memory.

@@ -1,0 +1,737 @@
+// Causal GQA varlen prefill on tcgen05 tensor cores (TMEM accumulators, TMA-fed).
+//
+// Source: "ページド・アテンション" (transformers docs), section "Varlen パス": packed
+// variable-length sequences indexed by cumulative lengths cu_seq_lens_q/k and
+// their maxima; "効率的な KV キャッシュ管理と Attention 計算" (itan.pw), section
+// "Attention モジュールの実装": causal prefill, reading K/V from the paged cache
+// through block_tables when prefixes are shared; "KV cache / batching / paged
+// attention" (1s.xyz ch. 15), "FlashAttention：注意計算そのものを速く": tiles in
+// on-chip memory give exactly ordinary attention.
+//
+// Causal alignment: query i of a sequence with Lq queries and Lk keys sees key
+// j iff j <= i + Lk - Lq (the queries are the last Lq positions; prefix reuse).
+//
+// CTA = 128 query rows of one (sequence, query head); 6 warps:
+//   warp 0      TMA producer: Q once, then K/V tiles of 128 keys (2 stages each);
+//               packed K/V: one box per head-dim half; paged: one box per page.
+//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, then O += P V.
+//   warps 2..5  softmax warpgroup, thread r <-> TMEM lane / query row r:
+//               loads its S row, masks, online softmax in the log2 domain
+//               (the running max moves only when it grows by more than 2^8,
+//               so O is rescaled rarely), writes P (bf16) to shared memory in
+//               the 128-byte-swizzled K-major layout the MMA reads, and
+//               finally normalises O and stores the bf16 output and lse.
+// TMEM: S in columns [0,128), O in [128, 128+D).
+// Every mbarrier wait is bounded by a deadline; on expiry the CTA flags
+// PKV_DEVERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kBM = 128;          // query rows per CTA
+constexpr int kBN = 128;          // keys per tile
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+
+struct PrefillParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* block_table;
+  int32_t max_blocks;
+  int32_t block_size;
+  int32_t box_rows;      // rows per paged TMA box: min(block_size, 128)
+  int32_t num_blocks;
+  int32_t num_heads;
+  int32_t group;
+  int32_t n_qtiles;
+  int32_t route_decode;  // sequences with exactly one query are left to the decode kernels
+  float scale_log2;
+  int64_t total_q;
+  uint16_t* out;
+  float* lse;
+  int32_t* err;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, TMA, tcgen05
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false on deadline expiry or when another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitNs) {
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 x bf16 -> f32, A K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+#define PKV_TMEM_LD32(taddr, r)                                                                                    \
+  asm volatile(                                                                                                    \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%" \
+      "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                                 \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),            \
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),      \
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),    \
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])     \
+      : "r"(taddr))
+
+#define PKV_TMEM_ST32(taddr, r)                                                                                   \
+  asm volatile(                                                                                                   \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%" \
+      "18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),                                 \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),          \
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),  \
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), \
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                                                   \
+      : "memory")
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// shared-memory plan
+// ---------------------------------------------------------------------------
+
+template <int D>
+struct Smem {
+  static constexpr int kAtoms = D / 64;                 // 64-element (128-byte) column groups
+  static constexpr int kTileBytes = 128 * D * 2;        // a [128 x D] bf16 tile
+  static constexpr int kAtomBytes = 128 * 128;          // [128 rows x 128 B]
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;            // 2 stages
+  static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
+  static constexpr int kP = kV + 2 * kTileBytes;        // [128 x 128] bf16 = 32 KB
+  static constexpr int kBar = kP + 128 * 128 * 2;
+  static constexpr int kNumBars = 14;
+  static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kAlloc = kTotal + 1024;          // slack to align the base to 1024
+};
+
+enum Bar {
+  kQFull = 0,
+  kKFull0 = 1,   // +stage
+  kKEmpty0 = 3,  // +stage
+  kVFull0 = 5,
+  kVEmpty0 = 7,
+  kSFull = 9,
+  kSFree = 10,
+  kPFull = 11,
+  kODone = 12,
+  kDrain = 13
+};
+
+struct Seq {
+  int q0, Lq, k0, Lk, row0, rows, diag, n_kv;
+  bool skip;
+};
+
+__device__ __forceinline__ Seq seq_info(const PrefillParams& p, int b, int qtile, bool report) {
+  Seq s;
+  s.q0 = __ldg(p.cu_q + b);
+  s.Lq = __ldg(p.cu_q + b + 1) - s.q0;
+  s.k0 = __ldg(p.cu_k + b);
+  s.Lk = __ldg(p.cu_k + b + 1) - s.k0;
+  bool bad = false;
+  if (s.Lq < 0) { s.Lq = 0; bad = true; }
+  if (s.Lk < 0) { s.Lk = 0; bad = true; }
+  if (p.block_table != nullptr && (int64_t)s.Lk > (int64_t)p.max_blocks * p.block_size) {
+    s.Lk = p.max_blocks * p.block_size;
+    bad = true;
+  }
+  if (bad && report) flag_error(p.err, PKV_DEVERR_LENGTH);
+  s.row0 = qtile * kBM;
+  s.rows = min(kBM, s.Lq - s.row0);
+  s.diag = s.Lk - s.Lq;
+  s.skip = s.rows <= 0 || (p.route_decode && s.Lq == 1);
+  const int kmax = s.row0 + s.rows - 1 + s.diag;  // last key the last row sees
+  const int kv_tiles = (s.Lk + kBN - 1) / kBN;
+  s.n_kv = kmax < 0 ? 0 : min(kmax / kBN + 1, kv_tiles);
+  return s;
+}
+
+template <int D, bool kPaged>
+__global__ void __launch_bounds__(kThreads, 1)
+    varlen_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int head = blockIdx.x;
+  const int qtile = p.n_qtiles - 1 - (int)blockIdx.y;  // longest causal rows first
+  const int b = blockIdx.z;
+  const int kvh = head / p.group;
+
+  const Seq sq = seq_info(p, b, qtile, qtile == 0 && head == 0 && threadIdx.x == 0);
+  if (sq.skip) return;
+
+  // rows that see no key at all: zeros and lse = -inf, nothing else to do
+  if (sq.n_kv == 0) {
+    for (int r = threadIdx.x; r < sq.rows; r += kThreads) {
+      const int64_t row = (int64_t)sq.q0 + sq.row0 + r;
+      uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.num_heads + head) * D);
+      for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+      if (p.lse) p.lse[(int64_t)head * p.total_q + row] = -INFINITY;
+    }
+    return;
+  }
+
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kKFull0 + s), 1);
+      mbar_init(bar(kKEmpty0 + s), 1);
+      mbar_init(bar(kVFull0 + s), 1);
+      mbar_init(bar(kVEmpty0 + s), 1);
+    }
+    mbar_init(bar(kSFull), 1);
+    mbar_init(bar(kSFree), 128);
+    mbar_init(bar(kPFull), 128);
+    mbar_init(bar(kODone), 1);
+    mbar_init(bar(kDrain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(256)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem;        // columns [0, 128)
+  const uint32_t tO = tmem + 128;  // columns [128, 128 + D)
+  const int n_kv = sq.n_kv;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    flag_error(p.err, PKV_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+      const int32_t* bt = kPaged ? p.block_table + (int64_t)b * p.max_blocks : nullptr;
+      mbar_expect_tx(bar(kQFull), L::kTileBytes);
+      for (int a = 0; a < L::kAtoms; ++a)
+        tma_load_3d(sbase + L::kQ + a * L::kAtomBytes, &tm_q, a * 64, head, sq.q0 + sq.row0, bar(kQFull));
+      bool ok = true;
+      auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
+        const int key0 = j * kBN;
+        if constexpr (!kPaged) {
+          mbar_expect_tx(full, L::kTileBytes);
+          for (int a = 0; a < L::kAtoms; ++a) tma_load_3d(dst + a * L::kAtomBytes, map, a * 64, kvh, sq.k0 + key0, full);
+        } else {
+          const int br = p.box_rows;
+          const int npages = kBN / br;
+          int loaded = 0;
+          for (int pg = 0; pg < npages; ++pg)
+            if (key0 + pg * br < sq.Lk) ++loaded;
+          mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
+          for (int pg = 0; pg < npages; ++pg) {
+            const int pos = key0 + pg * br;
+            if (pos >= sq.Lk) break;
+            int blk = __ldg(bt + pos / p.block_size);
+            if (blk < 0 || blk >= p.num_blocks) {
+              flag_error(p.err, PKV_DEVERR_BLOCK);
+              blk = 0;  // never dereference a bad id; the sequence's result is unspecified
+            }
+            const int slot = blk * p.block_size + pos % p.block_size;
+            for (int a = 0; a < L::kAtoms; ++a)
+              tma_load_3d(dst + a * L::kAtomBytes + pg * br * 128, map, a * 64, kvh, slot, full);
+          }
+        }
+      };
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j & 1, u = j >> 1;
+        if (u > 0 && !mbar_wait(bar(kKEmpty0 + s), (u - 1) & 1, abort_flag)) { ok = false; fail(); break; }
+        load_tile(&tm_k, sbase + L::kK + s * L::kTileBytes, bar(kKFull0 + s), j);
+        last_k[s] = u;
+        if (u > 0 && !mbar_wait(bar(kVEmpty0 + s), (u - 1) & 1, abort_flag)) { ok = false; fail(); break; }
+        load_tile(&tm_v, sbase + L::kV + s * L::kTileBytes, bar(kVFull0 + s), j);
+        last_v[s] = u;
+      }
+      // every copy this CTA issued has landed before shared memory is released
+      if (!mbar_wait(bar(kQFull), 0, abort_flag)) fail();
+      for (int s = 0; s < 2; ++s) {
+        if (last_k[s] >= 0) mbar_wait(bar(kKFull0 + s), last_k[s] & 1, abort_flag);
+        if (last_v[s] >= 0) mbar_wait(bar(kVFull0 + s), last_v[s] & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);
+    constexpr uint32_t kIdescPV = make_idesc(kBM, D, true);
+    bool ok = mbar_wait(bar(kQFull), 0, abort_flag);
+    if (!ok) fail();
+    bool issued = false;
+    auto issue_pv = [&](int t) -> bool {
+      if (!mbar_wait(bar(kPFull), t & 1, abort_flag)) return false;
+      if (!mbar_wait(bar(kVFull0 + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
+      const uint32_t vbase = sbase + L::kV + (t & 1) * L::kTileBytes;
+      // keys at or beyond Lk: zero their V rows (stale or foreign data must not meet P = 0)
+      const int valid = sq.Lk - t * kBN;
+      if (valid < kBN) {
+        uint8_t* vs = smem + L::kV + (t & 1) * L::kTileBytes;
+        const int first = valid > 0 ? valid : 0;
+        const int nchunks = (kBN - first) * 8;  // 16-byte chunks per atom
+        for (int a = 0; a < L::kAtoms; ++a)
+          for (int c = lane; c < nchunks; c += 32)
+            *reinterpret_cast<uint4*>(vs + a * L::kAtomBytes + (first + c / 8) * 128 + (c % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t pbase = sbase + L::kP;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t ad = sw128_desc(pbase + (kk >> 2) * L::kAtomBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, L::kAtomBytes, 1024);
+          mma_bf16(tO, ad, bd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(kODone));
+        mma_commit(bar(kVEmpty0 + (t & 1)));
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int s = j & 1, u = j >> 1;
+      if (!mbar_wait(bar(kKFull0 + s), u & 1, abort_flag)) { ok = false; break; }
+      if (j > 0 && !mbar_wait(bar(kSFree), (j - 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t qb = sbase + L::kQ;
+        const uint32_t kb = sbase + L::kK + s * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+          mma_bf16(tS, sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024), kIdescQK,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kSFull));
+        mma_commit(bar(kKEmpty0 + s));
+      }
+      __syncwarp();
+      issued = true;
+      if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+    }
+    if (ok && n_kv > 0 && !issue_pv(n_kv - 1)) ok = false;
+    if (!ok) fail();
+    // drain: all MMAs this thread issued have completed before TMEM is released
+    if (issued) {
+      if (lane == 0) mma_commit(bar(kDrain));
+      __syncwarp();
+      mbar_wait(bar(kDrain), 0, abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroup
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // TMEM lane == query row in the tile
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int qi = sq.row0 + r;
+    const int lim = qi + sq.diag;  // last visible key of this row
+    const float c = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    uint8_t* psm = smem + L::kP;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!mbar_wait(bar(kSFull), j & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[128];
+      PKV_TMEM_LD32(tS + lane_off + 0, (sr + 0));
+      PKV_TMEM_LD32(tS + lane_off + 32, (sr + 32));
+      PKV_TMEM_LD32(tS + lane_off + 64, (sr + 64));
+      PKV_TMEM_LD32(tS + lane_off + 96, (sr + 96));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(kSFree));
+
+      const int key0 = j * kBN;
+      const bool need_mask = (key0 + kBN - 1 > sq.row0 + sq.diag) || (key0 + kBN > sq.Lk);
+      float mx = -INFINITY;
+      if (need_mask) {
+        const int vis = min(lim, sq.Lk - 1) - key0;  // columns 0..vis are visible
+#pragma unroll
+        for (int k = 0; k < 128; ++k) {
+          float v = __uint_as_float(sr[k]);
+          v = (k <= vis) ? v : -INFINITY;
+          sr[k] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 128; ++k) mx = fmaxf(mx, __uint_as_float(sr[k]));
+      }
+      const float mt = mx * c;  // tile max in log2 units (-inf if the row sees nothing here)
+      float m_use = m;
+      if (mt > m + kRescaleThreshold || (m == -INFINITY && mt != -INFINITY)) m_use = mt;
+      const bool live = m_use != -INFINITY;
+      const bool moved = m_use != m;
+      const float alpha = (moved && m != -INFINITY) ? fast_exp2(m - m_use) : (moved ? 0.f : 1.f);
+      const float nm = live ? -m_use : 0.f;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int k = 0; k < 128; k += 2) {
+        const float p0 = live ? fast_exp2(fmaf(__uint_as_float(sr[k]), c, nm)) : 0.f;
+        const float p1 = live ? fast_exp2(fmaf(__uint_as_float(sr[k + 1]), c, nm)) : 0.f;
+        sum += p0 + p1;
+        pk[k >> 1] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + sum;
+      m = m_use;
+
+      if (j > 0) {
+        if (!mbar_wait(bar(kODone), (j - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // rescale O when this row's reference max moved (warp-collective TMEM access)
+        if (__any_sync(0xffffffffu, moved && alpha != 1.f)) {
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            PKV_TMEM_LD32(tO + lane_off + ch * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            PKV_TMEM_ST32(tO + lane_off + ch * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P (bf16) into the swizzled K-major tile: row r, keys 8c..8c+7 in chunk c
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const int atom = ch >> 3, cc = ch & 7;
+        uint4* dst = reinterpret_cast<uint4*>(psm + atom * L::kAtomBytes + r * 128 + ((cc ^ (r & 7)) << 4));
+        *dst = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kPFull));
+    }
+    if (ok && n_kv > 0) {
+      if (!mbar_wait(bar(kODone), (n_kv - 1) & 1, abort_flag)) ok = false;
+    }
+    if (!ok) {
+      fail();
+    } else {
+      tc_fence_after();
+      const bool row_valid = r < sq.rows;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t row = (int64_t)sq.q0 + qi;
+      uint16_t* orow = p.out + (row * p.num_heads + head) * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        PKV_TMEM_LD32(tO + lane_off + ch * 32, o);
+        tmem_wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[k + 0]) * inv, __uint_as_float(o[k + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + ch * 32 + k) = v;
+          }
+        }
+      }
+      if (row_valid && p.lse != nullptr)
+        p.lse[(int64_t)head * p.total_q + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+  }
+}
+
+// Varlen prep: compacts the sequences that have exactly one query (decode rows
+// of a mixed batch) into items[0..*count); the prefill kernel skips them and
+// the split-KV decode kernels serve them, one CTA per (split, kv head, item).
+__global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __restrict__ cu_q, int batch,
+                                                           int32_t* __restrict__ items, int32_t* __restrict__ count) {
+  __shared__ int n;
+  if (threadIdx.x == 0) n = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+    if (__ldg(cu_q + b + 1) - __ldg(cu_q + b) == 1) items[atomicAdd(&n, 1)] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *count = n;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+struct VarlenWs {
+  size_t count_off, items_off, decode_off, total;
+};
+
+VarlenWs varlen_ws_layout(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k, bool route) {
+  VarlenWs w{0, 0, 0, 0};
+  if (!route || batch <= 0) return w;
+  w.count_off = 0;
+  w.items_off = 256;
+  w.decode_off = w.items_off + (((size_t)batch * 4 + 255) / 256) * 256;
+  w.total = w.decode_off + varlen_decode_workspace(batch, num_heads, num_kv_heads, head_dim, max_len_k);
+  return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [rows, heads, dim] bf16, box = 64 elements x 1 head x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int dim, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool kPaged>
+int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillParams& p,
+                   int batch, cudaStream_t st) {
+  auto kern = varlen_prefill_kernel<D, kPaged>;
+  const int smem = Smem<D>::kAlloc;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= 64) dev = 63;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  dim3 grid(p.num_heads, p.n_qtiles, batch);
+  kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, p);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace pkv
+
+// Single-query sequences go to the decode kernels in paged mode when the GQA
+// group fits one decode CTA.
+static bool routes_decode(bool paged, int num_heads, int num_kv_heads) {
+  return paged && num_kv_heads > 0 && num_heads % num_kv_heads == 0 && num_heads / num_kv_heads <= 8;
+}
+
+extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, int32_t num_heads,
+                                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_len_q,
+                                                  int32_t max_len_k, int32_t paged) {
+  (void)total_q;
+  (void)max_len_q;
+  if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_len_k < 0) return 0;
+  return pkv::varlen_ws_layout(batch, num_heads, num_kv_heads, head_dim, max_len_k,
+                               routes_decode(paged != 0, num_heads, num_kv_heads))
+      .total;
+}
+
+extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v, int32_t kv_dtype,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                                     int32_t total_q, int32_t total_k, int32_t max_len_q, int32_t max_len_k,
+                                     const int32_t* block_table, int32_t max_blocks_per_seq, int32_t block_size,
+                                     int32_t num_blocks, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     float scale, int32_t causal, float k_scale, float v_scale, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                     void* stream) {
+  using namespace pkv;
+  (void)k_scale;
+  (void)v_scale;
+  if (batch < 0 || total_q < 0 || total_k < 0 || max_len_q < 0 || max_len_k < 0 || num_heads <= 0 ||
+      num_kv_heads <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 128 && head_dim != 64) return PKV_ERR_UNSUPPORTED;
+  if (kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (!causal) return PKV_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  const bool paged = block_table != nullptr;
+  if (paged) {
+    if (block_size <= 0 || block_size % 16 != 0 || (block_size < 128 && 128 % block_size != 0) ||
+        (block_size > 128 && block_size % 128 != 0))
+      return PKV_ERR_UNSUPPORTED;
+    if (num_blocks <= 0 || max_blocks_per_seq <= 0) return PKV_ERR_INVALID_ARG;
+  }
+  if (batch == 0 || total_q == 0 || max_len_q == 0) return PKV_OK;
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+
+  CUtensorMap mq, mk, mv;
+  const int64_t kv_rows = paged ? (int64_t)num_blocks * block_size : (int64_t)total_k;
+  const int kv_box = paged ? (block_size < 128 ? block_size : 128) : 128;
+  if (!make_map(&mq, q, total_q, num_heads, head_dim, 128) ||
+      !make_map(&mk, k, kv_rows, num_kv_heads, head_dim, kv_box) ||
+      !make_map(&mv, v, kv_rows, num_kv_heads, head_dim, kv_box))
+    return PKV_ERR_CUDA;
+
+  const bool route = routes_decode(paged, num_heads, num_kv_heads);
+  const VarlenWs wl = varlen_ws_layout(batch, num_heads, num_kv_heads, head_dim, max_len_k, route);
+  if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
+                       (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return PKV_ERR_WORKSPACE;
+
+  PrefillParams p{};
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = block_size;
+  p.box_rows = kv_box;
+  p.num_blocks = num_blocks;
+  p.num_heads = num_heads;
+  p.group = num_heads / num_kv_heads;
+  p.n_qtiles = (max_len_q + kBM - 1) / kBM;
+  p.route_decode = route ? 1 : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.total_q = total_q;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.err = err_flag;
+  cudaStream_t st = as_stream(stream);
+  int32_t* count = nullptr;
+  int32_t* items = nullptr;
+  if (route) {
+    count = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.count_off);
+    items = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.items_off);
+    varlen_prep_kernel<<<1, 1024, 0, st>>>(cu_seqlens_q, batch, items, count);
+  }
+  int rc;
+  if (head_dim == 128)
+    rc = paged ? launch_prefill<128, true>(mq, mk, mv, p, batch, st) : launch_prefill<128, false>(mq, mk, mv, p, batch, st);
+  else
+    rc = paged ? launch_prefill<64, true>(mq, mk, mv, p, batch, st) : launch_prefill<64, false>(mq, mk, mv, p, batch, st);
+  if (rc != PKV_OK || !route) return rc;
+  return launch_varlen_decode(q, k, v, items, count, cu_seqlens_q, cu_seqlens_k, block_table, max_blocks_per_seq,
+                              batch, num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_len_k, total_q,
+                              scale, out, lse, static_cast<char*>(workspace) + wl.decode_off,
+                              wl.total - wl.decode_off, err_flag, st);
+}

@@ -238,3 +238,55 @@ def paged_attn_decode_noalloc(q, k_cache, v_cache, cache_seqlens, block_table, s
                                              _ptr(out), _ptr(lse), _ptr(err_flag), _stream(stream))
     _check(st)
     return out
+
+
+# ---------------------------------------------------------------------------
+# varlen (prefill) attention
+# ---------------------------------------------------------------------------
+
+
+def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_len_k: int, block_table=None,
+                      scale: float = None, causal: bool = True, out=None, lse=None, return_lse=False,
+                      err_flag=None, workspace_buf=None, stream=None):
+    """Causal varlen attention; returns ``out [total_q, Hq, D]`` (and ``lse [Hq, total_q]``).
+
+    Without ``block_table``: ``k``/``v`` are packed ``[total_k, Hkv, D]``.  With it:
+    ``k``/``v`` are the paged caches ``[num_blocks, block_size, Hkv, D]`` and
+    ``block_table`` is int32 ``[B, max_blocks_per_seq]``.  ``max_len_q`` /
+    ``max_len_k`` are host upper bounds of the lengths (no device sync is made).
+    """
+    _require_cuda(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table)
+    T, Hq, D = q.shape
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bf16 [total_q, Hq, D]")
+    if not (k.is_contiguous() and v.is_contiguous()) or k.shape != v.shape:
+        raise ValueError("k and v must be contiguous and of the same shape")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    B = cu_seqlens_q.numel() - 1
+    if block_table is None:
+        total_k, Hkv, _ = k.shape
+        MB, bs, NB = 0, 0, 0
+    else:
+        NB, bs, Hkv, _ = k.shape
+        total_k = NB * bs
+        if block_table.dtype != torch.int32 or not block_table.is_contiguous():
+            raise ValueError("block_table must be contiguous int32")
+        MB = block_table.shape[1]
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    L = lib()
+    paged = 1 if block_table is not None else 0
+    need = L.pkv_paged_attn_varlen_workspace(B, T, Hq, Hkv, D, int(max_len_q), int(max_len_k), paged)
+    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device) if need else None)
+    st = L.pkv_paged_attn_varlen(_ptr(q), _ptr(k), _ptr(v), _cache_dtype(k), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), B, T, total_k, int(max_len_q), int(max_len_k),
+                                 _ptr(block_table), MB, bs, NB, Hq, Hkv, D, float(scale), 1 if causal else 0,
+                                 1.0, 1.0, _ptr(out), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
+                                 _ptr(err_flag), _stream(stream))
+    _check(st)
+    return (out, lse) if (return_lse or lse is not None) else out

@@ -1,0 +1,218 @@
+"""Causal varlen prefill (tcgen05 kernel) on the GPU vs the fp64 oracle.
+
+Small cases compare every output row; the full-size workloads (8 sequences of
+128..2048 tokens, packed and paged; the mixed chunked-prefill batch) compare
+sampled sequences in the launch configuration the benchmark uses.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from paged_kv_cache_200_gb300 import workloads as W
+from _helpers import BF16_ATOL, BF16_RTOL, assert_close, bits, built_library, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    return built_library()
+
+
+def _packed(pkv, wl):
+    out, lse = pkv.paged_attn_varlen(wl.q, wl.k, wl.v, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.max_len_q,
+                                     wl.max_len_k, scale=wl.scale, return_lse=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _check_rows(out, lse, ref, ref_lse, rows=None, what=""):
+    got, gl = f64(out), f64(lse)
+    if rows is not None:
+        got, ref, gl, ref_lse = got[rows], ref[rows], gl[:, rows], ref_lse[:, rows]
+    assert_close(got, ref, BF16_ATOL, BF16_RTOL, what + " out")
+    assert_close(gl, ref_lse, 1e-3, 1e-3, what + " lse")
+
+
+PACKED = [
+    # (q_lens, k_lens, Hq, Hkv, D)
+    ([128], [128], 4, 4, 128),
+    ([1, 2, 127, 128, 129, 300], [1, 2, 127, 128, 129, 300], 8, 2, 128),
+    ([100, 37, 260], [400, 37, 900], 8, 1, 128),              # queries are the last positions
+    ([10, 3, 1], [0, 1, 7], 4, 2, 64),                         # the docs' varlen example (empty rows)
+    ([256, 513], [256, 513], 16, 2, 64),
+    ([700, 5, 1000], [700, 5, 1000], 32, 8, 128),
+    ([33, 200], [33, 200], 8, 8, 64),
+]
+
+
+@pytest.mark.parametrize("case", PACKED, ids=[f"{len(c[0])}seq_{c[2]}q{c[3]}kv_d{c[4]}_{i}" for i, c in enumerate(PACKED)])
+def test_varlen_packed_small(pkv, case):
+    q_lens, k_lens, Hq, Hkv, D = case
+    wl = W.make_varlen_packed(q_lens, k_lens, Hq, Hkv, D, seed=sum(q_lens) + 7 * Hq + D, device="cuda")
+    out, lse = _packed(pkv, wl)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(wl.k), bits(wl.v), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True)
+    _check_rows(out, lse, ref, ref_lse, what=str(case))
+
+
+def _write_new_tokens(pkv, wl):
+    kc, vc = wl.k_cache.clone(), wl.v_cache.clone()
+    pkv.kv_cache_write(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
+    return kc, vc
+
+
+def _paged(pkv, wl, kc, vc):
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    out, lse = pkv.paged_attn_varlen(wl.q, kc.view(shape4), vc.view(shape4), wl.cu_seqlens_q, wl.cu_seqlens_k,
+                                     wl.max_len_q, wl.max_len_k, block_table=wl.block_table, scale=wl.scale,
+                                     return_lse=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+PAGED = [
+    # (q_lens, prefix_lens, Hq, Hkv, D, bs)
+    ([128, 50, 300], [0, 0, 0], 8, 2, 128, 16),
+    ([64, 129, 7], [500, 31, 1000], 8, 2, 128, 32),
+    ([200, 1, 1, 64], [0, 700, 33, 900], 32, 8, 128, 16),
+    ([90, 260], [130, 0], 4, 1, 64, 64),
+    ([300, 17], [40, 257], 8, 4, 128, 128),
+    ([150, 150], [600, 5], 8, 2, 128, 256),
+]
+
+
+@pytest.mark.parametrize("case", PAGED, ids=[f"bs{c[5]}_{c[2]}q{c[3]}kv_d{c[4]}_{i}" for i, c in enumerate(PAGED)])
+def test_varlen_paged_small(pkv, case):
+    q_lens, prefix, Hq, Hkv, D, bs = case
+    wl = W.make_varlen_paged(q_lens, prefix, Hq, Hkv, D, bs, seed=sum(q_lens) + sum(prefix) + bs, device="cuda",
+                             extra_blocks=3)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=bs)
+    _check_rows(out, lse, ref, ref_lse, what=str(case))
+
+
+def test_varlen_paged_equals_packed(pkv):
+    """The same keys read through a permuted pool or packed give the same result."""
+    wl = W.make_varlen_paged([300, 77, 500], [0, 0, 0], 16, 4, 128, 16, seed=41, device="cuda")
+    kc, vc = _write_new_tokens(pkv, wl)
+    out_p, _ = _paged(pkv, wl, kc, vc)
+    out_k = pkv.paged_attn_varlen(wl.q, wl.k_new, wl.v_new, wl.cu_seqlens_q, wl.cu_seqlens_q, wl.max_len_q,
+                                  wl.max_len_q, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert_close(f64(out_p), f64(out_k), 1e-2, 1e-2, "paged vs packed")
+
+
+def test_varlen_paged_nan_poisoned_unused_slots(pkv):
+    wl = W.make_varlen_paged([100, 45], [60, 200], 8, 2, 128, 32, seed=43, device="cuda", extra_blocks=4)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out0, lse0 = _paged(pkv, wl, kc, vc)
+    table = wl.block_table.cpu().numpy()
+    used = np.zeros(wl.num_blocks * wl.block_size, dtype=bool)
+    for b, L in enumerate(wl.k_lens):
+        for p in range(int(L)):
+            used[O.slot_of(table[b], p, wl.block_size)] = True
+    unused = torch.from_numpy(np.flatnonzero(~used)).cuda()
+    kc[unused] = float("nan")
+    vc[unused] = float("nan")
+    out1, lse1 = _paged(pkv, wl, kc, vc)
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+
+
+def test_varlen_chunked_equals_whole(pkv):
+    """Prefix reuse: the last chunk's queries over prefix+chunk keys equal the same rows of one prefill."""
+    L, split = 700, 450
+    whole = W.make_varlen_packed([L], [L], 8, 2, 128, seed=45, device="cuda")
+    out_w, _ = _packed(pkv, whole)
+    part = pkv.paged_attn_varlen(whole.q[split:].contiguous(), whole.k, whole.v,
+                                 torch.tensor([0, L - split], dtype=torch.int32, device="cuda"),
+                                 torch.tensor([0, L], dtype=torch.int32, device="cuda"), L - split, L,
+                                 scale=whole.scale)
+    torch.cuda.synchronize()
+    assert_close(f64(part), f64(out_w[split:]), 1e-2, 1e-2, "chunked")
+
+
+def test_varlen_bad_block_is_flagged(pkv):
+    wl = W.make_varlen_paged([64, 64], [100, 100], 8, 2, 128, 16, seed=47, device="cuda")
+    kc, vc = _write_new_tokens(pkv, wl)
+    bt = wl.block_table.clone()
+    bt[0, 2] = 1 << 29
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    out = pkv.paged_attn_varlen(wl.q, kc.view(shape4), vc.view(shape4), wl.cu_seqlens_q, wl.cu_seqlens_k,
+                                wl.max_len_q, wl.max_len_k, block_table=bt, scale=wl.scale, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.DEVERR_BLOCK
+    ref, _ = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                 wl.cu_seqlens_k.cpu().numpy(), wl.scale, True, block_table=wl.block_table.cpu().numpy(),
+                                 block_size=16, seqs=[1])
+    rows = np.arange(64, 128)
+    assert_close(f64(out)[rows], ref[rows], BF16_ATOL, BF16_RTOL, "sequence 1")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled sequences
+# ---------------------------------------------------------------------------
+
+
+def _sub_pool(wl, kc, vc, seqs):
+    """Host copies of only the blocks the sampled sequences use, with a remapped table."""
+    table = wl.block_table.cpu().numpy()
+    nb = [-(-int(L) // wl.block_size) for L in wl.k_lens]
+    blocks = sorted({int(x) for s in seqs for x in table[s][:nb[s]]})
+    remap = {blk: i for i, blk in enumerate(blocks)}
+    idx = torch.tensor(blocks, device="cuda")
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    ks = bits(kc.view(shape4)[idx]).reshape(-1, wl.num_kv_heads, wl.head_dim)
+    vs = bits(vc.view(shape4)[idx]).reshape(-1, wl.num_kv_heads, wl.head_dim)
+    tsub = np.full_like(table, -1)
+    for s in seqs:
+        tsub[s, :nb[s]] = [remap[int(x)] for x in table[s][:nb[s]]]
+    return ks, vs, tsub
+
+
+def _rows_of(wl, seqs):
+    cu = wl.cu_seqlens_q.cpu().numpy()
+    return np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
+
+
+def test_varlen_prefill_full_size_packed(pkv):
+    wl = W.varlen_prefill(device="cuda")
+    out, lse = _packed(pkv, wl)
+    seqs = [int(np.argmax(wl.q_lens)), int(np.argmin(wl.q_lens))]
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(wl.k), bits(wl.v), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True, seqs=seqs)
+    _check_rows(out, lse, ref, ref_lse, rows=_rows_of(wl, seqs), what="prefill packed")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_varlen_prefill_full_size_paged(pkv):
+    wl = W.varlen_prefill(device="cuda", paged=True)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc)
+    seqs = [int(np.argmax(wl.q_lens)), 3]
+    ks, vs, tsub = _sub_pool(wl, kc, vc, seqs)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), ks, vs, wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True, block_table=tsub,
+                                       block_size=wl.block_size, seqs=seqs)
+    _check_rows(out, lse, ref, ref_lse, rows=_rows_of(wl, seqs), what="prefill paged")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_mixed_chunked_full_size(pkv):
+    """Four 512-query chunks over 0/2K/4K/8K prefixes (two sharing blocks) + 60 decode rows, one call."""
+    wl = W.mixed_chunked(device="cuda")
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc)
+    seqs = [0, 1, 2, 3, 4, 30, 63]
+    ks, vs, tsub = _sub_pool(wl, kc, vc, seqs)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), ks, vs, wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True, block_table=tsub,
+                                       block_size=wl.block_size, seqs=seqs)
+    _check_rows(out, lse, ref, ref_lse, rows=_rows_of(wl, seqs), what="mixed")
+    assert torch.isfinite(out.float()).all()
