@@ -11,17 +11,21 @@
 // Causal alignment: query i of a sequence with Lq queries and Lk keys sees key
 // j iff j <= i + Lk - Lq (the queries are the last Lq positions; prefix reuse).
 //
-// CTA = 128 query rows of one (sequence, query head); 6 warps:
+// CTA = 128 query rows of one (sequence, query head); 10 warps:
 //   warp 0      TMA producer: Q once, then K/V tiles of 128 keys (2 stages each);
-//               packed K/V: one box per head-dim half; paged: one box per page.
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, then O += P V.
-//   warps 2..5  softmax warpgroup, thread r <-> TMEM lane / query row r:
-//               loads its S row, masks, online softmax in the log2 domain
-//               (the running max moves only when it grows by more than 2^8,
-//               so O is rescaled rarely), writes P (bf16) to shared memory in
-//               the 128-byte-swizzled K-major layout the MMA reads, and
-//               finally normalises O and stores the bf16 output and lse.
-// TMEM: S in columns [0,128), O in [128, 128+D).
+//               packed K/V: one box per head-dim half; paged: one box per page,
+//               the tile's block ids fetched by the warp's lanes in parallel.
+//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, then for each
+//               64-key half h of the tile O_h += P_h V_h.
+//   warps 2..9  softmax, two warps per 32 rows: warps 2..5 own keys 0..63 of
+//               every tile, warps 6..9 keys 64..127.  Each half is its own
+//               online-softmax stream with its own O accumulator, so the halves
+//               never synchronise inside the key loop; they are merged once in
+//               the epilogue (log2-sum-exp weights), like two KV splits.  The
+//               running max moves only when it grows by more than 2^8, so O is
+//               rescaled rarely.  P (bf16) goes to shared memory in the
+//               128-byte-swizzled K-major layout the MMA reads.
+// TMEM (512 columns): S in [0,128), O_0 in [128, 128+D), O_1 in [256, 256+D).
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA flags
 // PKV_DEVERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -38,7 +42,9 @@ namespace {
 
 constexpr int kBM = 128;          // query rows per CTA
 constexpr int kBN = 128;          // keys per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -193,9 +199,10 @@ struct Smem {
   static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
   static constexpr int kP = kV + 2 * kTileBytes;        // [128 x 128] bf16 = 32 KB
   static constexpr int kBar = kP + 128 * 128 * 2;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
-  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kXchg = kMisc + 16;              // float m[2][128], l[2][128]
+  static constexpr int kTotal = kXchg + 4 * 128 * 4;
   static constexpr int kAlloc = kTotal + 1024;          // slack to align the base to 1024
 };
 
@@ -207,9 +214,9 @@ enum Bar {
   kVEmpty0 = 7,
   kSFull = 9,
   kSFree = 10,
-  kPFull = 11,
-  kODone = 12,
-  kDrain = 13
+  kPFull0 = 11,  // +half
+  kODone0 = 13,  // +half
+  kDrain = 15
 };
 
 struct Seq {
@@ -283,9 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kVEmpty0 + s), 1);
     }
     mbar_init(bar(kSFull), 1);
-    mbar_init(bar(kSFree), 128);
-    mbar_init(bar(kPFull), 128);
-    mbar_init(bar(kODone), 1);
+    mbar_init(bar(kSFree), kSoftmaxThreads);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(kPFull0 + h), kSoftmaxThreads / 2);
+      mbar_init(bar(kODone0 + h), 1);
+    }
     mbar_init(bar(kDrain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -293,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_holder)),
-                 "r"(256)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -301,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem;        // columns [0, 128)
-  const uint32_t tO = tmem + 128;  // columns [128, 128 + D)
+  const uint32_t tS = tmem;  // columns [0, 128)
+  auto tO = [&](int h) -> uint32_t { return tmem + 128 + 128 * h; };
   const int n_kv = sq.n_kv;
 
   auto fail = [&]() {
@@ -312,54 +321,77 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
+    int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+    const int32_t* bt = kPaged ? p.block_table + (int64_t)b * p.max_blocks : nullptr;
     if (lane == 0) {
-      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-      const int32_t* bt = kPaged ? p.block_table + (int64_t)b * p.max_blocks : nullptr;
       mbar_expect_tx(bar(kQFull), L::kTileBytes);
       for (int a = 0; a < L::kAtoms; ++a)
         tma_load_3d(sbase + L::kQ + a * L::kAtomBytes, &tm_q, a * 64, head, sq.q0 + sq.row0, bar(kQFull));
-      bool ok = true;
-      auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
-        const int key0 = j * kBN;
-        if constexpr (!kPaged) {
+    }
+    const int br = kPaged ? p.box_rows : kBN;
+    const int npages = kBN / br;
+    // Block ids of tile j, one lane per page, fetched together (paged mode).
+    auto tile_slot = [&](int j) -> int {
+      int slot = 0;
+      if (kPaged && lane < npages) {
+        const int pos = j * kBN + lane * br;
+        if (pos < sq.Lk) {
+          int blk = __ldg(bt + pos / p.block_size);
+          if (blk < 0 || blk >= p.num_blocks) {
+            flag_error(p.err, PKV_DEVERR_BLOCK);
+            blk = 0;  // never dereference a bad id; the sequence's result is unspecified
+          }
+          slot = blk * p.block_size + pos % p.block_size;
+        }
+      }
+      return slot;
+    };
+    // Issue tile j of K (t = 0) or V (t = 1) into its stage once the stage is free.
+    auto issue = [&](int t, int j, int my_slot) -> bool {
+      const int s = j & 1, u = j >> 1;
+      const uint32_t empty = bar((t ? kVEmpty0 : kKEmpty0) + s);
+      const uint32_t full = bar((t ? kVFull0 : kKFull0) + s);
+      if (u > 0 && !mbar_wait(empty, (u - 1) & 1, abort_flag)) return false;
+      const uint32_t dst = sbase + (t ? L::kV : L::kK) + s * L::kTileBytes;
+      const CUtensorMap* map = t ? &tm_v : &tm_k;
+      const int key0 = j * kBN;
+      if constexpr (!kPaged) {
+        if (lane == 0) {
           mbar_expect_tx(full, L::kTileBytes);
           for (int a = 0; a < L::kAtoms; ++a) tma_load_3d(dst + a * L::kAtomBytes, map, a * 64, kvh, sq.k0 + key0, full);
-        } else {
-          const int br = p.box_rows;
-          const int npages = kBN / br;
-          int loaded = 0;
-          for (int pg = 0; pg < npages; ++pg)
-            if (key0 + pg * br < sq.Lk) ++loaded;
-          mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
-          for (int pg = 0; pg < npages; ++pg) {
-            const int pos = key0 + pg * br;
-            if (pos >= sq.Lk) break;
-            int blk = __ldg(bt + pos / p.block_size);
-            if (blk < 0 || blk >= p.num_blocks) {
-              flag_error(p.err, PKV_DEVERR_BLOCK);
-              blk = 0;  // never dereference a bad id; the sequence's result is unspecified
-            }
-            const int slot = blk * p.block_size + pos % p.block_size;
+        }
+      } else {
+        int loaded = 0;
+        for (int pg = 0; pg < npages; ++pg)
+          if (key0 + pg * br < sq.Lk) ++loaded;
+        if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
+        for (int pg = 0; pg < loaded; ++pg) {
+          const int slot = __shfl_sync(0xffffffffu, my_slot, pg);
+          if (lane == 0)
             for (int a = 0; a < L::kAtoms; ++a)
               tma_load_3d(dst + a * L::kAtomBytes + pg * br * 128, map, a * 64, kvh, slot, full);
-          }
         }
-      };
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j & 1, u = j >> 1;
-        if (u > 0 && !mbar_wait(bar(kKEmpty0 + s), (u - 1) & 1, abort_flag)) { ok = false; fail(); break; }
-        load_tile(&tm_k, sbase + L::kK + s * L::kTileBytes, bar(kKFull0 + s), j);
-        last_k[s] = u;
-        if (u > 0 && !mbar_wait(bar(kVEmpty0 + s), (u - 1) & 1, abort_flag)) { ok = false; fail(); break; }
-        load_tile(&tm_v, sbase + L::kV + s * L::kTileBytes, bar(kVFull0 + s), j);
-        last_v[s] = u;
       }
-      // every copy this CTA issued has landed before shared memory is released
-      if (!mbar_wait(bar(kQFull), 0, abort_flag)) fail();
-      for (int s = 0; s < 2; ++s) {
-        if (last_k[s] >= 0) mbar_wait(bar(kKFull0 + s), last_k[s] & 1, abort_flag);
-        if (last_v[s] >= 0) mbar_wait(bar(kVFull0 + s), last_v[s] & 1, abort_flag);
-      }
+      (t ? last_v : last_k)[s] = u;
+      return true;
+    };
+    // K runs one tile ahead of V: K(j+1) only waits for S(j-1), so a slow PV
+    // never delays the next QK^T's operand.
+    bool ok = true;
+    int slot_cur = tile_slot(0);
+    ok = issue(0, 0, slot_cur);
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int slot_next = (j + 1 < n_kv) ? tile_slot(j + 1) : 0;
+      if (j + 1 < n_kv && !issue(0, j + 1, slot_next)) { ok = false; break; }
+      if (!issue(1, j, slot_cur)) { ok = false; break; }
+      slot_cur = slot_next;
+    }
+    if (!ok) fail();
+    // every copy this CTA issued has landed before shared memory is released
+    if (!mbar_wait(bar(kQFull), 0, abort_flag)) fail();
+    for (int s = 0; s < 2; ++s) {
+      if (last_k[s] >= 0) mbar_wait(bar(kKFull0 + s), last_k[s] & 1, abort_flag);
+      if (last_v[s] >= 0) mbar_wait(bar(kVFull0 + s), last_v[s] & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -369,7 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) fail();
     bool issued = false;
     auto issue_pv = [&](int t) -> bool {
-      if (!mbar_wait(bar(kPFull), t & 1, abort_flag)) return false;
       if (!mbar_wait(bar(kVFull0 + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
       const uint32_t vbase = sbase + L::kV + (t & 1) * L::kTileBytes;
       // keys at or beyond Lk: zero their V rows (stale or foreign data must not meet P = 0)
@@ -385,18 +416,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t pbase = sbase + L::kP;
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait(bar(kPFull0 + h), t & 1, abort_flag)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t pbase = sbase + L::kP + h * L::kAtomBytes;  // keys 64h..64h+63
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t ad = sw128_desc(pbase + (kk >> 2) * L::kAtomBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, L::kAtomBytes, 1024);
-          mma_bf16(tO, ad, bd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_desc(pbase + kk * 32, 16, 1024);
+            const uint64_t bd = sw128_desc(vbase + (64 * h + 16 * kk) * 128, L::kAtomBytes, 1024);
+            mma_bf16(tO(h), ad, bd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(kODone0 + h));
         }
-        mma_commit(bar(kODone));
-        mma_commit(bar(kVEmpty0 + (t & 1)));
+        __syncwarp();
       }
+      if (lane == 0) mma_commit(bar(kVEmpty0 + (t & 1)));
       __syncwarp();
       return true;
     };
@@ -430,121 +465,140 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(kDrain), 0, abort_flag);
     }
   } else {
-    // ------------------------------------------------------------------ softmax warpgroup
+    // ------------------------------------------------------------------ softmax warps
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;   // keys [64*half, 64*half + 64) of every tile
     const int r = quarter * 32 + lane;  // TMEM lane == query row in the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int qi = sq.row0 + r;
     const int lim = qi + sq.diag;  // last visible key of this row
     const float c = p.scale_log2;
     float m = -INFINITY, l = 0.f;
-    uint8_t* psm = smem + L::kP;
+    uint8_t* psm = smem + L::kP + half * L::kAtomBytes;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       if (!mbar_wait(bar(kSFull), j & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[128];
-      PKV_TMEM_LD32(tS + lane_off + 0, (sr + 0));
-      PKV_TMEM_LD32(tS + lane_off + 32, (sr + 32));
-      PKV_TMEM_LD32(tS + lane_off + 64, (sr + 64));
-      PKV_TMEM_LD32(tS + lane_off + 96, (sr + 96));
+      uint32_t sr[64];
+      PKV_TMEM_LD32(tS + lane_off + 64 * half, (sr + 0));
+      PKV_TMEM_LD32(tS + lane_off + 64 * half + 32, (sr + 32));
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(kSFree));
 
-      const int key0 = j * kBN;
-      const bool need_mask = (key0 + kBN - 1 > sq.row0 + sq.diag) || (key0 + kBN > sq.Lk);
-      float mx = -INFINITY;
+      const int key0 = j * kBN + 64 * half;
+      const bool need_mask = (key0 + 63 > sq.row0 + sq.diag) || (key0 + 64 > sq.Lk);
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (need_mask) {
         const int vis = min(lim, sq.Lk - 1) - key0;  // columns 0..vis are visible
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
+        for (int k = 0; k < 64; ++k) {
           float v = __uint_as_float(sr[k]);
           v = (k <= vis) ? v : -INFINITY;
           sr[k] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          mx4[k & 3] = fmaxf(mx4[k & 3], v);
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < 128; ++k) mx = fmaxf(mx, __uint_as_float(sr[k]));
+        for (int k = 0; k < 64; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(sr[k]));
       }
-      const float mt = mx * c;  // tile max in log2 units (-inf if the row sees nothing here)
+      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
       float m_use = m;
       if (mt > m + kRescaleThreshold || (m == -INFINITY && mt != -INFINITY)) m_use = mt;
       const bool live = m_use != -INFINITY;
       const bool moved = m_use != m;
       const float alpha = (moved && m != -INFINITY) ? fast_exp2(m - m_use) : (moved ? 0.f : 1.f);
       const float nm = live ? -m_use : 0.f;
-      float sum = 0.f;
-      uint32_t pk[64];
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 128; k += 2) {
+      for (int k = 0; k < 64; k += 2) {
         const float p0 = live ? fast_exp2(fmaf(__uint_as_float(sr[k]), c, nm)) : 0.f;
         const float p1 = live ? fast_exp2(fmaf(__uint_as_float(sr[k + 1]), c, nm)) : 0.f;
-        sum += p0 + p1;
+        sum4[(k >> 1) & 3] += p0 + p1;
         pk[k >> 1] = pack_bf16x2(p0, p1);
       }
-      l = l * alpha + sum;
+      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m = m_use;
 
       if (j > 0) {
-        if (!mbar_wait(bar(kODone), (j - 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bar(kODone0 + half), (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // rescale O when this row's reference max moved (warp-collective TMEM access)
+        // rescale O_half when this row's reference max moved (warp-collective TMEM access)
         if (__any_sync(0xffffffffu, moved && alpha != 1.f)) {
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
-            PKV_TMEM_LD32(tO + lane_off + ch * 32, o);
+            PKV_TMEM_LD32(tO(half) + lane_off + ch * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            PKV_TMEM_ST32(tO + lane_off + ch * 32, o);
+            PKV_TMEM_ST32(tO(half) + lane_off + ch * 32, o);
           }
           tmem_wait_st();
         }
       }
-      // P (bf16) into the swizzled K-major tile: row r, keys 8c..8c+7 in chunk c
+      // P (bf16) into this half's swizzled K-major atom: row r, keys 8cc..8cc+7 in chunk cc
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const int atom = ch >> 3, cc = ch & 7;
-        uint4* dst = reinterpret_cast<uint4*>(psm + atom * L::kAtomBytes + r * 128 + ((cc ^ (r & 7)) << 4));
-        *dst = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+      for (int cc = 0; cc < 8; ++cc) {
+        uint4* dst = reinterpret_cast<uint4*>(psm + r * 128 + ((cc ^ (r & 7)) << 4));
+        *dst = make_uint4(pk[cc * 4 + 0], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(kPFull));
+      mbar_arrive(bar(kPFull0 + half));
     }
     if (ok && n_kv > 0) {
-      if (!mbar_wait(bar(kODone), (n_kv - 1) & 1, abort_flag)) ok = false;
+      if (!mbar_wait(bar(kODone0), (n_kv - 1) & 1, abort_flag) ||
+          !mbar_wait(bar(kODone0 + 1), (n_kv - 1) & 1, abort_flag))
+        ok = false;
     }
-    if (!ok) {
+    // exchange (m, l) between the two halves of each row
+    float* xm = reinterpret_cast<float*>(smem + L::kXchg);
+    float* xl = xm + 256;
+    xm[half * 128 + r] = m;
+    xl[half * 128 + r] = ok ? l : 0.f;
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+    if (!ok || *abort_flag) {
       fail();
     } else {
       tc_fence_after();
+      const float m0 = xm[r], m1 = xm[128 + r];
+      const float l0 = xl[r], l1 = xl[128 + r];
+      const float ms = fmaxf(m0, m1);
+      const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - ms);
+      const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - ms);
+      const float lt = l0 * f0 + l1 * f1;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float w0 = f0 * inv, w1 = f1 * inv;
       const bool row_valid = r < sq.rows;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t row = (int64_t)sq.q0 + qi;
       uint16_t* orow = p.out + (row * p.num_heads + head) * D;
+      // this half writes head dims [half*D/2, (half+1)*D/2)
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        PKV_TMEM_LD32(tO + lane_off + ch * 32, o);
+      for (int ch = 0; ch < D / 64; ++ch) {
+        const int col = half * (D / 2) + ch * 32;
+        uint32_t a[32], bb[32];
+        PKV_TMEM_LD32(tO(0) + lane_off + col, a);
+        PKV_TMEM_LD32(tO(1) + lane_off + col, bb);
         tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[k + 0]) * inv, __uint_as_float(o[k + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + ch * 32 + k) = v;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(a[k + e]) * w0 + __uint_as_float(bb[k + e]) * w1;
+            uint4 o4;
+            o4.x = pack_bf16x2(v[0], v[1]);
+            o4.y = pack_bf16x2(v[2], v[3]);
+            o4.z = pack_bf16x2(v[4], v[5]);
+            o4.w = pack_bf16x2(v[6], v[7]);
+            *reinterpret_cast<uint4*>(orow + col + k) = o4;
           }
         }
       }
-      if (row_valid && p.lse != nullptr)
-        p.lse[(int64_t)head * p.total_q + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (half == 0 && row_valid && p.lse != nullptr)
+        p.lse[(int64_t)head * p.total_q + row] = lt > 0.f ? (ms + log2f(lt)) * kLn2 : -INFINITY;
     }
     tc_fence_before();
   }
@@ -552,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
