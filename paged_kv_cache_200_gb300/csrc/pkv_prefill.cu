@@ -61,6 +61,7 @@ struct PrefillParams {
   int32_t num_heads;
   int32_t group;
   int32_t n_qtiles;
+  int32_t batch;
   int32_t route_decode;  // sequences with exactly one query are left to the decode kernels
   float scale_log2;
   int64_t total_q;
@@ -157,6 +158,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D (TMEM) (+)= A (TMEM, M x K, 16-bit pairs per column) * B (shared memory descriptor).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -194,12 +204,11 @@ struct Smem {
   static constexpr int kAtoms = D / 64;                 // 64-element (128-byte) column groups
   static constexpr int kTileBytes = 128 * D * 2;        // a [128 x D] bf16 tile
   static constexpr int kAtomBytes = 128 * 128;          // [128 rows x 128 B]
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;            // 2 stages
+  static constexpr int kQ = 0;                          // 2 buffers (by work item)
+  static constexpr int kK = kQ + 2 * kTileBytes;        // 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
-  static constexpr int kP = kV + 2 * kTileBytes;        // [128 x 128] bf16 = 32 KB
-  static constexpr int kBar = kP + 128 * 128 * 2;
-  static constexpr int kNumBars = 16;
+  static constexpr int kBar = kV + 2 * kTileBytes;
+  static constexpr int kNumBars = 28;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
   static constexpr int kXchg = kMisc + 16;              // float m[2][128], l[2][128]
   static constexpr int kTotal = kXchg + 4 * 128 * 4;
@@ -207,16 +216,26 @@ struct Smem {
 };
 
 enum Bar {
-  kQFull = 0,
-  kKFull0 = 1,   // +stage
-  kKEmpty0 = 3,  // +stage
-  kVFull0 = 5,
-  kVEmpty0 = 7,
-  kSFull = 9,
-  kSFree = 10,
-  kPFull0 = 11,  // +half
-  kODone0 = 13,  // +half
-  kDrain = 15
+  kQFull0 = 0,    // +buffer
+  kQEmpty0 = 2,   // +buffer
+  kKFull0 = 4,    // +stage
+  kKEmpty0 = 6,   // +stage
+  kVFull0 = 8,    // +stage
+  kVEmpty0 = 10,  // +stage
+  kSFull0 = 12,   // +S buffer
+  kSFree0 = 14,   // +S buffer (P of that buffer consumed by both PVs)
+  kDrain = 16,
+  kXchgA = 17,    // softmax threads: (m, l) of both halves published
+  kXchgB = 18,    // softmax threads: O read, exchange slots free again
+  // The next two sets have one barrier per (half, S buffer), i.e. per tile
+  // parity.  A parity wait can only tell "phase k done" from "phase k pending"
+  // when the barrier is never two phases away from the waiter; with one
+  // barrier per tile parity, tile t's phase has tile t-2's before it (known
+  // complete: S(t) needed its buffer) and tile t+2's after it (cannot have
+  // started), so every wait below is unambiguous even when skipped tiles'
+  // phases were never waited on.
+  kPFull0 = 19,   // +2*half + buffer: P of that tile written (softmax -> MMA)
+  kPvDone0 = 23   // +2*half + buffer: O_half += P V of that tile landed (MMA -> softmax)
 };
 
 struct Seq {
@@ -248,6 +267,25 @@ __device__ __forceinline__ Seq seq_info(const PrefillParams& p, int b, int qtile
   return s;
 }
 
+// Work item -> (sequence, query tile, head).  Items are ordered by query tile,
+// last tiles (most keys under causal masking) first, then sequence, then head,
+// so CTAs running side by side share K/V through L2.
+struct Item {
+  int b, qtile, head;
+};
+__device__ __forceinline__ Item item_of(const PrefillParams& p, int it) {
+  const int per = p.batch * p.num_heads;
+  Item x;
+  x.qtile = p.n_qtiles - 1 - it / per;
+  const int rem = it % per;
+  x.b = rem / p.num_heads;
+  x.head = rem % p.num_heads;
+  return x;
+}
+
+// Persistent kernel: one CTA per SM walks the work items blockIdx.x,
+// blockIdx.x + gridDim.x, ...  All roles walk the same list and keep running
+// counters (item, tile) so the barriers' phases continue across items.
 template <int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -258,44 +296,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int head = blockIdx.x;
-  const int qtile = p.n_qtiles - 1 - (int)blockIdx.y;  // longest causal rows first
-  const int b = blockIdx.z;
-  const int kvh = head / p.group;
-
-  const Seq sq = seq_info(p, b, qtile, qtile == 0 && head == 0 && threadIdx.x == 0);
-  if (sq.skip) return;
-
-  // rows that see no key at all: zeros and lse = -inf, nothing else to do
-  if (sq.n_kv == 0) {
-    for (int r = threadIdx.x; r < sq.rows; r += kThreads) {
-      const int64_t row = (int64_t)sq.q0 + sq.row0 + r;
-      uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.num_heads + head) * D);
-      for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
-      if (p.lse) p.lse[(int64_t)head * p.total_q + row] = -INFINITY;
-    }
-    return;
-  }
+  const int n_items = p.n_qtiles * p.batch * p.num_heads;
 
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kQFull), 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kQFull0 + s), 1);
+      mbar_init(bar(kQEmpty0 + s), 1);
       mbar_init(bar(kKFull0 + s), 1);
       mbar_init(bar(kKEmpty0 + s), 1);
       mbar_init(bar(kVFull0 + s), 1);
       mbar_init(bar(kVEmpty0 + s), 1);
-    }
-    mbar_init(bar(kSFull), 1);
-    mbar_init(bar(kSFree), kSoftmaxThreads);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(bar(kPFull0 + h), kSoftmaxThreads / 2);
-      mbar_init(bar(kODone0 + h), 1);
+      mbar_init(bar(kSFull0 + s), 1);
+      mbar_init(bar(kSFree0 + s), 1);
+      mbar_init(bar(kPFull0 + s), kSoftmaxThreads / 2);
+      mbar_init(bar(kPFull0 + 2 + s), kSoftmaxThreads / 2);
+      mbar_init(bar(kPvDone0 + s), 1);
+      mbar_init(bar(kPvDone0 + 2 + s), 1);
     }
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kXchgA), kSoftmaxThreads);
+    mbar_init(bar(kXchgB), kSoftmaxThreads);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -310,9 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem;  // columns [0, 128)
-  auto tO = [&](int h) -> uint32_t { return tmem + 128 + 128 * h; };
-  const int n_kv = sq.n_kv;
+  // TMEM columns: S buffers [0,128) and [128,256); O halves [256, 256+D) and [384, 384+D).
+  // P of a tile (bf16 pairs) overwrites the first 32 columns of each half's S columns.
+  auto tS = [&](int sb) -> uint32_t { return tmem + 128 * sb; };
+  auto tO = [&](int h) -> uint32_t { return tmem + 256 + 128 * h; };
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -321,75 +346,87 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-    const int32_t* bt = kPaged ? p.block_table + (int64_t)b * p.max_blocks : nullptr;
-    if (lane == 0) {
-      mbar_expect_tx(bar(kQFull), L::kTileBytes);
-      for (int a = 0; a < L::kAtoms; ++a)
-        tma_load_3d(sbase + L::kQ + a * L::kAtomBytes, &tm_q, a * 64, head, sq.q0 + sq.row0, bar(kQFull));
-    }
-    const int br = kPaged ? p.box_rows : kBN;
-    const int npages = kBN / br;
-    // Block ids of tile j, one lane per page, fetched together (paged mode).
-    auto tile_slot = [&](int j) -> int {
-      int slot = 0;
-      if (kPaged && lane < npages) {
-        const int pos = j * kBN + lane * br;
-        if (pos < sq.Lk) {
-          int blk = __ldg(bt + pos / p.block_size);
-          if (blk < 0 || blk >= p.num_blocks) {
-            flag_error(p.err, PKV_DEVERR_BLOCK);
-            blk = 0;  // never dereference a bad id; the sequence's result is unspecified
-          }
-          slot = blk * p.block_size + pos % p.block_size;
-        }
-      }
-      return slot;
-    };
-    // Issue tile j of K (t = 0) or V (t = 1) into its stage once the stage is free.
-    auto issue = [&](int t, int j, int my_slot) -> bool {
-      const int s = j & 1, u = j >> 1;
-      const uint32_t empty = bar((t ? kVEmpty0 : kKEmpty0) + s);
-      const uint32_t full = bar((t ? kVFull0 : kKFull0) + s);
-      if (u > 0 && !mbar_wait(empty, (u - 1) & 1, abort_flag)) return false;
-      const uint32_t dst = sbase + (t ? L::kV : L::kK) + s * L::kTileBytes;
-      const CUtensorMap* map = t ? &tm_v : &tm_k;
-      const int key0 = j * kBN;
-      if constexpr (!kPaged) {
-        if (lane == 0) {
-          mbar_expect_tx(full, L::kTileBytes);
-          for (int a = 0; a < L::kAtoms; ++a) tma_load_3d(dst + a * L::kAtomBytes, map, a * 64, kvh, sq.k0 + key0, full);
-        }
-      } else {
-        int loaded = 0;
-        for (int pg = 0; pg < npages; ++pg)
-          if (key0 + pg * br < sq.Lk) ++loaded;
-        if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
-        for (int pg = 0; pg < loaded; ++pg) {
-          const int slot = __shfl_sync(0xffffffffu, my_slot, pg);
-          if (lane == 0)
-            for (int a = 0; a < L::kAtoms; ++a)
-              tma_load_3d(dst + a * L::kAtomBytes + pg * br * 128, map, a * 64, kvh, slot, full);
-        }
-      }
-      (t ? last_v : last_k)[s] = u;
-      return true;
-    };
-    // K runs one tile ahead of V: K(j+1) only waits for S(j-1), so a slow PV
-    // never delays the next QK^T's operand.
+    int last_k[2] = {-1, -1}, last_v[2] = {-1, -1}, last_q[2] = {-1, -1};
+    int g = 0, uq = 0;  // tiles and work items issued by this CTA
     bool ok = true;
-    int slot_cur = tile_slot(0);
-    ok = issue(0, 0, slot_cur);
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int slot_next = (j + 1 < n_kv) ? tile_slot(j + 1) : 0;
-      if (j + 1 < n_kv && !issue(0, j + 1, slot_next)) { ok = false; break; }
-      if (!issue(1, j, slot_cur)) { ok = false; break; }
-      slot_cur = slot_next;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item x = item_of(p, it);
+      const Seq sq = seq_info(p, x.b, x.qtile, false);
+      if (sq.skip || sq.n_kv == 0) continue;
+      const int kvh = x.head / p.group;
+      const int32_t* bt = kPaged ? p.block_table + (int64_t)x.b * p.max_blocks : nullptr;
+      const int qb = uq & 1, qu = uq >> 1;
+      if (qu > 0 && !mbar_wait(bar(kQEmpty0 + qb), (qu - 1) & 1, abort_flag)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_expect_tx(bar(kQFull0 + qb), L::kTileBytes);
+        for (int a = 0; a < L::kAtoms; ++a)
+          tma_load_3d(sbase + L::kQ + qb * L::kTileBytes + a * L::kAtomBytes, &tm_q, a * 64, x.head,
+                      sq.q0 + sq.row0, bar(kQFull0 + qb));
+      }
+      last_q[qb] = qu;
+      const int br = kPaged ? p.box_rows : kBN;
+      const int npages = kBN / br;
+      auto tile_slot = [&](int j) -> int {  // block ids of local tile j, one lane per page
+        int slot = 0;
+        if (kPaged && lane < npages) {
+          const int pos = j * kBN + lane * br;
+          if (pos < sq.Lk) {
+            int blk = __ldg(bt + pos / p.block_size);
+            if (blk < 0 || blk >= p.num_blocks) {
+              flag_error(p.err, PKV_DEVERR_BLOCK);
+              blk = 0;  // never dereference a bad id; the sequence's result is unspecified
+            }
+            slot = blk * p.block_size + pos % p.block_size;
+          }
+        }
+        return slot;
+      };
+      auto issue = [&](int t, int j, int my_slot) -> bool {  // t = 0: K, 1: V; local tile j
+        const int gg = g + j;
+        const int s = gg & 1, u = gg >> 1;
+        const uint32_t empty = bar((t ? kVEmpty0 : kKEmpty0) + s);
+        const uint32_t full = bar((t ? kVFull0 : kKFull0) + s);
+        if (u > 0 && !mbar_wait(empty, (u - 1) & 1, abort_flag)) return false;
+        const uint32_t dst = sbase + (t ? L::kV : L::kK) + s * L::kTileBytes;
+        const CUtensorMap* map = t ? &tm_v : &tm_k;
+        const int key0 = j * kBN;
+        if constexpr (!kPaged) {
+          if (lane == 0) {
+            mbar_expect_tx(full, L::kTileBytes);
+            for (int a = 0; a < L::kAtoms; ++a)
+              tma_load_3d(dst + a * L::kAtomBytes, map, a * 64, kvh, sq.k0 + key0, full);
+          }
+        } else {
+          int loaded = 0;
+          for (int pg = 0; pg < npages; ++pg)
+            if (key0 + pg * br < sq.Lk) ++loaded;
+          if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
+          for (int pg = 0; pg < loaded; ++pg) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, pg);
+            if (lane == 0)
+              for (int a = 0; a < L::kAtoms; ++a)
+                tma_load_3d(dst + a * L::kAtomBytes + pg * br * 128, map, a * 64, kvh, slot, full);
+          }
+        }
+        (t ? last_v : last_k)[s] = u;
+        return true;
+      };
+      // K runs one tile ahead of V within the item
+      int slot_cur = tile_slot(0);
+      if (!issue(0, 0, slot_cur)) { ok = false; break; }
+      for (int j = 0; j < sq.n_kv && ok; ++j) {
+        const int slot_next = (j + 1 < sq.n_kv) ? tile_slot(j + 1) : 0;
+        if (j + 1 < sq.n_kv && !issue(0, j + 1, slot_next)) { ok = false; break; }
+        if (!issue(1, j, slot_cur)) { ok = false; break; }
+        slot_cur = slot_next;
+      }
+      g += sq.n_kv;
+      ++uq;
     }
     if (!ok) fail();
     // every copy this CTA issued has landed before shared memory is released
-    if (!mbar_wait(bar(kQFull), 0, abort_flag)) fail();
     for (int s = 0; s < 2; ++s) {
+      if (last_q[s] >= 0) mbar_wait(bar(kQFull0 + s), last_q[s] & 1, abort_flag);
       if (last_k[s] >= 0) mbar_wait(bar(kKFull0 + s), last_k[s] & 1, abort_flag);
       if (last_v[s] >= 0) mbar_wait(bar(kVFull0 + s), last_v[s] & 1, abort_flag);
     }
@@ -397,14 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);
     constexpr uint32_t kIdescPV = make_idesc(kBM, D, true);
-    bool ok = mbar_wait(bar(kQFull), 0, abort_flag);
-    if (!ok) fail();
-    bool issued = false;
-    auto issue_pv = [&](int t) -> bool {
+    bool ok = true, issued = false;
+    int g = 0, uq = 0;
+    // O_h += P_h V_h for global tile t (local index jt within its item, whose keys end at Lk)
+    auto issue_pv = [&](int t, int jt, int Lk) -> bool {
       if (!mbar_wait(bar(kVFull0 + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
       const uint32_t vbase = sbase + L::kV + (t & 1) * L::kTileBytes;
       // keys at or beyond Lk: zero their V rows (stale or foreign data must not meet P = 0)
-      const int valid = sq.Lk - t * kBN;
+      const int valid = Lk - jt * kBN;
       if (valid < kBN) {
         uint8_t* vs = smem + L::kV + (t & 1) * L::kTileBytes;
         const int first = valid > 0 ? valid : 0;
@@ -417,46 +454,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait(bar(kPFull0 + h), t & 1, abort_flag)) return false;
+        if (!mbar_wait(bar(kPFull0 + 2 * h + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t pbase = sbase + L::kP + h * L::kAtomBytes;  // keys 64h..64h+63
+          const uint32_t pa = tS(t & 1) + 64 * h;  // P_h: 32 columns of bf16 pairs = 64 keys
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sw128_desc(pbase + kk * 32, 16, 1024);
             const uint64_t bd = sw128_desc(vbase + (64 * h + 16 * kk) * 128, L::kAtomBytes, 1024);
-            mma_bf16(tO(h), ad, bd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tO(h), pa + 8 * kk, bd, kIdescPV, (jt > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(kODone0 + h));
+          mma_commit(bar(kPvDone0 + 2 * h + (t & 1)));
         }
         __syncwarp();
       }
-      if (lane == 0) mma_commit(bar(kVEmpty0 + (t & 1)));
+      if (lane == 0) {
+        mma_commit(bar(kVEmpty0 + (t & 1)));
+        mma_commit(bar(kSFree0 + (t & 1)));
+      }
       __syncwarp();
       return true;
     };
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j & 1, u = j >> 1;
-      if (!mbar_wait(bar(kKFull0 + s), u & 1, abort_flag)) { ok = false; break; }
-      if (j > 0 && !mbar_wait(bar(kSFree), (j - 1) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t qb = sbase + L::kQ;
-        const uint32_t kb = sbase + L::kK + s * L::kTileBytes;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item x = item_of(p, it);
+      const Seq sq = seq_info(p, x.b, x.qtile, false);
+      if (sq.skip || sq.n_kv == 0) continue;
+      const int qb = uq & 1;
+      if (!mbar_wait(bar(kQFull0 + qb), (uq >> 1) & 1, abort_flag)) { ok = false; break; }
+      for (int j = 0; j < sq.n_kv; ++j) {
+        const int gg = g + j, s = gg & 1;
+        if (!mbar_wait(bar(kKFull0 + s), (gg >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (gg >= 2 && !mbar_wait(bar(kSFree0 + s), ((gg >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t qbase = sbase + L::kQ + qb * L::kTileBytes;
+          const uint32_t kbase = sbase + L::kK + s * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
-          mma_bf16(tS, sw128_desc(qb + off, 16, 1024), sw128_desc(kb + off, 16, 1024), kIdescQK,
-                   kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
+            mma_bf16(tS(s), sw128_desc(qbase + off, 16, 1024), sw128_desc(kbase + off, 16, 1024), kIdescQK,
+                     kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(kSFull0 + s));
+          mma_commit(bar(kKEmpty0 + s));
+          if (j == sq.n_kv - 1) mma_commit(bar(kQEmpty0 + qb));
         }
-        mma_commit(bar(kSFull));
-        mma_commit(bar(kKEmpty0 + s));
+        __syncwarp();
+        issued = true;
+        if (j > 0 && !issue_pv(gg - 1, j - 1, sq.Lk)) { ok = false; break; }
       }
-      __syncwarp();
-      issued = true;
-      if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+      if (ok && !issue_pv(g + sq.n_kv - 1, sq.n_kv - 1, sq.Lk)) ok = false;
+      g += sq.n_kv;
+      ++uq;
     }
-    if (ok && n_kv > 0 && !issue_pv(n_kv - 1)) ok = false;
     if (!ok) fail();
     // drain: all MMAs this thread issued have completed before TMEM is released
     if (issued) {
@@ -470,62 +519,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;   // keys [64*half, 64*half + 64) of every tile
     const int r = quarter * 32 + lane;  // TMEM lane == query row in the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int qi = sq.row0 + r;
-    const int lim = qi + sq.diag;  // last visible key of this row
     const float c = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    uint8_t* psm = smem + L::kP + half * L::kAtomBytes;
+    float* xm = reinterpret_cast<float*>(smem + L::kXchg);
+    float* xl = xm + 256;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait(bar(kSFull), j & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[64];
-      PKV_TMEM_LD32(tS + lane_off + 64 * half, (sr + 0));
-      PKV_TMEM_LD32(tS + lane_off + 64 * half + 32, (sr + 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(kSFree));
-
-      const int key0 = j * kBN + 64 * half;
-      const bool need_mask = (key0 + 63 > sq.row0 + sq.diag) || (key0 + 64 > sq.Lk);
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (need_mask) {
-        const int vis = min(lim, sq.Lk - 1) - key0;  // columns 0..vis are visible
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          float v = __uint_as_float(sr[k]);
-          v = (k <= vis) ? v : -INFINITY;
-          sr[k] = __float_as_uint(v);
-          mx4[k & 3] = fmaxf(mx4[k & 3], v);
+    int g = 0, ux = 0;  // tiles and work items (with keys) processed
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item x = item_of(p, it);
+      const Seq sq = seq_info(p, x.b, x.qtile, x.qtile == 0 && x.head == 0 && half == 0 && r == 0);
+      if (sq.skip) continue;
+      const int qi = sq.row0 + r;
+      const int64_t row = (int64_t)sq.q0 + qi;
+      const bool row_valid = r < sq.rows;
+      uint16_t* orow = p.out + (row * p.num_heads + x.head) * D;
+      if (sq.n_kv == 0) {
+        // rows that see no key: zeros and lse = -inf
+        if (row_valid) {
+          for (int cc = half * (D / 16); cc < (half + 1) * (D / 16); ++cc)
+            reinterpret_cast<uint4*>(orow)[cc] = make_uint4(0, 0, 0, 0);
+          if (half == 0 && p.lse) p.lse[(int64_t)x.head * p.total_q + row] = -INFINITY;
         }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 64; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(sr[k]));
+        continue;
       }
-      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
-      float m_use = m;
-      if (mt > m + kRescaleThreshold || (m == -INFINITY && mt != -INFINITY)) m_use = mt;
-      const bool live = m_use != -INFINITY;
-      const bool moved = m_use != m;
-      const float alpha = (moved && m != -INFINITY) ? fast_exp2(m - m_use) : (moved ? 0.f : 1.f);
-      const float nm = live ? -m_use : 0.f;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
-#pragma unroll
-      for (int k = 0; k < 64; k += 2) {
-        const float p0 = live ? fast_exp2(fmaf(__uint_as_float(sr[k]), c, nm)) : 0.f;
-        const float p1 = live ? fast_exp2(fmaf(__uint_as_float(sr[k + 1]), c, nm)) : 0.f;
-        sum4[(k >> 1) & 3] += p0 + p1;
-        pk[k >> 1] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-      m = m_use;
-
-      if (j > 0) {
-        if (!mbar_wait(bar(kODone0 + half), (j - 1) & 1, abort_flag)) { ok = false; break; }
+      const int lim = qi + sq.diag;  // last visible key of this row
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < sq.n_kv; ++j) {
+        const int gg = g + j, sb = gg & 1;
+        if (!mbar_wait(bar(kSFull0 + sb), (gg >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // rescale O_half when this row's reference max moved (warp-collective TMEM access)
-        if (__any_sync(0xffffffffu, moved && alpha != 1.f)) {
+        uint32_t sr[64];
+        PKV_TMEM_LD32(tS(sb) + lane_off + 64 * half, (sr + 0));
+        PKV_TMEM_LD32(tS(sb) + lane_off + 64 * half + 32, (sr + 32));
+        tmem_wait_ld();
+
+        const int key0 = j * kBN + 64 * half;
+        const bool need_mask = (key0 + 63 > sq.row0 + sq.diag) || (key0 + 64 > sq.Lk);
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (need_mask) {
+          const int vis = min(lim, sq.Lk - 1) - key0;  // columns 0..vis are visible
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            float v = __uint_as_float(sr[k]);
+            v = (k <= vis) ? v : -INFINITY;
+            sr[k] = __float_as_uint(v);
+            mx4[k & 3] = fmaxf(mx4[k & 3], v);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(sr[k]));
+        }
+        const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+        float m_use = m;
+        if (mt > m + kRescaleThreshold || (m == -INFINITY && mt != -INFINITY)) m_use = mt;
+        const bool live = m_use != -INFINITY;
+        const bool moved = m_use != m;
+        const float alpha = (moved && m != -INFINITY) ? fast_exp2(m - m_use) : (moved ? 0.f : 1.f);
+        const float nm = live ? -m_use : 0.f;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          const float p0 = live ? fast_exp2(fmaf(__uint_as_float(sr[k]), c, nm)) : 0.f;
+          const float p1 = live ? fast_exp2(fmaf(__uint_as_float(sr[k + 1]), c, nm)) : 0.f;
+          sum4[(k >> 1) & 3] += p0 + p1;
+          pk[k >> 1] = pack_bf16x2(p0, p1);
+        }
+        l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+        m = m_use;
+
+        // rescale O_half when this row's reference max moved (warp-collective TMEM access);
+        // the previous tile's PV must have landed first
+        if (j > 0 && __any_sync(0xffffffffu, moved && alpha != 1.f)) {
+          const int tp = gg - 1;  // previous tile
+          if (!mbar_wait(bar(kPvDone0 + 2 * half + (tp & 1)), (tp >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
@@ -535,34 +602,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
             PKV_TMEM_ST32(tO(half) + lane_off + ch * 32, o);
           }
-          tmem_wait_st();
         }
+        // P_half (bf16 pairs) over the first 32 of this half's S columns
+        PKV_TMEM_ST32(tS(sb) + lane_off + 64 * half, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kPFull0 + 2 * half + sb));
       }
-      // P (bf16) into this half's swizzled K-major atom: row r, keys 8cc..8cc+7 in chunk cc
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint4* dst = reinterpret_cast<uint4*>(psm + r * 128 + ((cc ^ (r & 7)) << 4));
-        *dst = make_uint4(pk[cc * 4 + 0], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(kPFull0 + half));
-    }
-    if (ok && n_kv > 0) {
-      if (!mbar_wait(bar(kODone0), (n_kv - 1) & 1, abort_flag) ||
-          !mbar_wait(bar(kODone0 + 1), (n_kv - 1) & 1, abort_flag))
+      if (!ok) break;
+      const int glast = g + sq.n_kv - 1;
+      if (!mbar_wait(bar(kPvDone0 + (glast & 1)), (glast >> 1) & 1, abort_flag) ||
+          !mbar_wait(bar(kPvDone0 + 2 + (glast & 1)), (glast >> 1) & 1, abort_flag)) {
         ok = false;
-    }
-    // exchange (m, l) between the two halves of each row
-    float* xm = reinterpret_cast<float*>(smem + L::kXchg);
-    float* xl = xm + 256;
-    xm[half * 128 + r] = m;
-    xl[half * 128 + r] = ok ? l : 0.f;
-    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-    if (!ok || *abort_flag) {
-      fail();
-    } else {
+        break;
+      }
       tc_fence_after();
+      // exchange (m, l) between the two halves of each row
+      xm[half * 128 + r] = m;
+      xl[half * 128 + r] = l;
+      mbar_arrive(bar(kXchgA));
+      if (!mbar_wait(bar(kXchgA), ux & 1, abort_flag)) { ok = false; break; }
       const float m0 = xm[r], m1 = xm[128 + r];
       const float l0 = xl[r], l1 = xl[128 + r];
       const float ms = fmaxf(m0, m1);
@@ -571,9 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = l0 * f0 + l1 * f1;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float w0 = f0 * inv, w1 = f1 * inv;
-      const bool row_valid = r < sq.rows;
-      const int64_t row = (int64_t)sq.q0 + qi;
-      uint16_t* orow = p.out + (row * p.num_heads + head) * D;
       // this half writes head dims [half*D/2, (half+1)*D/2)
 #pragma unroll
       for (int ch = 0; ch < D / 64; ++ch) {
@@ -598,8 +654,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (half == 0 && row_valid && p.lse != nullptr)
-        p.lse[(int64_t)head * p.total_q + row] = lt > 0.f ? (ms + log2f(lt)) * kLn2 : -INFINITY;
+        p.lse[(int64_t)x.head * p.total_q + row] = lt > 0.f ? (ms + log2f(lt)) * kLn2 : -INFINITY;
+      // both halves have read O (and the exchange slots) before the next item overwrites them
+      tc_fence_before();
+      mbar_arrive(bar(kXchgB));
+      if (!mbar_wait(bar(kXchgB), ux & 1, abort_flag)) { ok = false; break; }
+      g += sq.n_kv;
+      ++ux;
     }
+    if (!ok) fail();
     tc_fence_before();
   }
 
@@ -684,7 +747,8 @@ int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
-  dim3 grid(p.num_heads, p.n_qtiles, batch);
+  const int64_t items = (int64_t)p.n_qtiles * batch * p.num_heads;
+  const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
   kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, p);
   return launch_status();
 }
@@ -764,6 +828,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.num_heads = num_heads;
   p.group = num_heads / num_kv_heads;
   p.n_qtiles = (max_len_q + kBM - 1) / kBM;
+  p.batch = batch;
   p.route_decode = route ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.total_q = total_q;

@@ -22,9 +22,11 @@ def pkv():
 
 
 def _packed(pkv, wl):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = pkv.paged_attn_varlen(wl.q, wl.k, wl.v, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.max_len_q,
-                                     wl.max_len_k, scale=wl.scale, return_lse=True)
+                                     wl.max_len_k, scale=wl.scale, return_lse=True, err_flag=err)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     return out, lse
 
 
@@ -66,10 +68,12 @@ def _write_new_tokens(pkv, wl):
 
 def _paged(pkv, wl, kc, vc):
     shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = pkv.paged_attn_varlen(wl.q, kc.view(shape4), vc.view(shape4), wl.cu_seqlens_q, wl.cu_seqlens_k,
                                      wl.max_len_q, wl.max_len_k, block_table=wl.block_table, scale=wl.scale,
-                                     return_lse=True)
+                                     return_lse=True, err_flag=err)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     return out, lse
 
 
