@@ -63,6 +63,7 @@ struct PrefillParams {
   int32_t n_qtiles;
   int32_t batch;
   int32_t route_decode;  // sequences with exactly one query are left to the decode kernels
+  int32_t* item_counter; // work-item counter, zero at launch
   float scale_log2;
   int64_t total_q;
   uint16_t* out;
@@ -208,35 +209,46 @@ struct Smem {
   static constexpr int kK = kQ + 2 * kTileBytes;        // 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
   static constexpr int kBar = kV + 2 * kTileBytes;
-  static constexpr int kNumBars = 28;
-  static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
-  static constexpr int kXchg = kMisc + 16;              // float m[2][128], l[2][128]
+  static constexpr int kNumBars = 34;
+  static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag, 4 ring slots
+  static constexpr int kXchg = kMisc + 32;              // float m[2][128], l[2][128]
   static constexpr int kTotal = kXchg + 4 * 128 * 4;
   static constexpr int kAlloc = kTotal + 1024;          // slack to align the base to 1024
 };
 
+constexpr int kRing = 4;  // work-item ring slots
+
+// mbarrier indices (each one distinct; checked below).
 enum Bar {
-  kQFull0 = 0,    // +buffer
-  kQEmpty0 = 2,   // +buffer
-  kKFull0 = 4,    // +stage
-  kKEmpty0 = 6,   // +stage
-  kVFull0 = 8,    // +stage
-  kVEmpty0 = 10,  // +stage
-  kSFull0 = 12,   // +S buffer
-  kSFree0 = 14,   // +S buffer (P of that buffer consumed by both PVs)
-  kDrain = 16,
-  kXchgA = 17,    // softmax threads: (m, l) of both halves published
-  kXchgB = 18,    // softmax threads: O read, exchange slots free again
+  kQFull0 = 0,       // +buffer (2)
+  kQEmpty0 = 2,      // +buffer (2)
+  kKFull0 = 4,       // +stage (2)
+  kKEmpty0 = 6,      // +stage (2)
+  kVFull0 = 8,       // +stage (2)
+  kVEmpty0 = 10,     // +stage (2)
+  kSFull0 = 12,      // +S buffer (2)
+  kRingFull0 = 14,   // +slot (4): a work item index published by the producer
+  kDrain = 18,
+  kXchgA = 19,       // softmax threads: (m, l) of both halves published
+  kXchgB = 20,       // softmax threads: O read, exchange slots free again
   // The next two sets have one barrier per (half, S buffer), i.e. per tile
   // parity.  A parity wait can only tell "phase k done" from "phase k pending"
   // when the barrier is never two phases away from the waiter; with one
   // barrier per tile parity, tile t's phase has tile t-2's before it (known
-  // complete: S(t) needed its buffer) and tile t+2's after it (cannot have
-  // started), so every wait below is unambiguous even when skipped tiles'
-  // phases were never waited on.
-  kPFull0 = 19,   // +2*half + buffer: P of that tile written (softmax -> MMA)
-  kPvDone0 = 23   // +2*half + buffer: O_half += P V of that tile landed (MMA -> softmax)
+  // complete: S(t) was issued after PV(t-2)) and tile t+2's after it (cannot
+  // have started), so every wait below is unambiguous even when skipped
+  // tiles' phases were never waited on.
+  kPFull0 = 21,      // +2*half + buffer (4): P of that tile written (softmax -> MMA)
+  kPvDone0 = 25,     // +2*half + buffer (4): O_half += P V of that tile landed (MMA -> softmax)
+  kRingEmpty0 = 29,  // +slot (4): the MMA warp and the 8 softmax warps have read the slot
+  kBarCount = 33
 };
+static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kKEmpty0 == kKFull0 + 2 &&
+                  kVFull0 == kKEmpty0 + 2 && kVEmpty0 == kVFull0 + 2 && kSFull0 == kVEmpty0 + 2 &&
+                  kRingFull0 == kSFull0 + 2 && kDrain == kRingFull0 + kRing && kXchgA == kDrain + 1 &&
+                  kXchgB == kXchgA + 1 && kPFull0 == kXchgB + 1 && kPvDone0 == kPFull0 + 4 &&
+                  kRingEmpty0 == kPvDone0 + 4 && kBarCount == kRingEmpty0 + kRing,
+              "mbarrier index ranges must not overlap");
 
 struct Seq {
   int q0, Lq, k0, Lk, row0, rows, diag, n_kv;
@@ -266,6 +278,8 @@ __device__ __forceinline__ Seq seq_info(const PrefillParams& p, int b, int qtile
   s.n_kv = kmax < 0 ? 0 : min(kmax / kBN + 1, kv_tiles);
   return s;
 }
+
+static_assert(Smem<128>::kNumBars >= kBarCount && Smem<64>::kNumBars >= kBarCount, "too few mbarrier slots");
 
 // Work item -> (sequence, query tile, head).  Items are ordered by query tile,
 // last tiles (most keys under causal masking) first, then sequence, then head,
@@ -311,13 +325,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kVFull0 + s), 1);
       mbar_init(bar(kVEmpty0 + s), 1);
       mbar_init(bar(kSFull0 + s), 1);
-      mbar_init(bar(kSFree0 + s), 1);
       mbar_init(bar(kPFull0 + s), kSoftmaxThreads / 2);
       mbar_init(bar(kPFull0 + 2 + s), kSoftmaxThreads / 2);
       mbar_init(bar(kPvDone0 + s), 1);
       mbar_init(bar(kPvDone0 + 2 + s), 1);
     }
     mbar_init(bar(kDrain), 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(bar(kRingFull0 + r), 1);
+      mbar_init(bar(kRingEmpty0 + r), 1 + (kSoftmaxThreads / 32));
+    }
     mbar_init(bar(kXchgA), kSoftmaxThreads);
     mbar_init(bar(kXchgB), kSoftmaxThreads);
     *abort_flag = 0;
@@ -343,16 +360,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1;
     flag_error(p.err, PKV_DEVERR_TIMEOUT);
   };
+  // Work items are handed out dynamically, longest first (item_of orders
+  // them), through a global counter; the producer warp claims them and
+  // publishes each one that has work into a 4-slot ring that the MMA and
+  // softmax warps read in order.  -1 ends the list.
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);
+  // Consumer side: item of the u-th ring entry (or -1, also on timeout).
+  auto ring_get = [&](int u) -> int {
+    const int slot = u & (kRing - 1);
+    if (!mbar_wait(bar(kRingFull0 + slot), (u / kRing) & 1, abort_flag)) return -1;
+    const int it = ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kRingEmpty0 + slot));
+    return it;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     int last_k[2] = {-1, -1}, last_v[2] = {-1, -1}, last_q[2] = {-1, -1};
-    int g = 0, uq = 0;  // tiles and work items issued by this CTA
+    int g = 0, uq = 0, ur = 0;  // tiles, items with keys, ring entries
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    auto publish = [&](int it) -> bool {
+      const int slot = ur & (kRing - 1);
+      if (ur >= kRing && !mbar_wait(bar(kRingEmpty0 + slot), ((ur / kRing) - 1) & 1, abort_flag)) return false;
+      if (lane == 0) {
+        ring[slot] = it;
+        mbar_arrive(bar(kRingFull0 + slot));
+      }
+      __syncwarp();
+      ++ur;
+      return true;
+    };
+    while (ok) {
+      int it = 0;
+      if (lane == 0) it = atomicAdd(p.item_counter, 1);
+      it = __shfl_sync(0xffffffffu, it, 0);
+      if (it >= n_items) break;
       const Item x = item_of(p, it);
-      const Seq sq = seq_info(p, x.b, x.qtile, false);
-      if (sq.skip || sq.n_kv == 0) continue;
+      const Seq sq = seq_info(p, x.b, x.qtile, x.qtile == 0 && x.head == 0 && lane == 0);
+      if (sq.skip) continue;
+      if (!publish(it)) { ok = false; break; }
+      if (sq.n_kv == 0) continue;
       const int kvh = x.head / p.group;
       const int32_t* bt = kPaged ? p.block_table + (int64_t)x.b * p.max_blocks : nullptr;
       const int qb = uq & 1, qu = uq >> 1;
@@ -423,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       g += sq.n_kv;
       ++uq;
     }
+    if (ok && !publish(-1)) ok = false;
     if (!ok) fail();
     // every copy this CTA issued has landed before shared memory is released
     for (int s = 0; s < 2; ++s) {
@@ -467,23 +516,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      if (lane == 0) {
-        mma_commit(bar(kVEmpty0 + (t & 1)));
-        mma_commit(bar(kSFree0 + (t & 1)));
-      }
+      if (lane == 0) mma_commit(bar(kVEmpty0 + (t & 1)));
       __syncwarp();
       return true;
     };
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int u = 0; ok; ++u) {
+      const int it = ring_get(u);
+      if (it < 0) break;
       const Item x = item_of(p, it);
       const Seq sq = seq_info(p, x.b, x.qtile, false);
-      if (sq.skip || sq.n_kv == 0) continue;
+      if (sq.n_kv == 0) continue;
       const int qb = uq & 1;
       if (!mbar_wait(bar(kQFull0 + qb), (uq >> 1) & 1, abort_flag)) { ok = false; break; }
       for (int j = 0; j < sq.n_kv; ++j) {
         const int gg = g + j, s = gg & 1;
         if (!mbar_wait(bar(kKFull0 + s), (gg >> 1) & 1, abort_flag)) { ok = false; break; }
-        if (gg >= 2 && !mbar_wait(bar(kSFree0 + s), ((gg >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+        // S(gg) overwrites buffer s, whose P(gg-2) the PV issued just before
+        // reads: tcgen05.mma operations from one thread execute in issue
+        // order, so no wait for that PV's completion is needed here.
         tc_fence_after();
         if (lane == 0) {
           const uint32_t qbase = sbase + L::kQ + qb * L::kTileBytes;
@@ -524,10 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xl = xm + 256;
     bool ok = true;
     int g = 0, ux = 0;  // tiles and work items (with keys) processed
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int u = 0; ok; ++u) {
+      const int it = ring_get(u);
+      if (it < 0) break;
       const Item x = item_of(p, it);
-      const Seq sq = seq_info(p, x.b, x.qtile, x.qtile == 0 && x.head == 0 && half == 0 && r == 0);
-      if (sq.skip) continue;
+      const Seq sq = seq_info(p, x.b, x.qtile, false);
       const int qi = sq.row0 + r;
       const int64_t row = (int64_t)sq.q0 + qi;
       const bool row_valid = r < sq.rows;
@@ -676,16 +727,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Varlen prep: compacts the sequences that have exactly one query (decode rows
 // of a mixed batch) into items[0..*count); the prefill kernel skips them and
 // the split-KV decode kernels serve them, one CTA per (split, kv head, item).
+// It also resets the prefill kernel's work-item counter.
 __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __restrict__ cu_q, int batch,
-                                                           int32_t* __restrict__ items, int32_t* __restrict__ count) {
+                                                           int32_t* __restrict__ items, int32_t* __restrict__ count,
+                                                           int32_t* __restrict__ item_counter) {
   __shared__ int n;
-  if (threadIdx.x == 0) n = 0;
-  __syncthreads();
-  for (int b = threadIdx.x; b < batch; b += blockDim.x) {
-    if (__ldg(cu_q + b + 1) - __ldg(cu_q + b) == 1) items[atomicAdd(&n, 1)] = b;
+  if (threadIdx.x == 0) {
+    n = 0;
+    *item_counter = 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0) *count = n;
+  if (items != nullptr) {
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+      if (__ldg(cu_q + b + 1) - __ldg(cu_q + b) == 1) items[atomicAdd(&n, 1)] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *count = n;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -696,10 +754,12 @@ struct VarlenWs {
   size_t count_off, items_off, decode_off, total;
 };
 
+// [0, 256): the prefill work-item counter and the routed-row count; then the
+// routed row list and the decode partials (paged mode only).
 VarlenWs varlen_ws_layout(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k, bool route) {
-  VarlenWs w{0, 0, 0, 0};
+  VarlenWs w{0, 0, 0, 256};
   if (!route || batch <= 0) return w;
-  w.count_off = 0;
+  w.count_off = 4;
   w.items_off = 256;
   w.decode_off = w.items_off + (((size_t)batch * 4 + 255) / 256) * 256;
   w.total = w.decode_off + varlen_decode_workspace(batch, num_heads, num_kv_heads, head_dim, max_len_k);
@@ -838,11 +898,12 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   cudaStream_t st = as_stream(stream);
   int32_t* count = nullptr;
   int32_t* items = nullptr;
+  p.item_counter = static_cast<int32_t*>(workspace);
   if (route) {
     count = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.count_off);
     items = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.items_off);
-    varlen_prep_kernel<<<1, 1024, 0, st>>>(cu_seqlens_q, batch, items, count);
   }
+  varlen_prep_kernel<<<1, route ? 1024 : 32, 0, st>>>(cu_seqlens_q, batch, items, count, p.item_counter);
   int rc;
   if (head_dim == 128)
     rc = paged ? launch_prefill<128, true>(mq, mk, mv, p, batch, st) : launch_prefill<128, false>(mq, mk, mv, p, batch, st);
