@@ -42,7 +42,6 @@ constexpr int kGroupTok = 16;       // positions per warp step
 constexpr int kMaxGroup = 8;        // query heads per kv head handled by one CTA
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFp8Bias = 1.329227995784916e36f;  // 2^120
 
 struct DecodeParams {
   const uint16_t* q;
@@ -100,26 +99,40 @@ __device__ __forceinline__ int attended_length(const DecodeParams& p, int b, boo
   return len;
 }
 
-template <int kChunks>
-__device__ __forceinline__ int swz(int row, int chunk) {
-  if constexpr (kChunks >= 8) {
-    return chunk ^ (row & 7);
-  } else {
-    return chunk ^ ((row >> 1) & 3);
+// Shared-memory layout of one staged 16-position tile of K or V (one kv head):
+// TMA boxes of 16 rows x kBoxRow bytes, 128-byte swizzle for 128-byte rows
+// (16-byte chunk c of row r at chunk c ^ (r & 7)), 64-byte swizzle for
+// 64-byte rows (chunk c ^ ((r >> 1) & 3)); a 256-byte bf16 row is two boxes.
+template <int kRowBytes>
+struct TileLayout {
+  static constexpr int kBoxRow = kRowBytes >= 128 ? 128 : kRowBytes;
+  static constexpr int kBoxes = kRowBytes / kBoxRow;
+  static constexpr int kBoxBytes = kGroupTok * kBoxRow;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kChunksPerBox = kBoxRow / 16;
+  static constexpr int kSwizzle = kBoxRow;  // 128 or 64 bytes
+  __device__ __forceinline__ static int offset(int row, int chunk) {
+    const int box = chunk / kChunksPerBox;
+    const int cc = chunk % kChunksPerBox;
+    const int sw = kChunksPerBox == 8 ? (cc ^ (row & 7)) : (cc ^ ((row >> 1) & 3));
+    return box * kBoxBytes + row * kBoxRow + sw * 16;
   }
-}
+};
 
 template <int D, bool kFp8, int kStages>
-__global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
+    paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                              const DecodeParams p) {
   constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one position, one kv head
-  constexpr int kChunks = kRowBytes / 16;
-  constexpr int kTileBytes = kGroupTok * kRowBytes;
-  constexpr int kWarpStageBytes = 2 * kTileBytes;
+  using TL = TileLayout<kRowBytes>;
+  constexpr int kTileBytes = TL::kTileBytes;
+  constexpr int kStageBytes = 2 * kTileBytes;     // K then V
+  constexpr int kWarpBytes = kStages * kStageBytes;
   constexpr int kDT = D / 16;
-  constexpr int kItems = kGroupTok * kChunks / 32;  // 16-byte copies per lane per tensor
-  static_assert(kItems >= 1, "tile too small");
+  constexpr int kBoxElems = TL::kBoxRow / (kFp8 ? 1 : 2);
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int split = blockIdx.x;
@@ -136,12 +149,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(cons
   const int t_end = min(t_begin + p.split_tokens, len);
   const int n_groups = t_end > t_begin ? (t_end - t_begin + kGroupTok - 1) / kGroupTok : 0;
   const int my_groups = n_groups > warp ? (n_groups - warp + kDecWarps - 1) / kDecWarps : 0;
-
-  const int64_t slot_bytes = (int64_t)p.num_kv_heads * kRowBytes;
-  const uint8_t* kbase = p.k_cache + (int64_t)kvh * kRowBytes;
-  const uint8_t* vbase = p.v_cache + (int64_t)kvh * kRowBytes;
   const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
-  uint8_t* wsm = smem + warp * kStages * kWarpStageBytes;
+
+  uint8_t* wsm = smem + warp * kWarpBytes;
+  const uint32_t wsm_u32 = smem_u32(wsm);
+  // one mbarrier per stage of this warp, after all warps' stages
+  const uint32_t bar0 = smem_u32(smem + kDecWarps * kWarpBytes) + warp * kStages * 8;
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
 
   // ---- Q as the B operand (n = head lane/4 of this group, k = head dim) ----
   uint32_t qf[kDT][2];
@@ -164,6 +182,32 @@ __global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(cons
       }
     }
   }
+  // FP8 cache: the MMAs run in f16 (E4M3 widens to f16 exactly).  Q goes from
+  // bf16 to f16 scaled by a power of two 2^-e chosen so that its largest
+  // magnitude stays below 2^14 (no overflow); 2^e is folded into the logit scale.
+  float scale_log2 = p.scale_log2;
+  if constexpr (kFp8) {
+    float qmax = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kDT; ++kk)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        qmax = fmaxf(qmax, fabsf(__uint_as_float(qf[kk][h2] << 16)));
+        qmax = fmaxf(qmax, fabsf(__uint_as_float(qf[kk][h2] & 0xFFFF0000u)));
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+    int e = 0;
+    if (qmax > 16384.f) e = (int)ceilf(log2f(qmax / 16384.f));  // qmax <= 2^14 * 2^e
+    const float qs = exp2f((float)-e);
+    scale_log2 *= exp2f((float)e);
+#pragma unroll
+    for (int kk = 0; kk < kDT; ++kk)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+        qf[kk][h2] = pack_f16x2(__uint_as_float(qf[kk][h2] << 16) * qs,
+                                __uint_as_float(qf[kk][h2] & 0xFFFF0000u) * qs);
+  }
 
   auto block_of = [&](int pos0, bool report) -> int {
     const int blk = __ldg(bt + pos0 / p.block_size);
@@ -174,26 +218,30 @@ __global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(cons
     return blk;
   };
 
+  // Stage i's copies: one TMA box per 128-byte (or 64-byte) column slice of K
+  // and of V; a bad block id issues nothing and just completes the phase.
   auto issue = [&](int i) {
-    if (i < my_groups) {
-      const int g = warp + i * kDecWarps;
-      const int pos0 = t_begin + g * kGroupTok;
-      const int blk = block_of(pos0, lane == 0);
-      const int64_t slot0 = (int64_t)blk * p.block_size + pos0 % p.block_size;
-      uint8_t* st = wsm + (i % kStages) * kWarpStageBytes;
+    if (i >= my_groups) return;
+    const int g = warp + i * kDecWarps;
+    const int pos0 = t_begin + g * kGroupTok;
+    const int blk = block_of(pos0, lane == 0);
+    if (lane == 0) {
+      const int st = i % kStages;
+      const uint32_t bar = bar0 + 8 * st;
+      const uint32_t dst = wsm_u32 + st * kStageBytes;
+      fence_proxy_async_smem();  // order earlier generic writes (V tail zeroing) before the async copies
+      if (blk >= 0) {
+        const int slot0 = blk * p.block_size + pos0 % p.block_size;
+        mbar_expect_tx(bar, kStageBytes);
 #pragma unroll
-      for (int u = 0; u < kItems; ++u) {
-        const int item = lane + 32 * u;
-        const int row = item / kChunks;
-        const int ch = item % kChunks;
-        const bool valid = blk >= 0 && pos0 + row < t_end;
-        const int64_t off = valid ? (slot0 + row) * slot_bytes + ch * 16 : 0;
-        const uint32_t dst = smem_u32(st + row * kRowBytes + swz<kChunks>(row, ch) * 16);
-        cp_async_16(dst, kbase + off, valid ? 16u : 0u);
-        cp_async_16(dst + kTileBytes, vbase + off, valid ? 16u : 0u);
+        for (int bx = 0; bx < TL::kBoxes; ++bx) {
+          tma_load_3d(dst + bx * TL::kBoxBytes, &tm_k, bx * kBoxElems, kvh, slot0, bar);
+          tma_load_3d(dst + kTileBytes + bx * TL::kBoxBytes, &tm_v, bx * kBoxElems, kvh, slot0, bar);
+        }
+      } else {
+        mbar_arrive(bar);
       }
     }
-    cp_async_commit();
   };
 
   float o[kDT][4];
@@ -204,117 +252,141 @@ __global__ void __launch_bounds__(kDecThreads, 2) paged_decode_split_kernel(cons
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i) issue(i);
 
+  int consumed = 0;
   for (int i = 0; i < my_groups; ++i) {
-    cp_async_wait<kStages - 2>();
-    __syncwarp();
+    const int st = i % kStages;
+    if (!mbar_wait(bar0 + 8 * st, (i / kStages) & 1, nullptr)) {
+      if (lane == 0) flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      break;
+    }
+    consumed = i + 1;
     const int g = warp + i * kDecWarps;
     const int pos0 = t_begin + g * kGroupTok;
     const bool blk_ok = block_of(pos0, false) >= 0;
-    const uint8_t* st = wsm + (i % kStages) * kWarpStageBytes;
-    const uint32_t ks = smem_u32(st);
+    uint8_t* stp = wsm + st * kStageBytes;
+    const uint32_t ks = smem_u32(stp);
     const uint32_t vs = ks + kTileBytes;
-
-    // ---- S^T = K Q^T (16 positions x 8 heads) ----
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int csel = lane >> 4;
-      if constexpr (!kFp8) {
-#pragma unroll
-        for (int kk = 0; kk < kDT; ++kk) {
-          uint32_t a0, a1, a2, a3;
-          ldmatrix_x4(ks + row * kRowBytes + swz<kChunks>(row, 2 * kk + csel) * 16, a0, a1, a2, a3);
-          mma_bf16_16816(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-        }
-      } else {
-#pragma unroll
-        for (int pp = 0; pp < kDT / 2; ++pp) {
-          uint32_t r0, r1, r2, r3;
-          ldmatrix_x4(ks + row * kRowBytes + swz<kChunks>(row, 2 * pp + csel) * 16, r0, r1, r2, r3);
-          const uint32_t lo0 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x1404u));
-          const uint32_t hi0 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x3424u));
-          const uint32_t lo1 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x1404u));
-          const uint32_t hi1 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x3424u));
-          mma_bf16_16816(s, lo0, lo1, hi0, hi1, qf[2 * pp][0], qf[2 * pp][1]);
-          const uint32_t lo2 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x1404u));
-          const uint32_t hi2 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x3424u));
-          const uint32_t lo3 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x1404u));
-          const uint32_t hi3 = e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x3424u));
-          mma_bf16_16816(s, lo2, lo3, hi2, hi3, qf[2 * pp + 1][0], qf[2 * pp + 1][1]);
-        }
+    const int valid = t_end - pos0;  // rows of this group inside the sequence (may exceed 16)
+    if (blk_ok && valid < kGroupTok) {
+      // rows past the sequence end hold other positions' (or stale) values: zero V there
+      for (int idx = lane; idx < kGroupTok * (kRowBytes / 16); idx += 32) {
+        const int row = idx / (kRowBytes / 16);
+        const int ch = idx % (kRowBytes / 16);
+        if (row >= valid) *reinterpret_cast<uint4*>(stp + kTileBytes + TL::offset(row, ch)) = make_uint4(0, 0, 0, 0);
       }
+      __syncwarp();
     }
 
-    // ---- online softmax (log2 domain); this thread: positions lane/4 (+8), heads 2j, 2j+1 ----
-    const int tok0 = pos0 + (lane >> 2);
-    const bool v0 = blk_ok && tok0 < t_end;
-    const bool v1 = blk_ok && tok0 + 8 < t_end;
-    const float x0 = v0 ? s[0] * p.scale_log2 : -INFINITY;
-    const float x1 = v0 ? s[1] * p.scale_log2 : -INFINITY;
-    const float x2 = v1 ? s[2] * p.scale_log2 : -INFINITY;
-    const float x3 = v1 ? s[3] * p.scale_log2 : -INFINITY;
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    if (blk_ok) {
+      // ---- S^T = K Q^T (16 positions x 8 heads) ----
+      // two independent accumulator chains (even / odd 16-wide slices of the head dim)
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int csel = lane >> 4;
+        if constexpr (!kFp8) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const bool live0 = mn0 != -INFINITY, live1 = mn1 != -INFINITY;
-    const float al0 = live0 ? fast_exp2(m0 - mn0) : 1.f;
-    const float al1 = live1 ? fast_exp2(m1 - mn1) : 1.f;
-    const float p0 = live0 ? fast_exp2(x0 - mn0) : 0.f;
-    const float p1 = live1 ? fast_exp2(x1 - mn1) : 0.f;
-    const float p2 = live0 ? fast_exp2(x2 - mn0) : 0.f;
-    const float p3 = live1 ? fast_exp2(x3 - mn1) : 0.f;
-    m0 = mn0;
-    m1 = mn1;
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
+          for (int kk = 0; kk < kDT; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(ks + TL::offset(row, 2 * kk + csel), a0, a1, a2, a3);
+            mma_bf16_16816((kk & 1) ? s2 : s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+          }
+        } else {
 #pragma unroll
-    for (int t = 0; t < kDT; ++t) {
-      o[t][0] *= al0;
-      o[t][1] *= al1;
-      o[t][2] *= al0;
-      o[t][3] *= al1;
-    }
-    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // positions 0..7 as B (k = pos, n = head)
-    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // positions 8..15
+          for (int pp = 0; pp < kDT / 2; ++pp) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4(ks + TL::offset(row, 2 * pp + csel), r0, r1, r2, r3);
+            mma_f16_16816(s, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
+                          e4m3x2_hi_to_f16x2(r1), qf[2 * pp][0], qf[2 * pp][1]);
+            mma_f16_16816(s2, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
+                          e4m3x2_hi_to_f16x2(r3), qf[2 * pp + 1][0], qf[2 * pp + 1][1]);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[e] += s2[e];
+      }
 
-    // ---- O^T += V^T P^T ----
-    {
-      const int row = (lane & 7) + (lane >> 4) * 8;
-      const int csel = (lane >> 3) & 1;
-      if constexpr (!kFp8) {
+      // ---- online softmax (log2 domain); this thread: positions lane/4 (+8), heads 2j, 2j+1 ----
+      // The reference max m moves only when the tile max exceeds it by more
+      // than 2^8, so O is rescaled rarely; P stays below 2^8.
+      const int tok0 = pos0 + (lane >> 2);
+      const bool v0 = tok0 < t_end;
+      const bool v1 = tok0 + 8 < t_end;
+      const float x0 = v0 ? s[0] * scale_log2 : -INFINITY;
+      const float x1 = v0 ? s[1] * scale_log2 : -INFINITY;
+      const float x2 = v1 ? s[2] * scale_log2 : -INFINITY;
+      const float x3 = v1 ? s[3] * scale_log2 : -INFINITY;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mu0 = (mx0 > m0 + 8.f || (m0 == -INFINITY && mx0 != -INFINITY)) ? mx0 : m0;
+      const float mu1 = (mx1 > m1 + 8.f || (m1 == -INFINITY && mx1 != -INFINITY)) ? mx1 : m1;
+      const bool live0 = mu0 != -INFINITY, live1 = mu1 != -INFINITY;
+      const float p0 = live0 ? fast_exp2(x0 - mu0) : 0.f;
+      const float p1 = live1 ? fast_exp2(x1 - mu1) : 0.f;
+      const float p2 = live0 ? fast_exp2(x2 - mu0) : 0.f;
+      const float p3 = live1 ? fast_exp2(x3 - mu1) : 0.f;
+      if (__any_sync(0xffffffffu, (mu0 != m0 && m0 != -INFINITY) || (mu1 != m1 && m1 != -INFINITY))) {
+        const float al0 = (mu0 != m0 && m0 != -INFINITY) ? fast_exp2(m0 - mu0) : 1.f;
+        const float al1 = (mu1 != m1 && m1 != -INFINITY) ? fast_exp2(m1 - mu1) : 1.f;
+        l0 *= al0;
+        l1 *= al1;
 #pragma unroll
         for (int t = 0; t < kDT; ++t) {
-          uint32_t a0, a1, a2, a3;
-          ldmatrix_x4_trans(vs + row * kRowBytes + swz<kChunks>(row, 2 * t + csel) * 16, a0, a1, a2, a3);
-          mma_bf16_16816(o[t], a0, a1, a2, a3, pb0, pb1);
+          o[t][0] *= al0;
+          o[t][1] *= al1;
+          o[t][2] *= al0;
+          o[t][3] *= al1;
         }
-      } else {
+      }
+      m0 = mu0;
+      m1 = mu1;
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      // P as the B operand (k = position, n = head): positions 0..7, then 8..15
+      const uint32_t pb0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+
+      // ---- O^T += V^T P^T ----
+      {
+        const int row = (lane & 7) + (lane >> 4) * 8;
+        const int csel = (lane >> 3) & 1;
+        if constexpr (!kFp8) {
 #pragma unroll
-        for (int pp = 0; pp < kDT / 2; ++pp) {
-          uint32_t r0, r1, r2, r3;
-          ldmatrix_x4_trans(vs + row * kRowBytes + swz<kChunks>(row, 2 * pp + csel) * 16, r0, r1, r2, r3);
-          // r: bytes (pos 2j, dim 2u), (2j, 2u+1), (2j+1, 2u), (2j+1, 2u+1); split even / odd dims
-          mma_bf16_16816(o[2 * pp], e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x2404u)),
-                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x2404u)),
-                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x2404u)),
-                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x2404u)), pb0, pb1);
-          mma_bf16_16816(o[2 * pp + 1], e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r0, 0u, 0x3414u)),
-                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r1, 0u, 0x3414u)),
-                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r2, 0u, 0x3414u)),
-                         e4m3x2_hi_bytes_to_bf16x2_scaled(prmt(r3, 0u, 0x3414u)), pb0, pb1);
+          for (int t = 0; t < kDT; ++t) {
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(vs + TL::offset(row, 2 * t + csel), a0, a1, a2, a3);
+            mma_bf16_16816(o[t], a0, a1, a2, a3, pb0, pb1);
+          }
+        } else {
+#pragma unroll
+          for (int pp = 0; pp < kDT / 2; ++pp) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4_trans(vs + TL::offset(row, 2 * pp + csel), r0, r1, r2, r3);
+            // r: bytes (pos 2j, dim 2u), (2j, 2u+1), (2j+1, 2u), (2j+1, 2u+1); reorder to
+            // (2j,2u), (2j+1,2u) | (2j,2u+1), (2j+1,2u+1) and widen: even dims, then odd dims
+            const uint32_t t0 = prmt(r0, 0u, 0x3120u), t1 = prmt(r1, 0u, 0x3120u);
+            const uint32_t t2 = prmt(r2, 0u, 0x3120u), t3 = prmt(r3, 0u, 0x3120u);
+            mma_f16_16816(o[2 * pp], e4m3x2_lo_to_f16x2(t0), e4m3x2_lo_to_f16x2(t1), e4m3x2_lo_to_f16x2(t2),
+                          e4m3x2_lo_to_f16x2(t3), pb0, pb1);
+            mma_f16_16816(o[2 * pp + 1], e4m3x2_hi_to_f16x2(t0), e4m3x2_hi_to_f16x2(t1), e4m3x2_hi_to_f16x2(t2),
+                          e4m3x2_hi_to_f16x2(t3), pb0, pb1);
+          }
         }
       }
     }
-    __syncwarp();
+    __syncwarp();  // every lane is done with this stage before it is refilled
     issue(i + kStages - 1);
   }
+  // copies issued but never consumed (only after a timeout) land before the CTA exits
+  for (int i = consumed; i < min(my_groups, consumed + kStages - 1); ++i)
+    mbar_wait(bar0 + 8 * (i % kStages), (i / kStages) & 1, nullptr);
 
   // ---- merge the four warps of the CTA ----
-  cp_async_wait<0>();
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -467,12 +539,18 @@ SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, i
 }
 
 template <int D, bool kFp8>
-int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, cudaStream_t st) {
-  constexpr int kStages = kFp8 ? 6 : 3;
+int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t num_slots, cudaStream_t st) {
+  constexpr int kStages = kFp8 ? 4 : 3;  // FP8: 3 CTAs (12 warps) per SM; bf16: 2 CTAs
   constexpr int kRowBytes = D * (kFp8 ? 1 : 2);
-  constexpr int kSmemPipe = kDecWarps * kStages * 2 * kGroupTok * kRowBytes;
+  using TL = TileLayout<kRowBytes>;
+  constexpr int kSmemPipe = kDecWarps * kStages * 2 * TL::kTileBytes + kDecWarps * kStages * 8;
   constexpr int kSmemMerge = (2 * kDecWarps * kMaxGroup + kDecWarps * kMaxGroup * D) * (int)sizeof(float);
-  constexpr int kSmem = kSmemPipe > kSmemMerge ? kSmemPipe : kSmemMerge;
+  constexpr int kSmem = (kSmemPipe > kSmemMerge ? kSmemPipe : kSmemMerge) + 1024;
+  CUtensorMap mk, mv;
+  const int box_elems = TL::kBoxRow / (kFp8 ? 1 : 2);
+  if (!make_tmap_3d(&mk, p.k_cache, kFp8 ? 1 : 2, num_slots, p.num_kv_heads, D, box_elems, kGroupTok, TL::kSwizzle) ||
+      !make_tmap_3d(&mv, p.v_cache, kFp8 ? 1 : 2, num_slots, p.num_kv_heads, D, box_elems, kGroupTok, TL::kSwizzle))
+    return PKV_ERR_CUDA;
   auto kern = paged_decode_split_kernel<D, kFp8, kStages>;
   static bool attr_set[64] = {false};  // per instantiation and device
   int dev = 0;
@@ -484,7 +562,7 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, cudaStr
     attr_set[dev] = true;
   }
   dim3 grid(pl.max_splits, p.num_kv_heads, batch);
-  kern<<<grid, kDecThreads, kSmem, st>>>(p);
+  kern<<<grid, kDecThreads, kSmem, st>>>(mk, mv, p);
   if (pl.max_splits > 1) {
     const int64_t rows = (int64_t)batch * p.num_heads;
     paged_decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p, batch);
@@ -547,8 +625,8 @@ extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const v
   p.split_tokens = pl.split_tokens;
   p.max_splits = pl.max_splits;
   const bool fp8 = cache_dtype == PKV_FP8_E4M3;
-  p.scale_log2 = scale * kLog2e * (fp8 ? k_scale * kFp8Bias : 1.f);
-  p.v_mul = fp8 ? v_scale * kFp8Bias : 1.f;
+  p.scale_log2 = scale * kLog2e * (fp8 ? k_scale : 1.f);
+  p.v_mul = fp8 ? v_scale : 1.f;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   if (pl.max_splits > 1) {
@@ -560,8 +638,10 @@ extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const v
   p.lse_head_stride = 1;
   p.lse_row_stride = num_heads;
   cudaStream_t st = as_stream(stream);
-  if (head_dim == 128) return fp8 ? launch_decode<128, true>(p, batch, pl, st) : launch_decode<128, false>(p, batch, pl, st);
-  return fp8 ? launch_decode<64, true>(p, batch, pl, st) : launch_decode<64, false>(p, batch, pl, st);
+  const int64_t ns = (int64_t)num_blocks * block_size;
+  if (head_dim == 128)
+    return fp8 ? launch_decode<128, true>(p, batch, pl, ns, st) : launch_decode<128, false>(p, batch, pl, ns, st);
+  return fp8 ? launch_decode<64, true>(p, batch, pl, ns, st) : launch_decode<64, false>(p, batch, pl, ns, st);
 }
 
 namespace pkv {
@@ -611,8 +691,9 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.cu_k = cu_k;
   p.lse_head_stride = total_q;
   p.lse_row_stride = 1;
-  if (head_dim == 128) return launch_decode<128, false>(p, batch, pl, st);
-  return launch_decode<64, false>(p, batch, pl, st);
+  const int64_t ns = (int64_t)num_blocks * block_size;
+  if (head_dim == 128) return launch_decode<128, false>(p, batch, pl, ns, st);
+  return launch_decode<64, false>(p, batch, pl, ns, st);
 }
 
 }  // namespace pkv

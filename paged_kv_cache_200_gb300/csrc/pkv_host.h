@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "pkv.h"
@@ -18,6 +19,12 @@ int device_sm_count();
 inline int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Tensor map over a [rows, heads, dim] array of `elt_bytes`-byte elements
+// (bf16 = 2, e4m3 = 1), boxes of box_inner elements x 1 head x box_rows rows,
+// swizzle of 128 or 64 bytes (or 0 for none).  False if the driver refuses it.
+bool make_tmap_3d(CUtensorMap* map, const void* base, int elt_bytes, int64_t rows, int heads, int dim,
+                  int box_inner, int box_rows, int swizzle_bytes);
 
 // Decode kernels serving the single-query sequences of a paged varlen batch.
 size_t varlen_decode_workspace(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k);

@@ -28,11 +28,7 @@
 // TMEM (512 columns): S in [0,128), O_0 in [128, 128+D), O_1 in [256, 256+D).
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA flags
 // PKV_DEVERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cmath>
-#include <mutex>
 
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -45,7 +41,6 @@ constexpr int kBN = 128;          // keys per tile
 constexpr int kThreads = 320;
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -75,58 +70,6 @@ struct PrefillParams {
 // PTX wrappers: mbarrier, TMA, tcgen05
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false on deadline expiry or when another role aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort_flag) return false;
-      const uint64_t now = globaltimer();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > kWaitNs) {
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -766,33 +709,6 @@ VarlenWs varlen_ws_layout(int batch, int num_heads, int num_kv_heads, int head_d
   return w;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// [rows, heads, dim] bf16, box = 64 elements x 1 head x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int dim, int box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, bool kPaged>
 int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillParams& p,
                    int batch, cudaStream_t st) {
@@ -866,9 +782,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   CUtensorMap mq, mk, mv;
   const int64_t kv_rows = paged ? (int64_t)num_blocks * block_size : (int64_t)total_k;
   const int kv_box = paged ? (block_size < 128 ? block_size : 128) : 128;
-  if (!make_map(&mq, q, total_q, num_heads, head_dim, 128) ||
-      !make_map(&mk, k, kv_rows, num_kv_heads, head_dim, kv_box) ||
-      !make_map(&mv, v, kv_rows, num_kv_heads, head_dim, kv_box))
+  // [rows, heads, dim] bf16, boxes of 64 elements x 1 head x box rows, 128-byte swizzle
+  if (!make_tmap_3d(&mq, q, 2, total_q, num_heads, head_dim, 64, 128, 128) ||
+      !make_tmap_3d(&mk, k, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128) ||
+      !make_tmap_3d(&mv, v, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128))
     return PKV_ERR_CUDA;
 
   const bool route = routes_decode(paged, num_heads, num_kv_heads);
