@@ -391,13 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           int loaded = 0;
           for (int pg = 0; pg < npages; ++pg)
             if (key0 + pg * br < sq.Lk) ++loaded;
+          // one lane per page issues that page's boxes (after the byte count is registered)
           if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
-          for (int pg = 0; pg < loaded; ++pg) {
-            const int slot = __shfl_sync(0xffffffffu, my_slot, pg);
-            if (lane == 0)
-              for (int a = 0; a < L::kAtoms; ++a)
-                tma_load_3d(dst + a * L::kAtomBytes + pg * br * 128, map, a * 64, kvh, slot, full);
-          }
+          __syncwarp();
+          if (lane < loaded)
+            for (int a = 0; a < L::kAtoms; ++a)
+              tma_load_3d(dst + a * L::kAtomBytes + lane * br * 128, map, a * 64, kvh, my_slot, full);
+          __syncwarp();
         }
         (t ? last_v : last_k)[s] = u;
         return true;
