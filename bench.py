@@ -144,6 +144,25 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (one replica per rank; no collective on the data path)
+# ---------------------------------------------------------------------------
+
+
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over all ranks (the slowest rank's time); the value itself when not distributed."""
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(bytes_per_rank_step: int, ms_per_step_max: float, world: int) -> float:
+    """Whole-job GB/s: every rank processed its own step's bytes within the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
 
@@ -321,17 +340,12 @@ def run_pkv(args, rank, world, device):
     clocks.start()
     ms, dec_ms = time_decode_steps(step, args.steps, args.warmup)
     clk = clocks.stop()
-    t = torch.tensor([ms], device=device)
+    ms_max = max_over_ranks(ms, device)
     if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         torch.distributed.barrier()
-    ms_max = float(t.item())
 
     e2e_ms, h2d, d2h = time_e2e(step, max(1, min(args.steps, args.e2e_steps)), 3)
-    te = torch.tensor([e2e_ms], device=device)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = max_over_ranks(e2e_ms, device)
 
     also = {}
     if not args.no_extra:
@@ -342,7 +356,7 @@ def run_pkv(args, rank, world, device):
     traffic = profile_traffic("paged_decode_split_bf16_d128")
     result = {
         "metric": METRIC,
-        "value": world * nbytes / (ms_max * 1e-3) / 1e9,
+        "value": job_throughput_gbs(nbytes, ms_max, world),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -376,7 +390,7 @@ def run_pkv(args, rank, world, device):
             "launch_ms": dec_ms,
             "peak_source": pk["source"],
         },
-        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput_gbs(nbytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": step.launches * args.steps,
         "clocks": clk,
