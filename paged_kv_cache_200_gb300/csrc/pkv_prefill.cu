@@ -445,16 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
+      // descriptors differ only in their start-address field (bits 0..13, address >> 4)
+      const uint64_t vdesc = sw128_desc(vbase, L::kAtomBytes, 1024);
       for (int h = 0; h < 2; ++h) {
         if (!mbar_wait(bar(kPFull0 + 2 * h + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t pa = tS(t & 1) + 64 * h;  // P_h: 32 columns of bf16 pairs = 64 keys
+          const uint32_t acc = jt > 0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sw128_desc(vbase + (64 * h + 16 * kk) * 128, L::kAtomBytes, 1024);
-            mma_bf16_ts(tO(h), pa + 8 * kk, bd, kIdescPV, (jt > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tO(h), pa + 8 * kk, vdesc + (uint64_t)(((64 * h + 16 * kk) * 128) >> 4), kIdescPV,
+                        kk > 0 ? 1u : acc);
           mma_commit(bar(kPvDone0 + 2 * h + (t & 1)));
         }
         __syncwarp();
@@ -479,13 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // order, so no wait for that PV's completion is needed here.
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t qbase = sbase + L::kQ + qb * L::kTileBytes;
-          const uint32_t kbase = sbase + L::kK + s * L::kTileBytes;
+          const uint64_t qdesc = sw128_desc(sbase + L::kQ + qb * L::kTileBytes, 16, 1024);
+          const uint64_t kdesc = sw128_desc(sbase + L::kK + s * L::kTileBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::kAtomBytes + (kk & 3) * 32;
-            mma_bf16(tS(s), sw128_desc(qbase + off, 16, 1024), sw128_desc(kbase + off, 16, 1024), kIdescQK,
-                     kk > 0 ? 1u : 0u);
+            const uint64_t off = (uint64_t)(((kk >> 2) * L::kAtomBytes + (kk & 3) * 32) >> 4);
+            mma_bf16(tS(s), qdesc + off, kdesc + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(kSFull0 + s));
           mma_commit(bar(kKEmpty0 + s));
@@ -548,37 +549,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const int key0 = j * kBN + 64 * half;
         const bool need_mask = (key0 + 63 > sq.row0 + sq.diag) || (key0 + 64 > sq.Lk);
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (need_mask) {
           const int vis = min(lim, sq.Lk - 1) - key0;  // columns 0..vis are visible
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            float v = __uint_as_float(sr[k]);
-            v = (k <= vis) ? v : -INFINITY;
-            sr[k] = __float_as_uint(v);
-            mx4[k & 3] = fmaxf(mx4[k & 3], v);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(sr[k]));
+          for (int k = 0; k < 64; ++k) sr[k] = (k <= vis) ? sr[k] : __float_as_uint(-INFINITY);
         }
-        const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int k = 0; k < 64; k += 2)
+          mx4[(k >> 1) & 3] = fmax3(mx4[(k >> 1) & 3], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+        const float mt = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c;
         float m_use = m;
         if (mt > m + kRescaleThreshold || (m == -INFINITY && mt != -INFINITY)) m_use = mt;
         const bool live = m_use != -INFINITY;
         const bool moved = m_use != m;
         const float alpha = (moved && m != -INFINITY) ? fast_exp2(m - m_use) : (moved ? 0.f : 1.f);
-        const float nm = live ? -m_use : 0.f;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        // p = 2^(s*c - m) on fp32 pairs; a row that saw no key yet (m = -inf) gives 0
+        const float nm = live ? -m_use : -INFINITY;
+        const uint64_t c2 = f32x2_pack(c, c), nm2 = f32x2_pack(nm, nm);
+        uint64_t sum2[2] = {0ull, 0ull};
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 64; k += 2) {
-          const float p0 = live ? fast_exp2(fmaf(__uint_as_float(sr[k]), c, nm)) : 0.f;
-          const float p1 = live ? fast_exp2(fmaf(__uint_as_float(sr[k + 1]), c, nm)) : 0.f;
-          sum4[(k >> 1) & 3] += p0 + p1;
+          float x0, x1;
+          f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nm2), x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          sum2[(k >> 1) & 1] = fadd2(sum2[(k >> 1) & 1], f32x2_pack(p0, p1));
           pk[k >> 1] = pack_bf16x2(p0, p1);
         }
-        l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+        float s00, s01, s10, s11;
+        f32x2_unpack(sum2[0], s00, s01);
+        f32x2_unpack(sum2[1], s10, s11);
+        l = l * alpha + ((s00 + s01) + (s10 + s11));
         m = m_use;
 
         // rescale O_half when this row's reference max moved (warp-collective TMEM access);
