@@ -173,7 +173,7 @@ enum Bar {
   kRingFull0 = 14,   // +slot (4): a work item index published by the producer
   kDrain = 18,
   kXchgA = 19,       // softmax threads: (m, l) of both halves published
-  kXchgB = 20,       // softmax threads: O read, exchange slots free again
+  kXchgB = 20,       // softmax threads have read O and the exchange slots (MMA waits before the next item's PV)
   // The next two sets have one barrier per (half, S buffer), i.e. per tile
   // parity.  A parity wait can only tell "phase k done" from "phase k pending"
   // when the barrier is never two phases away from the waiter; with one
@@ -431,6 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O_h += P_h V_h for global tile t (local index jt within its item, whose keys end at Lk)
     auto issue_pv = [&](int t, int jt, int Lk) -> bool {
       if (!mbar_wait(bar(kVFull0 + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
+      // the first PV of an item overwrites O: the previous item's epilogue must have read it
+      if (jt == 0 && uq > 0 && !mbar_wait(bar(kXchgB), (uq - 1) & 1, abort_flag)) return false;
       const uint32_t vbase = sbase + L::kV + (t & 1) * L::kTileBytes;
       // keys at or beyond Lk: zero their V rows (stale or foreign data must not meet P = 0)
       const int valid = Lk - jt * kBN;
@@ -651,10 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (half == 0 && row_valid && p.lse != nullptr)
         p.lse[(int64_t)x.head * p.total_q + row] = lt > 0.f ? (ms + log2f(lt)) * kLn2 : -INFINITY;
-      // both halves have read O (and the exchange slots) before the next item overwrites them
+      // this thread has read O and the exchange slots; the MMA thread waits for all of them
+      // before the next item's first PV (so the softmax warps do not wait here)
       tc_fence_before();
       mbar_arrive(bar(kXchgB));
-      if (!mbar_wait(bar(kXchgB), ux & 1, abort_flag)) { ok = false; break; }
       g += sq.n_kv;
       ++ux;
     }
