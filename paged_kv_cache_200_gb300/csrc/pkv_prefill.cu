@@ -11,21 +11,24 @@
 // Causal alignment: query i of a sequence with Lq queries and Lk keys sees key
 // j iff j <= i + Lk - Lq (the queries are the last Lq positions; prefix reuse).
 //
-// CTA = 128 query rows of one (sequence, query head); 10 warps:
-//   warp 0      TMA producer: Q once, then K/V tiles of 128 keys (2 stages each);
-//               packed K/V: one box per head-dim half; paged: one box per page,
-//               the tile's block ids fetched by the warp's lanes in parallel.
+// Persistent kernel, one 320-thread CTA per SM.  A work item is 128 query rows
+// of one (sequence, query head); items are claimed through a global counter,
+// longest first, and published to the CTA's warps through a shared ring.
+//   warp 0      producer: Q once per item (TMA), then K/V tiles of 128 keys
+//               (2 stages each), K one tile ahead of V.  Packed K/V: one TMA
+//               box per head-dim half.  Paged K/V: one box per page and
+//               half, each issued by its own lane, the block ids read two
+//               tiles ahead.
 //   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, then for each
-//               64-key half h of the tile O_h += P_h V_h.
+//               64-key half h of the tile O_h += P_h V_h with P read from TMEM.
 //   warps 2..9  softmax, two warps per 32 rows: warps 2..5 own keys 0..63 of
 //               every tile, warps 6..9 keys 64..127.  Each half is its own
 //               online-softmax stream with its own O accumulator, so the halves
 //               never synchronise inside the key loop; they are merged once in
 //               the epilogue (log2-sum-exp weights), like two KV splits.  The
 //               running max moves only when it grows by more than 2^8, so O is
-//               rescaled rarely.  P (bf16) goes to shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads.
-// TMEM (512 columns): S in [0,128), O_0 in [128, 128+D), O_1 in [256, 256+D).
+//               rescaled rarely.  P (bf16 pairs) overwrites its S columns.
+// TMEM (512 columns): S buffers [0,128) and [128,256); O_0 at 256, O_1 at 384.
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA flags
 // PKV_DEVERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cmath>
@@ -357,20 +360,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_q[qb] = qu;
       const int br = kPaged ? p.box_rows : kBN;
       const int npages = kBN / br;
-      auto tile_slot = [&](int j) -> int {  // block ids of local tile j, one lane per page
-        int slot = 0;
-        if (kPaged && lane < npages) {
-          const int pos = j * kBN + lane * br;
-          if (pos < sq.Lk) {
-            int blk = __ldg(bt + pos / p.block_size);
-            if (blk < 0 || blk >= p.num_blocks) {
-              flag_error(p.err, PKV_DEVERR_BLOCK);
-              blk = 0;  // never dereference a bad id; the sequence's result is unspecified
-            }
-            slot = blk * p.block_size + pos % p.block_size;
-          }
+      // Paged tiles: lane (page pg, head-dim atom at) issues one box; at most
+      // 8 pages x 2 atoms, as block sizes are multiples of 16.
+      const int pg = lane % npages, at = lane / npages;
+      const bool box_lane = lane < npages * L::kAtoms;
+      // Block id of this lane's page of local tile j (0 past the keys).  The
+      // table is read two tiles before the id is used, so the load's latency
+      // overlaps the waits in between; tile_slot checks and converts it.
+      auto tile_blk = [&](int j) -> int {
+        int blk = 0;
+        if (kPaged && box_lane && j < sq.n_kv) {
+          const int pos = j * kBN + pg * br;
+          if (pos < sq.Lk) blk = __ldg(bt + pos / p.block_size);
         }
-        return slot;
+        return blk;
+      };
+      auto tile_slot = [&](int j, int blk) -> int {
+        if (!kPaged || !box_lane) return 0;
+        if (blk < 0 || blk >= p.num_blocks) {
+          flag_error(p.err, PKV_DEVERR_BLOCK);
+          blk = 0;  // never dereference a bad id; the sequence's result is unspecified
+        }
+        return blk * p.block_size + (j * kBN + pg * br) % p.block_size;
       };
       auto issue = [&](int t, int j, int my_slot) -> bool {  // t = 0: K, 1: V; local tile j
         const int gg = g + j;
@@ -391,25 +402,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           int loaded = 0;
           for (int pg = 0; pg < npages; ++pg)
             if (key0 + pg * br < sq.Lk) ++loaded;
-          // one lane per page issues that page's boxes (after the byte count is registered)
+          // one lane per (page, atom) issues that box, after the byte count is registered
           if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
           __syncwarp();
-          if (lane < loaded)
-            for (int a = 0; a < L::kAtoms; ++a)
-              tma_load_3d(dst + a * L::kAtomBytes + lane * br * 128, map, a * 64, kvh, my_slot, full);
+          if (box_lane && pg < loaded)
+            tma_load_3d(dst + at * L::kAtomBytes + pg * br * 128, map, at * 64, kvh, my_slot, full);
           __syncwarp();
         }
         (t ? last_v : last_k)[s] = u;
         return true;
       };
       // K runs one tile ahead of V within the item
-      int slot_cur = tile_slot(0);
+      int slot_cur = tile_slot(0, tile_blk(0));
+      int blk_next = tile_blk(1);
       if (!issue(0, 0, slot_cur)) { ok = false; break; }
       for (int j = 0; j < sq.n_kv && ok; ++j) {
-        const int slot_next = (j + 1 < sq.n_kv) ? tile_slot(j + 1) : 0;
+        const int blk_after = tile_blk(j + 2);
+        const int slot_next = (j + 1 < sq.n_kv) ? tile_slot(j + 1, blk_next) : 0;
         if (j + 1 < sq.n_kv && !issue(0, j + 1, slot_next)) { ok = false; break; }
         if (!issue(1, j, slot_cur)) { ok = false; break; }
         slot_cur = slot_next;
+        blk_next = blk_after;
       }
       g += sq.n_kv;
       ++uq;

@@ -85,6 +85,8 @@ PAGED = [
     ([90, 260], [130, 0], 4, 1, 64, 64),
     ([300, 17], [40, 257], 8, 4, 128, 128),
     ([150, 150], [600, 5], 8, 2, 128, 256),
+    ([100, 333], [77, 0], 8, 2, 64, 16),
+    ([250, 3], [200, 600], 16, 4, 128, 64),
 ]
 
 
