@@ -155,7 +155,7 @@ struct Smem {
   static constexpr int kK = kQ + 2 * kTileBytes;        // 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
   static constexpr int kBar = kV + 2 * kTileBytes;
-  static constexpr int kNumBars = 34;
+  static constexpr int kNumBars = 28;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag, 4 ring slots
   static constexpr int kXchg = kMisc + 32;              // float m[2][128], l[2][128]
   static constexpr int kTotal = kXchg + 4 * 128 * 4;
@@ -164,36 +164,37 @@ struct Smem {
 
 constexpr int kRing = 4;  // work-item ring slots
 
-// mbarrier indices (each one distinct; checked below).
+// mbarrier indices (each one distinct; checked below).  K and V stages have
+// no "empty" barriers of their own: a K stage is free once S of its tile is
+// done (kSFull), a V stage once the tile's PV is (kPvDone).  Fewer commits
+// and waits keep the MMA thread, which runs nearly in step with the tensor
+// core, issuing MMAs.
 enum Bar {
   kQFull0 = 0,       // +buffer (2)
   kQEmpty0 = 2,      // +buffer (2)
   kKFull0 = 4,       // +stage (2)
-  kKEmpty0 = 6,      // +stage (2)
-  kVFull0 = 8,       // +stage (2)
-  kVEmpty0 = 10,     // +stage (2)
-  kSFull0 = 12,      // +S buffer (2)
-  kRingFull0 = 14,   // +slot (4): a work item index published by the producer
-  kDrain = 18,
-  kXchgA = 19,       // softmax threads: (m, l) of both halves published
-  kXchgB = 20,       // softmax threads have read O and the exchange slots (MMA waits before the next item's PV)
-  // The next two sets have one barrier per (half, S buffer), i.e. per tile
-  // parity.  A parity wait can only tell "phase k done" from "phase k pending"
-  // when the barrier is never two phases away from the waiter; with one
-  // barrier per tile parity, tile t's phase has tile t-2's before it (known
-  // complete: S(t) was issued after PV(t-2)) and tile t+2's after it (cannot
-  // have started), so every wait below is unambiguous even when skipped
-  // tiles' phases were never waited on.
-  kPFull0 = 21,      // +2*half + buffer (4): P of that tile written (softmax -> MMA)
-  kPvDone0 = 25,     // +2*half + buffer (4): O_half += P V of that tile landed (MMA -> softmax)
-  kRingEmpty0 = 29,  // +slot (4): the MMA warp and the 8 softmax warps have read the slot
-  kBarCount = 33
+  kVFull0 = 6,       // +stage (2)
+  kSFull0 = 8,       // +S buffer (2)
+  kRingFull0 = 10,   // +slot (4): a work item index published by the producer
+  kDrain = 14,
+  kXchgA = 15,       // softmax threads: (m, l) of both halves published
+  kXchgB = 16,       // softmax threads have read O and the exchange slots (MMA waits before the next item's PV)
+  // The next two sets have one barrier per S buffer, i.e. per tile parity.
+  // A parity wait can only tell "phase k done" from "phase k pending" when
+  // the barrier is never two phases away from the waiter; with one barrier
+  // per tile parity, tile t's phase has tile t-2's before it (known complete:
+  // S(t) was issued after PV(t-2)) and tile t+2's after it (cannot have
+  // started), so every wait below is unambiguous even when skipped tiles'
+  // phases were never waited on.
+  kPFull0 = 17,      // +buffer (2): P of that tile written, both halves (softmax -> MMA)
+  kPvDone0 = 19,     // +buffer (2): O += P V of that tile landed (MMA -> softmax, producer)
+  kRingEmpty0 = 21,  // +slot (4): the MMA warp and the 8 softmax warps have read the slot
+  kBarCount = 25
 };
-static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kKEmpty0 == kKFull0 + 2 &&
-                  kVFull0 == kKEmpty0 + 2 && kVEmpty0 == kVFull0 + 2 && kSFull0 == kVEmpty0 + 2 &&
-                  kRingFull0 == kSFull0 + 2 && kDrain == kRingFull0 + kRing && kXchgA == kDrain + 1 &&
-                  kXchgB == kXchgA + 1 && kPFull0 == kXchgB + 1 && kPvDone0 == kPFull0 + 4 &&
-                  kRingEmpty0 == kPvDone0 + 4 && kBarCount == kRingEmpty0 + kRing,
+static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kVFull0 == kKFull0 + 2 &&
+                  kSFull0 == kVFull0 + 2 && kRingFull0 == kSFull0 + 2 && kDrain == kRingFull0 + kRing &&
+                  kXchgA == kDrain + 1 && kXchgB == kXchgA + 1 && kPFull0 == kXchgB + 1 &&
+                  kPvDone0 == kPFull0 + 2 && kRingEmpty0 == kPvDone0 + 2 && kBarCount == kRingEmpty0 + kRing,
               "mbarrier index ranges must not overlap");
 
 struct Seq {
@@ -267,14 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kQFull0 + s), 1);
       mbar_init(bar(kQEmpty0 + s), 1);
       mbar_init(bar(kKFull0 + s), 1);
-      mbar_init(bar(kKEmpty0 + s), 1);
       mbar_init(bar(kVFull0 + s), 1);
-      mbar_init(bar(kVEmpty0 + s), 1);
       mbar_init(bar(kSFull0 + s), 1);
-      mbar_init(bar(kPFull0 + s), kSoftmaxThreads / 2);
-      mbar_init(bar(kPFull0 + 2 + s), kSoftmaxThreads / 2);
+      mbar_init(bar(kPFull0 + s), kSoftmaxThreads);
       mbar_init(bar(kPvDone0 + s), 1);
-      mbar_init(bar(kPvDone0 + 2 + s), 1);
     }
     mbar_init(bar(kDrain), 1);
     for (int r = 0; r < kRing; ++r) {
@@ -386,7 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue = [&](int t, int j, int my_slot) -> bool {  // t = 0: K, 1: V; local tile j
         const int gg = g + j;
         const int s = gg & 1, u = gg >> 1;
-        const uint32_t empty = bar((t ? kVEmpty0 : kKEmpty0) + s);
+        // the stage is free once the MMAs that read it are done: S(gg-2) for K, PV(gg-2) for V
+        const uint32_t empty = t ? bar(kPvDone0 + s) : bar(kSFull0 + s);
         const uint32_t full = bar((t ? kVFull0 : kKFull0) + s);
         if (u > 0 && !mbar_wait(empty, (u - 1) & 1, abort_flag)) return false;
         const uint32_t dst = sbase + (t ? L::kV : L::kK) + s * L::kTileBytes;
@@ -462,21 +460,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // descriptors differ only in their start-address field (bits 0..13, address >> 4)
       const uint64_t vdesc = sw128_desc(vbase, L::kAtomBytes, 1024);
-      for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait(bar(kPFull0 + 2 * h + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        if (lane == 0) {
+      // both halves' P, then all eight PV MMAs and one commit: every wait and
+      // commit the MMA thread runs between MMAs leaves the tensor core idle
+      if (!mbar_wait(bar(kPFull0 + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t acc = jt > 0 ? 1u : 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
           const uint32_t pa = tS(t & 1) + 64 * h;  // P_h: 32 columns of bf16 pairs = 64 keys
-          const uint32_t acc = jt > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ts(tO(h), pa + 8 * kk, vdesc + (uint64_t)(((64 * h + 16 * kk) * 128) >> 4), kIdescPV,
                         kk > 0 ? 1u : acc);
-          mma_commit(bar(kPvDone0 + 2 * h + (t & 1)));
         }
-        __syncwarp();
+        mma_commit(bar(kPvDone0 + (t & 1)));  // also frees V stage t & 1
       }
-      if (lane == 0) mma_commit(bar(kVEmpty0 + (t & 1)));
       __syncwarp();
       return true;
     };
@@ -503,8 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t off = (uint64_t)(((kk >> 2) * L::kAtomBytes + (kk & 3) * 32) >> 4);
             mma_bf16(tS(s), qdesc + off, kdesc + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(kSFull0 + s));
-          mma_commit(bar(kKEmpty0 + s));
+          mma_commit(bar(kSFull0 + s));  // also frees K stage s
           if (j == sq.n_kv - 1) mma_commit(bar(kQEmpty0 + qb));
         }
         __syncwarp();
@@ -602,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous tile's PV must have landed first
         if (j > 0 && __any_sync(0xffffffffu, moved && alpha != 1.f)) {
           const int tp = gg - 1;  // previous tile
-          if (!mbar_wait(bar(kPvDone0 + 2 * half + (tp & 1)), (tp >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(kPvDone0 + (tp & 1)), (tp >> 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
@@ -618,12 +616,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         PKV_TMEM_ST32(tS(sb) + lane_off + 64 * half, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(kPFull0 + 2 * half + sb));
+        mbar_arrive(bar(kPFull0 + sb));
       }
       if (!ok) break;
       const int glast = g + sq.n_kv - 1;
-      if (!mbar_wait(bar(kPvDone0 + (glast & 1)), (glast >> 1) & 1, abort_flag) ||
-          !mbar_wait(bar(kPvDone0 + 2 + (glast & 1)), (glast >> 1) & 1, abort_flag)) {
+      if (!mbar_wait(bar(kPvDone0 + (glast & 1)), (glast >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }

@@ -47,6 +47,9 @@ PACKED = [
     ([256, 513], [256, 513], 16, 2, 64),
     ([700, 5, 1000], [700, 5, 1000], 32, 8, 128),
     ([33, 200], [33, 200], 8, 8, 64),
+    ([50], [50], 2, 1, 128),                                   # one pair of heads, one tile
+    ([10, 3, 1], [0, 1, 7], 4, 2, 128),                        # empty rows, paired heads
+    ([300, 129], [300, 500], 6, 2, 128),                       # odd group: single-CTA path
 ]
 
 
