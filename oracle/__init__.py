@@ -15,6 +15,7 @@ from .pkv_oracle import (  # noqa: F401
     bf16_bits_to_f64,
     cache_values_f64,
     blocks_needed,
+    copy_blocks,
     cu_seqlens_from_lens,
     e4m3_decode,
     e4m3_encode_rne_satfinite,

@@ -233,6 +233,32 @@ def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, cache_dtype: str = "bf1
     return kc, vc
 
 
+def copy_blocks(k_cache, v_cache, block_pairs, block_size: int):
+    """Copy-on-write of shared blocks: block ``dst`` of each cache becomes a copy of block ``src``.
+
+    [CH15] "PagedAttention：メモリを「ページ」で貸し出す": answers generated from
+    one prompt share the blocks of the common part, and a shared block is
+    copied only when it has to be written.  ``k_cache``/``v_cache``:
+    ``[num_slots, Hkv, D]`` (any element type; the copy is of the stored
+    values, bit for bit).  ``block_pairs``: ``[n, 2]`` rows ``(src, dst)``.
+    Every copy reads the caches as they were before the call.  Returns new
+    arrays; the inputs are not modified.
+    """
+    kc0 = np.asarray(k_cache)
+    vc0 = np.asarray(v_cache)
+    kc = np.array(kc0, copy=True)
+    vc = np.array(vc0, copy=True)
+    nb = kc0.shape[0] // block_size
+    for src, dst in np.asarray(block_pairs, dtype=np.int64).reshape(-1, 2):
+        if not (0 <= src < nb and 0 <= dst < nb):
+            raise IndexError(f"block pair ({src}, {dst}) outside the pool of {nb} blocks")
+        rows_s = slice(int(src) * block_size, (int(src) + 1) * block_size)
+        rows_d = slice(int(dst) * block_size, (int(dst) + 1) * block_size)
+        kc[rows_d] = kc0[rows_s]
+        vc[rows_d] = vc0[rows_s]
+    return kc, vc
+
+
 # ---------------------------------------------------------------------------
 # attention (plain definition; [CH15] FlashAttention section: the tiled result
 # equals ordinary attention, so the oracle is ordinary attention)

@@ -442,3 +442,57 @@ def test_fp8_attention_uses_dequantised_values():
         vr = np.stack([vd[table[b][p // 4] * 4 + p % 4] for p in range(L)])
         o, _ = O.attention_rows(O.bf16_bits_to_f64(q[b])[None], kr, vr, 0.3, True)
         assert np.array_equal(out[b], o[0])
+
+
+# ---------------------------------------------------------------------------
+# copy-on-write of shared blocks ([CH15] "PagedAttention：メモリを「ページ」で貸し出す")
+# ---------------------------------------------------------------------------
+
+
+def _pool(nb, bs, hkv, d, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.integers(0, 1 << 16, size=(nb * bs, hkv, d), dtype=np.uint64).astype(np.uint16),
+            rng.integers(0, 1 << 16, size=(nb * bs, hkv, d), dtype=np.uint64).astype(np.uint16))
+
+
+def test_copy_on_write_fork_keeps_the_shared_prefix():
+    # sequence A holds 70 tokens in blocks [3, 0, 6] (block size 32); B forks
+    # from A sharing blocks 3 and 0 and gets a private copy of the partly
+    # filled block 6 in block 5 before either writes token 70
+    bs = 32
+    kc, vc = _pool(8, bs, 2, 16, 11)
+    kc2, vc2 = O.copy_blocks(kc, vc, [[6, 5]], bs)
+    for cache, new in ((kc, kc2), (vc, vc2)):
+        a_rows = O.gather_paged_rows(cache, [3, 0, 6], 70, bs)
+        b_rows = O.gather_paged_rows(new, [3, 0, 5], 70, bs)
+        assert np.array_equal(a_rows, b_rows)
+    # B's next token goes to its private block; A's rows do not change
+    k_new = np.full((1, 2, 16), 0x3F80, dtype=np.uint16)
+    slot_b = O.slot_of([3, 0, 5], 70, bs)
+    kc3, vc3 = O.kv_cache_write(k_new, k_new, kc2, vc2, [slot_b])
+    assert np.array_equal(O.gather_paged_rows(kc3, [3, 0, 6], 71, bs), O.gather_paged_rows(kc, [3, 0, 6], 71, bs))
+    assert np.array_equal(O.gather_paged_rows(kc3, [3, 0, 5], 71, bs)[70], k_new[0])
+
+
+def test_copy_blocks_touches_only_destinations_bitwise():
+    bs = 16
+    kc, vc = _pool(10, bs, 2, 8, 12)
+    kc[5 * bs, 0, 0] = 0x7FC1  # a NaN payload is copied as bits
+    pairs = [[5, 1], [2, 9], [7, 7]]
+    kc2, vc2 = O.copy_blocks(kc, vc, pairs, bs)
+    for cache, new in ((kc, kc2), (vc, vc2)):
+        for blk in range(10):
+            rows = slice(blk * bs, (blk + 1) * bs)
+            src = {1: 5, 9: 2}.get(blk, blk)
+            assert np.array_equal(new[rows], cache[src * bs:(src + 1) * bs])
+    assert kc2[1 * bs, 0, 0] == 0x7FC1
+
+
+def test_copy_blocks_reads_the_cache_as_before_the_call():
+    bs = 4
+    kc, vc = _pool(4, bs, 1, 4, 13)
+    kc2, _ = O.copy_blocks(kc, vc, [[0, 1], [1, 2]], bs)
+    assert np.array_equal(kc2[2 * bs:3 * bs], kc[1 * bs:2 * bs])   # old block 1, not block 0
+    assert np.array_equal(kc2[1 * bs:2 * bs], kc[0:bs])
+    with pytest.raises(IndexError):
+        O.copy_blocks(kc, vc, [[0, 4]], bs)
