@@ -373,6 +373,8 @@ def run_pkv(args, rank, world, device):
                         "new tokens + paged decode attention",
             "batch": wl.batch,
             "attended_tokens": int((wl.lens_before + 1).sum()),
+            # share of the block pool holding tokens (the pool has exactly the blocks the lengths need)
+            "pool_utilisation": float((wl.lens_before + 1).sum()) / float(wl.num_blocks * wl.block_size),
             "bytes_per_step": nbytes,
             "l2": "inputs larger than L2 (%.2f GB of K/V read per step)" % (dec_bytes / 1e9),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -418,7 +420,55 @@ def extra_workloads(pkv, W, device, pk, args):
         torch.cuda.empty_cache()
     if hasattr(pkv, "paged_attn_varlen") and hasattr(pkv.lib(), "pkv_paged_attn_varlen"):
         out.update(prefill_workload(pkv, W, device, pk, args))
+    out.update(copy_workload(pkv, W, device, pk, args))
+    out.update(write_sweep(pkv, device, pk, args))
     return out
+
+
+def copy_workload(pkv, W, device, pk, args):
+    """Copy-on-write of 8192 shared blocks of the decode pool (32 KB per block and cache)."""
+    wl = W.decode_batch(device=device)
+    sh = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    kc, vc = wl.k_cache.view(sh), wl.v_cache.view(sh)
+    rng = np.random.default_rng(1006)
+    n = min(8192, wl.num_blocks // 2)
+    perm = rng.permutation(wl.num_blocks)
+    pairs = torch.from_numpy(np.stack([perm[n:2 * n], perm[:n]], axis=1).astype(np.int32)).to(device)
+    iters = max(10, min(100, args.steps // 20))
+    ms = time_calls(lambda: pkv.copy_blocks(kc, vc, pairs), iters)
+    moved = 2 * 2 * n * kc[0].numel() * kc.element_size()  # K and V, read and write
+    gbs = moved / (ms * 1e-3) / 1e9
+    res = {"copy_blocks": {
+        "workload": f"{n} (src, dst) block pairs of the 64-sequence decode pool, 16-token blocks, 8 kv heads x "
+                    "128 bf16 (32 KB per block and cache), K and V", "ms": ms, "bytes": moved, "GB_per_s": gbs,
+        "frac_of_hbm_peak": gbs / pk["hbm_gbs"], "iters": iters}}
+    del wl, kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+def write_sweep(pkv, device, pk, args):
+    """KV write at 2^14..2^18 tokens (8 kv heads x 128), bf16 and FP8, into a permuted pool of as many slots."""
+    res = {}
+    iters = max(10, min(50, args.steps // 40))
+    g = torch.Generator(device=device).manual_seed(1007)
+    for T in (1 << 14, 1 << 16, 1 << 18):
+        k = torch.randn((T, 8, 128), generator=g, device=device).to(torch.bfloat16)
+        v = torch.randn((T, 8, 128), generator=g, device=device).to(torch.bfloat16)
+        slots = torch.randperm(T, generator=g, device=device).to(torch.int32)
+        for dt in ("bf16", "fp8_e4m3"):
+            cdt = torch.bfloat16 if dt == "bf16" else torch.uint8
+            kc = torch.empty((T, 8, 128), dtype=cdt, device=device)
+            vc = torch.empty_like(kc)
+            ms = time_calls(lambda: pkv.kv_cache_write(k, v, kc, vc, slots, k_inv_scale=0.25, v_inv_scale=0.25),
+                            iters)
+            moved = 2 * T * 8 * 128 * (2 + kc.element_size())  # read bf16, write the cache type; K and V
+            gbs = moved / (ms * 1e-3) / 1e9
+            res[f"write_{T}_{dt}"] = {"tokens": T, "ms": ms, "GB_per_s": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"]}
+            del kc, vc
+        del k, v, slots
+        torch.cuda.empty_cache()
+    return res
 
 
 def causal_pairs(q_lens, k_lens):

@@ -1,12 +1,13 @@
 /*
  * pkv.h -- C ABI of libpkv, paged KV-cache attention for one NVIDIA GB300 (sm_103a).
  *
- * Three operations, in the order a serving layer calls them for one step:
+ * The operations, in the order a serving layer calls them for one step:
  *
  *   pkv_kv_cache_write      scatter each new token's K/V row into the paged cache
  *   pkv_paged_attn_decode   one query token per sequence over its paged cache
  *   pkv_paged_attn_varlen   causal GQA attention over packed variable-length
  *                           sequences, K/V packed or read from the paged cache
+ *   pkv_copy_blocks         copy-on-write of shared cache blocks
  *
  * Sources (web pages, by title and section):
  *   [KVM]  "効率的な KV キャッシュ管理と Attention 計算" (itan.pw): "Triton カーネルによる
@@ -112,6 +113,27 @@ PKV_API int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const void* 
                        void* k_cache, void* v_cache, int32_t cache_dtype, int64_t num_slots,
                        const int32_t* slot_mapping, float k_inv_scale, float v_inv_scale,
                        int32_t* err_flag, void* stream);
+
+/*
+ * Copy-on-write of shared blocks ([CH15] "PagedAttention：メモリを「ページ」で貸し出す":
+ * answers generated from one prompt share the blocks of their common part, and
+ * a shared block is copied only once one of them must write into it).
+ *
+ * For each i in [0, num_pairs), with (src, dst) = (block_pairs[2i], block_pairs[2i+1]):
+ *   block dst of k_cache := block src of k_cache, and the same for v_cache,
+ * byte for byte.  A block is block_bytes bytes (block_size*num_kv_heads*head_dim
+ * elements of the cache's type); block b starts at byte b*block_bytes.
+ *
+ * k_cache, v_cache: the pools, 16-byte aligned; v_cache may be NULL (K only).
+ * block_bytes:   a positive multiple of 16.
+ * block_pairs:   int32 [num_pairs][2] (src, dst).  A pair with a block id outside
+ *                [0, num_blocks) is skipped and flagged (PKV_DEVERR_BLOCK).  Every
+ *                copy must read a block no pair of the same call writes (no dst
+ *                is also a src, no two pairs share a dst); otherwise the result
+ *                is unspecified.  num_pairs == 0 does nothing.
+ */
+PKV_API int pkv_copy_blocks(void* k_cache, void* v_cache, int64_t block_bytes, int32_t num_blocks,
+                            const int32_t* block_pairs, int32_t num_pairs, int32_t* err_flag, void* stream);
 
 /*
  * Workspace bytes pkv_paged_attn_decode needs for these sizes on the current

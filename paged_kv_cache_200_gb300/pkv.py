@@ -44,6 +44,7 @@ _SIGNATURES = {
     "pkv_kv_cache_write": (ctypes.c_int, [
         _c_void_p, _i64, _c_void_p, _i64, _i32, _i32, _i32, _c_void_p, _c_void_p, _i32, _i64,
         _c_void_p, _f32, _f32, _c_void_p, _c_void_p]),
+    "pkv_copy_blocks": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i32, _c_void_p, _i32, _c_void_p, _c_void_p]),
     "pkv_paged_attn_decode_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pkv_paged_attn_decode": (ctypes.c_int, [
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
@@ -166,6 +167,33 @@ def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, k_inv_scale: float = 1.
     st = lib().pkv_kv_cache_write(_ptr(k), k.stride(0), _ptr(v), v.stride(0), T, Hkv, D, _ptr(k_cache),
                                   _ptr(v_cache), _cache_dtype(k_cache), num_slots, _ptr(slot_mapping),
                                   float(k_inv_scale), float(v_inv_scale), _ptr(err_flag), _stream(stream))
+    _check(st)
+
+
+# ---------------------------------------------------------------------------
+# copy-on-write of shared blocks
+# ---------------------------------------------------------------------------
+
+
+def copy_blocks(k_cache, v_cache, block_pairs, err_flag=None, stream=None):
+    """Block ``dst`` of each cache becomes a copy of block ``src``, for each row of ``block_pairs``.
+
+    Caches: ``[num_blocks, block_size, Hkv, D]`` contiguous (bf16 or uint8 E4M3
+    codes); ``v_cache`` may be ``None``.  ``block_pairs``: int32 ``[n, 2]``
+    ``(src, dst)`` on the device; no dst may also be a src of the same call.
+    """
+    _require_cuda(k_cache, block_pairs, *([] if v_cache is None else [v_cache]))
+    if not k_cache.is_contiguous() or (v_cache is not None and
+                                       (not v_cache.is_contiguous() or v_cache.shape != k_cache.shape
+                                        or v_cache.dtype != k_cache.dtype)):
+        raise ValueError("caches must be contiguous and match each other")
+    if block_pairs.dtype != torch.int32 or block_pairs.dim() != 2 or block_pairs.shape[1] != 2 or \
+            not block_pairs.is_contiguous():
+        raise ValueError("block_pairs must be a contiguous int32 [n, 2] tensor")
+    num_blocks = k_cache.shape[0]
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    st = lib().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), block_bytes, num_blocks, _ptr(block_pairs),
+                               block_pairs.shape[0], _ptr(err_flag), _stream(stream))
     _check(st)
 
 

@@ -53,3 +53,16 @@ def test_host_side_argument_validation():
     assert lib.pkv_paged_attn_decode(*args(32, 2, 128, 16)) == 2
     assert lib.pkv_paged_attn_decode(*args(8, 2, 128, 8)) == 2
     assert lib.pkv_paged_attn_decode(*args(8, 3, 128, 16)) == 1
+
+
+def test_copy_blocks_host_validation():
+    pkv = built_library()
+    lib = pkv.lib()
+    nul = ctypes.c_void_p(0)
+    # negative pair count, block bytes not a multiple of 16, empty pool: rejected before any launch
+    assert lib.pkv_copy_blocks(nul, nul, 4096, 8, nul, -1, nul, nul) == 1
+    assert lib.pkv_copy_blocks(nul, nul, 4100, 8, nul, 1, nul, nul) == 1
+    assert lib.pkv_copy_blocks(nul, nul, 4096, 0, nul, 1, nul, nul) == 1
+    # no pairs: nothing to do; pairs without a cache: rejected
+    assert lib.pkv_copy_blocks(nul, nul, 4096, 8, nul, 0, nul, nul) == 0
+    assert lib.pkv_copy_blocks(nul, nul, 4096, 8, nul, 3, nul, nul) == 1
