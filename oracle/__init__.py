@@ -23,6 +23,7 @@ from .pkv_oracle import (  # noqa: F401
     kv_bytes,
     kv_cache_write,
     paged_attn_decode,
+    paged_attn_decode_with_kvcache,
     paged_attn_varlen,
     quantize_to_e4m3,
     request_index,

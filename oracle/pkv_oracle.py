@@ -330,6 +330,27 @@ def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, block_siz
     return out, lse
 
 
+def paged_attn_decode_with_kvcache(q, k_new, v_new, k_cache, v_cache, cache_seqlens_before, block_table,
+                                   block_size: int, scale: float, cache_dtype: str = "bf16", k_scale: float = 1.0,
+                                   v_scale: float = 1.0, k_inv_scale: float = 1.0, v_inv_scale: float = 1.0,
+                                   seqs=None):
+    """Append each sequence's new token to its cache, then decode ([PA] "デコードパス"; [KVM] layer).
+
+    The [PA] example counts cached tokens before the step: sequence ``b``'s new
+    token takes position ``cache_seqlens_before[b]``, i.e. the slot its block
+    table gives for that position ("fits in the held block" or "needs the next
+    block").  [KVM]: the layer writes the step's K/V first and then attends.
+    So: ``kv_cache_write`` at those slots, then ``paged_attn_decode`` over
+    ``cache_seqlens_before + 1`` positions.  Returns ``(out, lse, k_cache, v_cache)``.
+    """
+    lens = np.asarray(cache_seqlens_before, dtype=np.int64)
+    slots = [slot_of(block_table[b], int(lens[b]), block_size) for b in range(len(lens))]
+    kc, vc = kv_cache_write(k_new, v_new, k_cache, v_cache, slots, cache_dtype, k_inv_scale, v_inv_scale)
+    out, lse = paged_attn_decode(q, kc, vc, lens + 1, block_table, block_size, scale, cache_dtype, k_scale,
+                                 v_scale, seqs=seqs)
+    return out, lse, kc, vc
+
+
 def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = True,
                       block_table=None, block_size: int | None = None, kv_dtype: str = "bf16",
                       k_scale: float = 1.0, v_scale: float = 1.0, seqs=None):

@@ -496,3 +496,52 @@ def test_copy_blocks_reads_the_cache_as_before_the_call():
     assert np.array_equal(kc2[1 * bs:2 * bs], kc[0:bs])
     with pytest.raises(IndexError):
         O.copy_blocks(kc, vc, [[0, 4]], bs)
+
+
+# ---------------------------------------------------------------------------
+# decode with the step's append ([PA] "デコードパス" example: lengths before the step)
+# ---------------------------------------------------------------------------
+
+
+def test_decode_with_append_on_the_worked_example():
+    g = _golden("decode_example.json")
+    bs, table = g["block_size"], np.array(g["block_table"])
+    rng = np.random.default_rng(21)
+    Hq, Hkv, D = 4, 2, 8
+    nb = 8
+    kc = _rand_bf16(rng, (nb * bs, Hkv, D))
+    vc = _rand_bf16(rng, (nb * bs, Hkv, D))
+    q = _rand_bf16(rng, (3, Hq, D))
+    k_new = _rand_bf16(rng, (3, Hkv, D))
+    v_new = _rand_bf16(rng, (3, Hkv, D))
+    out, lse, kc2, vc2 = O.paged_attn_decode_with_kvcache(q, k_new, v_new, kc, vc, g["cache_seqlens"], table, bs,
+                                                          0.25)
+    # the new rows land in the slots the page's example implies; nothing else changes
+    slots = g["derived_new_token_slots"]
+    for b, s in enumerate(slots):
+        assert np.array_equal(kc2[s], k_new[b]) and np.array_equal(vc2[s], v_new[b])
+    other = np.setdiff1d(np.arange(nb * bs), slots)
+    assert np.array_equal(kc2[other], kc[other]) and np.array_equal(vc2[other], vc[other])
+    # each sequence attends its cached tokens followed by the new one (plain-Python recomputation)
+    for b, L in enumerate(g["cache_seqlens"]):
+        for h in range(Hq):
+            kvh = h // (Hq // Hkv)
+            keys = [O.bf16_bits_to_f64(kc[O.slot_of(table[b], p, bs), kvh]).tolist() for p in range(L)]
+            vals = [O.bf16_bits_to_f64(vc[O.slot_of(table[b], p, bs), kvh]).tolist() for p in range(L)]
+            keys.append(O.bf16_bits_to_f64(k_new[b, kvh]).tolist())
+            vals.append(O.bf16_bits_to_f64(v_new[b, kvh]).tolist())
+            ref, ref_lse = _brute_attention(O.bf16_bits_to_f64(q[b, h]).tolist(), keys, vals, 0.25)
+            assert np.allclose(out[b, h], ref, rtol=1e-12, atol=1e-12)
+            assert math.isclose(lse[b, h], ref_lse, rel_tol=1e-12, abs_tol=1e-12)
+
+
+def test_decode_with_append_on_an_empty_cache_returns_the_new_value():
+    rng = np.random.default_rng(22)
+    kc = _rand_bf16(rng, (4 * 16, 1, 8))
+    vc = _rand_bf16(rng, (4 * 16, 1, 8))
+    q = _rand_bf16(rng, (1, 2, 8))
+    kn = _rand_bf16(rng, (1, 1, 8))
+    vn = _rand_bf16(rng, (1, 1, 8))
+    out, _, _, _ = O.paged_attn_decode_with_kvcache(q, kn, vn, kc, vc, [0], np.array([[2, -1]]), 16, 0.5)
+    assert np.array_equal(out[0, 0], O.bf16_bits_to_f64(vn[0, 0]))
+    assert np.array_equal(out[0, 1], O.bf16_bits_to_f64(vn[0, 0]))
