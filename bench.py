@@ -420,9 +420,39 @@ def extra_workloads(pkv, W, device, pk, args):
         torch.cuda.empty_cache()
     if hasattr(pkv, "paged_attn_varlen") and hasattr(pkv.lib(), "pkv_paged_attn_varlen"):
         out.update(prefill_workload(pkv, W, device, pk, args))
+    out.update(with_kvcache_workload(pkv, W, device, pk, args))
     out.update(copy_workload(pkv, W, device, pk, args))
     out.update(write_sweep(pkv, device, pk, args))
     return out
+
+
+def with_kvcache_workload(pkv, W, device, pk, args):
+    """The decode-batch step as one launch (append + decode) against write + decode (two launches)."""
+    wl = W.decode_batch(device=device)
+    step = DecodeStep(pkv, wl)
+    before = (wl.cache_seqlens - 1).contiguous()
+
+    def fused():
+        pkv.paged_attn_decode_with_kvcache(wl.q, wl.k_new, wl.v_new, step.kc4, step.vc4, before, wl.block_table,
+                                           wl.scale, max_seqlen_k=wl.max_seqlen, out=step.out,
+                                           workspace_buf=step.ws)
+
+    def separate():
+        step.write()
+        step.decode()
+
+    iters = max(20, min(200, args.steps // 10))
+    ms_f = time_calls(fused, iters)
+    ms_s = time_calls(separate, iters)
+    b = decode_bytes(wl) + write_bytes(wl)
+    res = {"decode_with_kvcache": {
+        "workload": "decode_batch64 step (64 seqs, U[1024,16384] cached + 1 appended, 32 q / 8 kv, d128, bs16) "
+                    "as one launch: append + decode", "step_ms": ms_f, "two_launch_step_ms": ms_s,
+        "GB_per_s": b / (ms_f * 1e-3) / 1e9, "frac_of_hbm_peak": b / (ms_f * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "tokens_per_s": wl.batch / (ms_f * 1e-3), "iters": iters}}
+    del step, wl
+    torch.cuda.empty_cache()
+    return res
 
 
 def copy_workload(pkv, W, device, pk, args):

@@ -5,6 +5,7 @@
  *
  *   pkv_kv_cache_write      scatter each new token's K/V row into the paged cache
  *   pkv_paged_attn_decode   one query token per sequence over its paged cache
+ *   pkv_paged_attn_decode_with_kvcache  the write and the decode in one launch
  *   pkv_paged_attn_varlen   causal GQA attention over packed variable-length
  *                           sequences, K/V packed or read from the paged cache
  *   pkv_copy_blocks         copy-on-write of shared cache blocks
@@ -168,6 +169,39 @@ PKV_API int pkv_paged_attn_decode(const void* q, const void* k_cache, const void
                           int32_t num_blocks, int32_t max_seqlen_k, float scale, float k_scale,
                           float v_scale, void* out, float* lse, void* workspace,
                           size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
+ * Decode attention with an in-place cache append ([PA] "デコードパス": the
+ * example's cache_seqlens count the tokens cached BEFORE this step, and the
+ * new token goes to the next position, in a held block or a new one; [KVM]
+ * "Attention モジュールの実装": write the step's K/V, then attend).  One call does
+ * both: for each sequence b, position pos = cache_seqlens[b] is
+ *   slot = block_table[b*max_blocks_per_seq + pos/block_size]*block_size + pos%block_size,
+ * k_cache row slot := k_new row b and v_cache row slot := v_new row b (bf16
+ * copied, or FP8 as e4m3_rne_satfinite(float(x)*inv_scale) like
+ * pkv_kv_cache_write), and then q[b] attends cache_seqlens[b] + 1 positions
+ * exactly as pkv_paged_attn_decode does.  The row is stored by the CTA that
+ * reads that position, before it reads it, so no separate write launch is
+ * needed.
+ *
+ * k_new, v_new:  bf16 [batch, num_kv_heads, head_dim] rows at k_new_row_stride /
+ *                v_new_row_stride elements (multiples of 8), 16-byte aligned.
+ * k_inv_scale, v_inv_scale: 1/scale of each FP8 cache (ignored for PKV_BF16).
+ * max_seqlen_k:  host upper bound of cache_seqlens + 1 (the attended length);
+ *                the workspace is pkv_paged_attn_decode_workspace(..., max_seqlen_k).
+ * Other arguments as for pkv_paged_attn_decode.  A position whose block id is
+ * outside [0, num_blocks) is flagged (PKV_DEVERR_BLOCK) and not written.
+ */
+PKV_API int pkv_paged_attn_decode_with_kvcache(const void* q, const void* k_new, int64_t k_new_row_stride,
+                                               const void* v_new, int64_t v_new_row_stride, void* k_cache,
+                                               void* v_cache, int32_t cache_dtype, const int32_t* cache_seqlens,
+                                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                                               int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                               int32_t max_seqlen_k, float scale, float k_scale, float v_scale,
+                                               float k_inv_scale, float v_inv_scale, void* out, float* lse,
+                                               void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                               void* stream);
 
 /*
  * Workspace bytes pkv_paged_attn_varlen needs for these sizes on the current

@@ -13,21 +13,26 @@
 // * Grid (split, kv_head, seq).  A CTA owns one kv head of one sequence over a
 //   contiguous range of positions, and serves every query head of that GQA
 //   group, so each K/V page row is read from HBM once per group.
-// * 4 warps; each warp streams its own 16-token groups (positions
-//   16*(warp + 4*i)) through a private cp.async ring of shared-memory stages
-//   (16-byte copies, zero-filled beyond the sequence end, XOR-swizzled rows).
+// * 4 warps; each warp streams its own 16-position groups (positions
+//   16*(warp + 4*i)) through a private ring of shared-memory stages, filled by
+//   one lane with TMA boxes of 16 rows (128- or 64-byte swizzle) that complete
+//   on a per-stage mbarrier; V rows past the sequence end are zeroed after
+//   the copy lands.  A bad block id issues no copy and is flagged.
 // * Scores on tensor cores with the operands swapped: S^T[16 tok x 8 heads] =
 //   K[16 x D] * Q^T[D x 8] (mma.sync m16n8k16), so a group of up to 8 heads
 //   fills the N=8 side and no token row is padding.  P is transposed in
 //   registers (movmatrix) into the B operand of O^T[D x 8] += V^T * P^T.
-// * Online softmax in the log2 domain, fp32; masked positions get -inf
-//   (never multiply-by-zero, so stale or NaN cache rows cannot leak in).
-// * FP8 E4M3 cache: codes are widened to bf16 in registers with a bit move that
-//   is exact up to a 2^-120 factor (see pkv_device.cuh); k_scale * 2^120 is
-//   folded into the logit scale and v_scale * 2^120 into the output.
+// * Online softmax in the log2 domain, fp32; the running max moves only when
+//   it grows by more than 2^8; masked positions get -inf (never
+//   multiply-by-zero, so stale or NaN cache rows cannot leak in).
+// * FP8 E4M3 cache: codes widen exactly to f16 with the hardware conversion
+//   and the MMAs run in f16; Q is scaled by a power of two into f16 range,
+//   k_scale folds into the logit scale and v_scale into the output.
 // * Per-CTA partials (O/l, log2-sum-exp) go to the caller's workspace; a
 //   second kernel merges the splits of each (seq, head).  A sequence that fits
 //   one split is written directly by the split kernel.
+// * Append mode (decode with the step's cache update): the warp whose copies
+//   read the new position stores the new K/V rows first.
 #include <cmath>
 
 #include "pkv_device.cuh"
@@ -73,6 +78,15 @@ struct DecodeParams {
   const int32_t* cu_k;
   int64_t lse_head_stride;
   int64_t lse_row_stride;
+  // Append (decode with an in-place cache update): seqlens hold the lengths
+  // before this step's token, which takes position seqlens[b]; its K/V rows
+  // (k_new/v_new row b, quantised for an FP8 cache) are stored there by the
+  // CTA whose positions end with it, before that CTA's copies read them, and
+  // the sequence attends seqlens[b] + 1 positions.  k_new == null: no append.
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int64_t k_new_stride, v_new_stride;  // elements between rows
+  float k_inv, v_inv;                  // FP8: 1 / scale of each cache
 };
 
 // Sequence served by grid index z (or -1), its q/out row and its length source.
@@ -89,6 +103,7 @@ __device__ __forceinline__ int64_t item_row(const DecodeParams& p, int b) {
 // workspace can hold (violations are flagged by the caller thread).
 __device__ __forceinline__ int attended_length(const DecodeParams& p, int b, bool report) {
   int len = p.cu_k != nullptr ? __ldg(p.cu_k + b + 1) - __ldg(p.cu_k + b) : __ldg(p.seqlens + b);
+  if (p.k_new != nullptr && len >= 0) len += 1;  // the appended token
   const int64_t cap_bt = (int64_t)p.max_blocks * p.block_size;
   const int64_t cap_ws = (int64_t)p.max_splits * p.split_tokens;
   bool bad = false;
@@ -248,6 +263,32 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
 #pragma unroll
   for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  // Append: the warp whose copies read the new position stores its K/V rows
+  // for this kv head first (a generic write, then a proxy fence so the TMA
+  // reads see it).  Skipped when the length was clamped (flagged above).
+  if (p.k_new != nullptr && t_end == len && len > 0 && __ldg(p.seqlens + b) == len - 1) {
+    const int pos = len - 1;
+    if (warp == ((pos - t_begin) / kGroupTok) % kDecWarps) {
+      const int blk = block_of(pos, lane == 0);
+      constexpr int kChunks = D / 8;  // 16-byte bf16 vectors per head row
+      if (blk >= 0 && lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = lane % kChunks;
+        const int64_t slot = (int64_t)blk * p.block_size + pos % p.block_size;
+        const uint16_t* src = (is_v ? p.v_new + b * p.v_new_stride : p.k_new + b * p.k_new_stride) + kvh * D;
+        const uint4 w = *reinterpret_cast<const uint4*>(src + c * 8);
+        uint8_t* row = const_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) +
+                       (slot * p.num_kv_heads + kvh) * (int64_t)kRowBytes;
+        if constexpr (kFp8)
+          reinterpret_cast<uint2*>(row)[c] = quantize8_e4m3(w, is_v ? p.v_inv : p.k_inv);
+        else
+          reinterpret_cast<uint4*>(row)[c] = w;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __syncwarp();
+    }
+  }
 
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i) issue(i);
@@ -579,14 +620,24 @@ extern "C" size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_hea
   return pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k).workspace;
 }
 
-extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, int32_t cache_dtype,
+namespace pkv {
+namespace {
+
+struct AppendArgs {
+  const void* k_new;
+  int64_t k_new_stride;
+  const void* v_new;
+  int64_t v_new_stride;
+  float k_inv, v_inv;
+};
+
+int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t cache_dtype,
                                      const int32_t* cache_seqlens, const int32_t* block_table,
                                      int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                      int32_t num_blocks, int32_t max_seqlen_k, float scale, float k_scale,
                                      float v_scale, void* out, float* lse, void* workspace,
-                                     size_t workspace_bytes, int32_t* err_flag, void* stream) {
-  using namespace pkv;
+                                     size_t workspace_bytes, int32_t* err_flag, void* stream, const AppendArgs* app) {
   if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
       max_seqlen_k < 0 || block_size <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -637,11 +688,61 @@ extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const v
   p.err = err_flag;
   p.lse_head_stride = 1;
   p.lse_row_stride = num_heads;
+  if (app != nullptr) {
+    p.k_new = static_cast<const uint16_t*>(app->k_new);
+    p.v_new = static_cast<const uint16_t*>(app->v_new);
+    p.k_new_stride = app->k_new_stride;
+    p.v_new_stride = app->v_new_stride;
+    p.k_inv = app->k_inv;
+    p.v_inv = app->v_inv;
+  }
   cudaStream_t st = as_stream(stream);
   const int64_t ns = (int64_t)num_blocks * block_size;
   if (head_dim == 128)
     return fp8 ? launch_decode<128, true>(p, batch, pl, ns, st) : launch_decode<128, false>(p, batch, pl, ns, st);
   return fp8 ? launch_decode<64, true>(p, batch, pl, ns, st) : launch_decode<64, false>(p, batch, pl, ns, st);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, int32_t cache_dtype,
+                                     const int32_t* cache_seqlens, const int32_t* block_table,
+                                     int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                     int32_t num_blocks, int32_t max_seqlen_k, float scale, float k_scale,
+                                     float v_scale, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  return pkv::decode_impl(q, k_cache, v_cache, cache_dtype, cache_seqlens, block_table, max_blocks_per_seq, batch,
+                          num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_seqlen_k, scale, k_scale,
+                          v_scale, out, lse, workspace, workspace_bytes, err_flag, stream, nullptr);
+}
+
+extern "C" int pkv_paged_attn_decode_with_kvcache(const void* q, const void* k_new, int64_t k_new_row_stride,
+                                                  const void* v_new, int64_t v_new_row_stride, void* k_cache,
+                                                  void* v_cache, int32_t cache_dtype, const int32_t* cache_seqlens,
+                                                  const int32_t* block_table, int32_t max_blocks_per_seq,
+                                                  int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                                  int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                                  int32_t max_seqlen_k, float scale, float k_scale, float v_scale,
+                                                  float k_inv_scale, float v_inv_scale, void* out, float* lse,
+                                                  void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                                  void* stream) {
+  using namespace pkv;
+  if (batch > 0) {
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+    if (k_new_row_stride < row || v_new_row_stride < row || k_new_row_stride % 8 || v_new_row_stride % 8)
+      return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype == PKV_FP8_E4M3 && (!(k_inv_scale > 0.f) || !(v_inv_scale > 0.f) ||
+                                        !std::isfinite(k_inv_scale) || !std::isfinite(v_inv_scale)))
+      return PKV_ERR_INVALID_ARG;
+  }
+  const AppendArgs app{k_new, k_new_row_stride, v_new, v_new_row_stride, k_inv_scale, v_inv_scale};
+  return decode_impl(q, k_cache, v_cache, cache_dtype, cache_seqlens, block_table, max_blocks_per_seq, batch,
+                     num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_seqlen_k, scale, k_scale, v_scale,
+                     out, lse, workspace, workspace_bytes, err_flag, stream, &app);
 }
 
 namespace pkv {

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "pkv.h"
@@ -88,6 +89,29 @@ __device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);  // .x = lo (low half), .y = hi
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Eight bf16 values (one 16-byte vector) -> eight OCP E4M3 codes, each
+// e4m3_rne_satfinite(float(x) * inv): one fp32 multiply and the hardware's
+// round-to-nearest-even saturating conversion.
+__device__ __forceinline__ uint2 quantize8_e4m3(uint4 v, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t packed[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const uint32_t word = w[h * 2 + p];
+      const float lo = __uint_as_float(word << 16);
+      const float hi = __uint_as_float(word & 0xFFFF0000u);
+      const __nv_fp8x2_storage_t two =
+          __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(lo, inv), __fmul_rn(hi, inv)), __NV_SATFINITE, __NV_E4M3);
+      bytes |= (uint32_t)two << (16 * p);
+    }
+    packed[h] = bytes;
+  }
+  return make_uint2(packed[0], packed[1]);
 }
 
 // Packed fp32 pairs (sm_100+): two lanes of arithmetic per instruction.

@@ -58,25 +58,8 @@ __global__ void __launch_bounds__(kWriteThreads) kv_cache_write_kernel(
           uint4* dst = reinterpret_cast<uint4*>(is_v ? v_cache : k_cache) + (int64_t)slot * chunks + c;
           *dst = buf[u];
         } else {
-          const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
-          uint32_t packed[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-              const uint32_t word = w[h * 2 + p];
-              const float lo = __uint_as_float(word << 16);
-              const float hi = __uint_as_float(word & 0xFFFF0000u);
-              const __nv_fp8x2_storage_t two =
-                  __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(lo, inv), __fmul_rn(hi, inv)), __NV_SATFINITE,
-                                           __NV_E4M3);
-              bytes |= (uint32_t)two << (16 * p);
-            }
-            packed[h] = bytes;
-          }
           uint2* dst = reinterpret_cast<uint2*>(is_v ? v_cache : k_cache) + (int64_t)slot * chunks + c;
-          *dst = make_uint2(packed[0], packed[1]);
+          *dst = quantize8_e4m3(buf[u], inv);
         }
       }
     }

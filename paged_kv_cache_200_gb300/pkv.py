@@ -49,6 +49,10 @@ _SIGNATURES = {
     "pkv_paged_attn_decode": (ctypes.c_int, [
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
         _i32, _i32, _i32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p, _c_void_p]),
+    "pkv_paged_attn_decode_with_kvcache": (ctypes.c_int, [
+        _c_void_p, _c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32,
+        _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _sz,
+        _c_void_p, _c_void_p]),
     "pkv_paged_attn_decode_noalloc": (ctypes.c_int, [
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
         _i32, _i32, _i32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
@@ -238,6 +242,53 @@ def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale: fl
                                  int(max_seqlen_k), float(scale), float(k_scale), float(v_scale), _ptr(out),
                                  _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(err_flag),
                                  _stream(stream))
+    _check(st)
+    return (out, lse) if (return_lse or lse is not None) else out
+
+
+def paged_attn_decode_with_kvcache(q, k_new, v_new, k_cache, v_cache, cache_seqlens, block_table, scale: float,
+                                   max_seqlen_k: int = None, k_scale: float = 1.0, v_scale: float = 1.0,
+                                   k_inv_scale: float = 1.0, v_inv_scale: float = 1.0, out=None, lse=None,
+                                   return_lse=False, err_flag=None, workspace_buf=None, stream=None):
+    """Append each sequence's new K/V row to its cache, then decode, in one launch.
+
+    ``cache_seqlens``: int32 ``[B]`` tokens cached BEFORE this step; the new row
+    ``k_new[b]``/``v_new[b]`` (bf16 ``[B, Hkv, D]``, inner dims contiguous) goes
+    to position ``cache_seqlens[b]`` and ``cache_seqlens[b] + 1`` positions are
+    attended.  ``max_seqlen_k``: host bound of ``cache_seqlens + 1`` (default:
+    the block table's capacity).  FP8 caches store ``e4m3(x * inv_scale)``.
+    """
+    _require_cuda(q, k_new, v_new, k_cache, v_cache, cache_seqlens, block_table)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be contiguous bf16 [B, Hq, D]")
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or k_new.dtype != torch.bfloat16 or \
+            v_new.dtype != torch.bfloat16:
+        raise ValueError("k_new and v_new must be bf16 [B, Hkv, D]")
+    if k_new.stride(-1) != 1 or v_new.stride(-1) != 1 or k_new.stride(1) != D or v_new.stride(1) != D:
+        raise ValueError("k_new/v_new inner dims [Hkv, D] must be contiguous")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.is_contiguous()):
+        raise ValueError("caches and block_table must be contiguous")
+    if cache_seqlens.dtype != torch.int32 or block_table.dtype != torch.int32:
+        raise ValueError("cache_seqlens and block_table must be int32")
+    MB = block_table.shape[1]
+    if max_seqlen_k is None:
+        max_seqlen_k = MB * bs
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    L = lib()
+    need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
+    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device) if need else None)
+    st = L.pkv_paged_attn_decode_with_kvcache(
+        _ptr(q), _ptr(k_new), k_new.stride(0), _ptr(v_new), v_new.stride(0), _ptr(k_cache), _ptr(v_cache),
+        _cache_dtype(k_cache), _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB, int(max_seqlen_k),
+        float(scale), float(k_scale), float(v_scale), float(k_inv_scale), float(v_inv_scale), _ptr(out), _ptr(lse),
+        _ptr(ws), 0 if ws is None else ws.numel(), _ptr(err_flag), _stream(stream))
     _check(st)
     return (out, lse) if (return_lse or lse is not None) else out
 
