@@ -543,37 +543,64 @@ def prefill_workload(pkv, W, device, pk, args):
     wp = W.varlen_prefill(device=device, paged=True)
     shape4 = (wp.num_blocks, wp.block_size, wp.num_kv_heads, wp.head_dim)
     kc4, vc4 = wp.k_cache.view(shape4), wp.v_cache.view(shape4)
-    need = pkv.lib().pkv_paged_attn_varlen_workspace(wp.batch, wp.total_q, wp.num_heads, wp.num_kv_heads,
-                                                      wp.head_dim, wp.max_len_q, wp.max_len_k, 1)
-    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     out = torch.empty_like(wp.q)
 
-    def paged_step():
-        pkv.kv_cache_write(wp.k_new, wp.v_new, wp.k_cache, wp.v_cache, wp.slot_mapping)
-        pkv.paged_attn_varlen(wp.q, kc4, vc4, wp.cu_seqlens_q, wp.cu_seqlens_k, wp.max_len_q, wp.max_len_k,
-                              block_table=wp.block_table, scale=wp.scale, out=out, workspace_buf=ws)
+    def paged_leg(gather, dt="bf16", wlx=wp):
+        gtok = W.gather_tokens(wlx) if gather else 0
+        kc, vc = wlx.k_cache.view(shape4), wlx.v_cache.view(shape4)
+        ks = wlx.extra.get("k_scale", 1.0) if dt != "bf16" else 1.0
+        vs = wlx.extra.get("v_scale", 1.0) if dt != "bf16" else 1.0
+        kinv = wlx.extra.get("k_inv_scale", 1.0)
+        vinv = wlx.extra.get("v_inv_scale", 1.0)
+        need = pkv.lib().pkv_paged_attn_varlen_workspace(wlx.batch, wlx.total_q, gtok, wlx.num_heads,
+                                                          wlx.num_kv_heads, wlx.head_dim, wlx.max_len_q,
+                                                          wlx.max_len_k, 1, 2 if dt != "bf16" else 0,
+                                                          wlx.block_size)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
 
-    ms = time_calls(paged_step, iters)
+        def step():
+            pkv.kv_cache_write(wlx.k_new, wlx.v_new, wlx.k_cache, wlx.v_cache, wlx.slot_mapping, k_inv_scale=kinv,
+                               v_inv_scale=vinv)
+            pkv.paged_attn_varlen(wlx.q, kc, vc, wlx.cu_seqlens_q, wlx.cu_seqlens_k, wlx.max_len_q, wlx.max_len_k,
+                                  block_table=wlx.block_table, scale=wlx.scale, out=out, workspace_buf=ws,
+                                  gather_k_tokens=gtok, k_scale=ks, v_scale=vs)
+
+        return time_calls(step, iters)
+
+    for key, gather, dt, what in (
+            ("varlen_prefill_paged", True, "bf16", "K/V gathered into a packed buffer first (the default with a gather "
+                                                   "bound)"),
+            ("varlen_prefill_paged_direct", False, "bf16", "K/V read through the block table by the tile loop"),
+    ):
+        ms = paged_leg(gather, dt)
+        tf = flops / (ms * 1e-3) / 1e12
+        res[key] = {
+            "workload": "same sequences written by slot mapping into a 16-token-block permuted pool, then causal "
+                        "varlen attention over the paged cache, " + what + " (step = write + attention)",
+            "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "iters": iters}
+    wf = W.to_fp8_cache(wp)
+    ms = paged_leg(True, "fp8_e4m3", wf)
     tf = flops / (ms * 1e-3) / 1e12
-    res["varlen_prefill_paged"] = {
-        "workload": "same sequences written by slot mapping into a 16-token-block permuted pool, then causal "
-                    "varlen attention reading K/V through the block table (step = write + attention)",
+    res["varlen_prefill_paged_fp8"] = {
+        "workload": "same, FP8 E4M3 cache (per-tensor scales; write quantises, prefill widens the gathered codes)",
         "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "iters": iters}
-    del wp, kc4, vc4, out, ws
+    del wp, wf, kc4, vc4, out
     torch.cuda.empty_cache()
 
     wm = W.mixed_chunked(device=device)
     shape4 = (wm.num_blocks, wm.block_size, wm.num_kv_heads, wm.head_dim)
     kc4, vc4 = wm.k_cache.view(shape4), wm.v_cache.view(shape4)
-    need = pkv.lib().pkv_paged_attn_varlen_workspace(wm.batch, wm.total_q, wm.num_heads, wm.num_kv_heads,
-                                                      wm.head_dim, wm.max_len_q, wm.max_len_k, 1)
+    gtok = W.gather_tokens(wm)
+    need = pkv.lib().pkv_paged_attn_varlen_workspace(wm.batch, wm.total_q, gtok, wm.num_heads, wm.num_kv_heads,
+                                                      wm.head_dim, wm.max_len_q, wm.max_len_k, 1, 0, wm.block_size)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     out = torch.empty_like(wm.q)
 
     def mixed_step():
         pkv.kv_cache_write(wm.k_new, wm.v_new, wm.k_cache, wm.v_cache, wm.slot_mapping)
         pkv.paged_attn_varlen(wm.q, kc4, vc4, wm.cu_seqlens_q, wm.cu_seqlens_k, wm.max_len_q, wm.max_len_k,
-                              block_table=wm.block_table, scale=wm.scale, out=out, workspace_buf=ws)
+                              block_table=wm.block_table, scale=wm.scale, out=out, workspace_buf=ws,
+                              gather_k_tokens=gtok)
 
     ms = time_calls(mixed_step, iters)
     pre = wm.q_lens > 1
@@ -582,7 +609,8 @@ def prefill_workload(pkv, W, device, pk, args):
     t_roof = max(mflops / (pk["bf16_tflops"] * 1e12), dec_bytes / (pk["hbm_gbs"] * 1e9))
     res["mixed_chunked"] = {
         "workload": "4 x 512-query chunks over 0/2K/4K/8K prefixes (2K prefix shares the 4K chunk's blocks) + 60 "
-                    "decode rows of 513..8193 keys, one varlen call after the write; 32 q / 8 kv, d128, bs16",
+                    "decode rows of 513..8193 keys, one varlen call after the write (chunks' K/V gathered); "
+                    "32 q / 8 kv, d128, bs16",
         "ms": ms, "prefill_flops": mflops, "decode_kv_bytes": dec_bytes, "roofline_ms": t_roof * 1e3,
         "frac_of_roofline": t_roof * 1e3 / ms, "tokens_per_s": wm.total_q / (ms * 1e-3), "iters": iters}
     return res

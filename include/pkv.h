@@ -204,13 +204,16 @@ PKV_API int pkv_paged_attn_decode_with_kvcache(const void* q, const void* k_new,
                                                void* stream);
 
 /*
- * Workspace bytes pkv_paged_attn_varlen needs for these sizes on the current
- * device (0 is a valid answer).  `paged` is non-zero when a block table will be
- * passed.  Returns 0 for invalid sizes as well.
+ * Workspace bytes pkv_paged_attn_varlen needs for these arguments on the
+ * current device (0 is a valid answer).  `paged` is non-zero when a block table
+ * will be passed; total_k, kv_dtype and block_size are the values the call will
+ * get (they decide whether the paged K/V are gathered first, see below).
+ * Returns 0 for invalid sizes as well.
  */
-PKV_API size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, int32_t num_heads,
+PKV_API size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
                                                int32_t num_kv_heads, int32_t head_dim, int32_t max_len_q,
-                                               int32_t max_len_k, int32_t paged);
+                                               int32_t max_len_k, int32_t paged, int32_t kv_dtype,
+                                               int32_t block_size);
 
 /*
  * Variable-length causal attention ([PA] "Varlen パス"; [KVM] "Attention モジュールの実装",
@@ -233,10 +236,18 @@ PKV_API size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, i
  * zeros and lse = -inf.
  *
  * max_len_q, max_len_k: host upper bounds of the lengths (grid sizing).
- * total_k: rows of the packed k/v (ignored in paged mode).
- * Supported: head_dim 64 or 128, bf16 K/V (kv_dtype PKV_BF16; k_scale and
- * v_scale are reserved), causal != 0; paged block_size a multiple of 16 that
- * divides 128 or is a multiple of 128.  All of q, k, v, out 16-byte aligned.
+ * total_k: packed mode: rows of the packed k/v.  Paged mode: 0, or an upper
+ *          bound on the summed key counts of the sequences with more than one
+ *          query.  With total_k > 0 and an FP8 cache or block_size < 64, those
+ *          sequences' K/V are first gathered through the block table into a
+ *          packed bf16 buffer in the workspace (FP8 codes widened exactly), and
+ *          the packed tile loop runs on it: one small copy box per page and
+ *          head-dim half would bound the paged loop.  Keys past the bound are
+ *          not gathered and flagged (PKV_DEVERR_LENGTH).
+ * kv_dtype: PKV_BF16, or PKV_FP8_E4M3 (paged mode with total_k > 0 only) where a
+ *          cached code c stands for float(c)*k_scale (resp. v_scale).
+ * Supported: head_dim 64 or 128, causal != 0; paged block_size a multiple of 16
+ * that divides 128 or is a multiple of 128.  All of q, k, v, out 16-byte aligned.
  * In paged mode sequences with exactly one query are computed by the decode
  * kernels (split-KV over the GQA group) instead of a 128-row tile.
  */

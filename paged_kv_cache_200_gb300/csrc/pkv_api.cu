@@ -66,4 +66,4 @@ extern "C" const char* pkv_status_string(int status) {
   }
 }
 
-extern "C" int pkv_abi_version(void) { return 1; }
+extern "C" int pkv_abi_version(void) { return 2; }

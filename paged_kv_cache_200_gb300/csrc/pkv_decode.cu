@@ -758,8 +758,9 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,
                          const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                         int32_t max_len_k, int64_t total_q, float scale, void* out, float* lse, void* workspace,
-                         size_t workspace_bytes, int32_t* err_flag, cudaStream_t st) {
+                         int32_t max_len_k, int64_t total_q, float scale, bool fp8, float k_scale, float v_scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                         cudaStream_t st) {
   if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
   const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1);
   if (pl.workspace > workspace_bytes) return PKV_ERR_WORKSPACE;
@@ -776,8 +777,8 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.num_blocks = num_blocks;
   p.split_tokens = pl.split_tokens;
   p.max_splits = pl.max_splits;
-  p.scale_log2 = scale * kLog2e;
-  p.v_mul = 1.f;
+  p.scale_log2 = scale * kLog2e * (fp8 ? k_scale : 1.f);
+  p.v_mul = fp8 ? v_scale : 1.f;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   if (pl.max_splits > 1) {
@@ -793,8 +794,9 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.lse_head_stride = total_q;
   p.lse_row_stride = 1;
   const int64_t ns = (int64_t)num_blocks * block_size;
-  if (head_dim == 128) return launch_decode<128, false>(p, batch, pl, ns, st);
-  return launch_decode<64, false>(p, batch, pl, ns, st);
+  if (head_dim == 128)
+    return fp8 ? launch_decode<128, true>(p, batch, pl, ns, st) : launch_decode<128, false>(p, batch, pl, ns, st);
+  return fp8 ? launch_decode<64, true>(p, batch, pl, ns, st) : launch_decode<64, false>(p, batch, pl, ns, st);
 }
 
 }  // namespace pkv

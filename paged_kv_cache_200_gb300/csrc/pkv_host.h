@@ -32,7 +32,8 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,
                          const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                         int32_t max_len_k, int64_t total_q, float scale, void* out, float* lse, void* workspace,
-                         size_t workspace_bytes, int32_t* err_flag, cudaStream_t st);
+                         int32_t max_len_k, int64_t total_q, float scale, bool fp8, float k_scale, float v_scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                         cudaStream_t st);
 
 }  // namespace pkv

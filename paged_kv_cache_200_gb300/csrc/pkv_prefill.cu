@@ -63,6 +63,7 @@ struct PrefillParams {
   int32_t route_decode;  // sequences with exactly one query are left to the decode kernels
   int32_t* item_counter; // work-item counter, zero at launch
   float scale_log2;
+  float v_mul;           // output factor (FP8 V scale of a gathered cache, else 1)
   int64_t total_q;
   uint16_t* out;
   float* lse;
@@ -398,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           int loaded = 0;
-          for (int pg = 0; pg < npages; ++pg)
-            if (key0 + pg * br < sq.Lk) ++loaded;
+          for (int q = 0; q < npages; ++q)
+            if (key0 + q * br < sq.Lk) ++loaded;
           // one lane per (page, atom) issues that box, after the byte count is registered
           if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
           __syncwarp();
@@ -636,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - ms);
       const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - ms);
       const float lt = l0 * f0 + l1 * f1;
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float inv = lt > 0.f ? p.v_mul / lt : 0.f;
       const float w0 = f0 * inv, w1 = f1 * inv;
       // this half writes head dims [half*D/2, (half+1)*D/2)
 #pragma unroll
@@ -685,12 +686,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // of a mixed batch) into items[0..*count); the prefill kernel skips them and
 // the split-KV decode kernels serve them, one CTA per (split, kv head, item).
 // It also resets the prefill kernel's work-item counter.
-__global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __restrict__ cu_q, int batch,
+__global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __restrict__ cu_q,
+                                                           const int32_t* __restrict__ cu_k, int batch,
                                                            int32_t* __restrict__ items, int32_t* __restrict__ count,
-                                                           int32_t* __restrict__ item_counter) {
+                                                           int32_t* __restrict__ item_counter,
+                                                           int32_t* __restrict__ cu_g, int64_t gather_cap,
+                                                           int32_t* err) {
   __shared__ int n;
+  __shared__ int64_t carry;
   if (threadIdx.x == 0) {
     n = 0;
+    carry = 0;
     *item_counter = 0;
   }
   __syncthreads();
@@ -701,6 +707,105 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
     __syncthreads();
     if (threadIdx.x == 0) *count = n;
   }
+  if (cu_g != nullptr) {
+    // Packed offsets of the gathered sequences (those the prefill kernel
+    // serves: more than one query, or any query when nothing is routed):
+    // cu_g[b] = sum of their key counts before b.  Exclusive scan, one
+    // 32-sequence chunk per warp step, carried across passes.
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __shared__ int64_t warp_sum[32];
+    for (int base = 0; base < batch; base += blockDim.x) {
+      const int b = base + threadIdx.x;
+      int64_t v = 0;
+      if (b < batch) {
+        const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
+        const int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
+        const bool gathered = lq > 0 && !(items != nullptr && lq == 1);
+        v = gathered && lk > 0 ? lk : 0;
+      }
+      int64_t x = v;  // inclusive warp scan
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) warp_sum[warp] = x;
+      __syncthreads();
+      int64_t before = carry;
+      for (int w = 0; w < warp; ++w) before += warp_sum[w];
+      if (b < batch) cu_g[b] = (int32_t)(before + x - v);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int w = 0; w < nw; ++w) carry += warp_sum[w];
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      cu_g[batch] = (int32_t)carry;
+      if (carry > gather_cap) flag_error(err, PKV_DEVERR_LENGTH);  // rows past the buffer are not gathered
+    }
+  }
+}
+
+// Gather (paged -> packed): key j of every gathered sequence b is copied from
+// its cache slot to row cu_g[b] + j of a packed bf16 buffer, for K and V.  An
+// FP8 cache is widened exactly (every E4M3 value is a bf16 value; the scales
+// are applied by the attention).  Bad block ids are flagged and give zero rows;
+// rows at or past `cap` are not written.  CTA (t, b): positions [64 t, 64 t + 64).
+template <bool kFp8>
+__global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restrict__ k_cache,
+                                                        const uint8_t* __restrict__ v_cache,
+                                                        const int32_t* __restrict__ cu_q,
+                                                        const int32_t* __restrict__ cu_k,
+                                                        const int32_t* __restrict__ cu_g,
+                                                        const int32_t* __restrict__ block_table, int32_t max_blocks,
+                                                        int32_t block_size, int32_t num_blocks, int32_t row_elems,
+                                                        int route, int64_t cap, uint16_t* __restrict__ k_out,
+                                                        uint16_t* __restrict__ v_out, int32_t* err) {
+  const int b = blockIdx.y;
+  const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
+  if (lq <= 0 || (route && lq == 1)) return;
+  int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
+  if ((int64_t)lk > (int64_t)max_blocks * block_size) {  // more keys than the table holds
+    lk = max_blocks * block_size;
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, PKV_DEVERR_LENGTH);
+  }
+  const int64_t g0 = __ldg(cu_g + b);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunks = row_elems >> 3;  // 16-byte bf16 vectors per row
+  for (int j = blockIdx.x * 64 + warp; j < min(lk, blockIdx.x * 64 + 64); j += 8) {
+    const int64_t row = g0 + j;
+    if (row >= cap) break;
+    int blk = __ldg(block_table + (int64_t)b * max_blocks + j / block_size);
+    const bool bad = blk < 0 || blk >= num_blocks;
+    if (bad && lane == 0) flag_error(err, PKV_DEVERR_BLOCK);
+    const int64_t slot = bad ? 0 : (int64_t)blk * block_size + j % block_size;
+    for (int t = 0; t < 2; ++t) {
+      const uint8_t* src = t ? v_cache : k_cache;
+      uint4* dst = reinterpret_cast<uint4*>((t ? v_out : k_out) + row * row_elems);
+      for (int c = lane; c < chunks; c += 32) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (!bad) {
+          if constexpr (!kFp8) {
+            w = __ldg(reinterpret_cast<const uint4*>(src + slot * row_elems * 2) + c);
+          } else {
+            const uint2 codes = __ldg(reinterpret_cast<const uint2*>(src + slot * row_elems) + c);
+            const uint32_t cw[2] = {codes.x, codes.y};
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t lo = e4m3x2_lo_to_f16x2(cw[h]), hi = e4m3x2_hi_to_f16x2(cw[h]);
+              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+              const float2 bb = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+              o[2 * h] = pack_bf16x2(a.x, a.y);
+              o[2 * h + 1] = pack_bf16x2(bb.x, bb.y);
+            }
+            w = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        dst[c] = w;
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -708,18 +813,41 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
 // ---------------------------------------------------------------------------
 
 struct VarlenWs {
-  size_t count_off, items_off, decode_off, total;
+  size_t count_off, items_off, decode_off, cu_g_off, gk_off, gv_off, total;
 };
 
+// Paged K/V with blocks smaller than this (or FP8) are gathered into a packed
+// bf16 buffer first when the caller sizes it (total_k > 0): one small TMA box
+// per 16-token page and head-dim half bounds the paged loop, while the gather
+// is a plain HBM copy and the packed loop runs at the full tile rate.
+constexpr int kGatherBelowBlock = 64;
+
+bool uses_gather(bool paged, int kv_dtype, int block_size, int64_t total_k) {
+  return paged && total_k > 0 && (kv_dtype == PKV_FP8_E4M3 || block_size < kGatherBelowBlock);
+}
+
 // [0, 256): the prefill work-item counter and the routed-row count; then the
-// routed row list and the decode partials (paged mode only).
-VarlenWs varlen_ws_layout(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k, bool route) {
-  VarlenWs w{0, 0, 0, 256};
-  if (!route || batch <= 0) return w;
-  w.count_off = 4;
-  w.items_off = 256;
-  w.decode_off = w.items_off + (((size_t)batch * 4 + 255) / 256) * 256;
-  w.total = w.decode_off + varlen_decode_workspace(batch, num_heads, num_kv_heads, head_dim, max_len_k);
+// routed row list and the decode partials (paged mode), then, when K/V are
+// gathered, the packed offsets cu_g[batch+1] and the packed K and V buffers
+// of total_k rows each.
+VarlenWs varlen_ws_layout(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k, bool route,
+                          bool gather, int64_t total_k) {
+  VarlenWs w{0, 0, 0, 0, 0, 0, 256};
+  if (batch <= 0) return w;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  if (route) {
+    w.count_off = 4;
+    w.items_off = 256;
+    w.decode_off = w.items_off + up((size_t)batch * 4);
+    w.total = w.decode_off + varlen_decode_workspace(batch, num_heads, num_kv_heads, head_dim, max_len_k);
+  }
+  if (gather) {
+    w.cu_g_off = up(w.total);
+    w.gk_off = w.cu_g_off + up(((size_t)batch + 1) * 4);
+    const size_t buf = up((size_t)total_k * num_kv_heads * head_dim * 2);
+    w.gv_off = w.gk_off + buf;
+    w.total = w.gv_off + buf;
+  }
   return w;
 }
 
@@ -752,14 +880,16 @@ static bool routes_decode(bool paged, int num_heads, int num_kv_heads) {
   return paged && num_kv_heads > 0 && num_heads % num_kv_heads == 0 && num_heads / num_kv_heads <= 8;
 }
 
-extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, int32_t num_heads,
-                                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_len_q,
-                                                  int32_t max_len_k, int32_t paged) {
+extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, int32_t total_k,
+                                                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                  int32_t max_len_q, int32_t max_len_k, int32_t paged,
+                                                  int32_t kv_dtype, int32_t block_size) {
   (void)total_q;
   (void)max_len_q;
-  if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_len_k < 0) return 0;
+  if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_len_k < 0 || total_k < 0) return 0;
+  const bool gather = pkv::uses_gather(paged != 0, kv_dtype, block_size, total_k);
   return pkv::varlen_ws_layout(batch, num_heads, num_kv_heads, head_dim, max_len_k,
-                               routes_decode(paged != 0, num_heads, num_kv_heads))
+                               routes_decode(paged != 0, num_heads, num_kv_heads), gather, total_k)
       .total;
 }
 
@@ -772,14 +902,17 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
                                      float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
                                      void* stream) {
   using namespace pkv;
-  (void)k_scale;
-  (void)v_scale;
   if (batch < 0 || total_q < 0 || total_k < 0 || max_len_q < 0 || max_len_k < 0 || num_heads <= 0 ||
       num_kv_heads <= 0)
     return PKV_ERR_INVALID_ARG;
   if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (head_dim != 128 && head_dim != 64) return PKV_ERR_UNSUPPORTED;
-  if (kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  const bool fp8 = kv_dtype == PKV_FP8_E4M3;
+  // an FP8 cache is read through the gather (paged mode, total_k > 0)
+  if (fp8 && (block_table == nullptr || total_k <= 0)) return PKV_ERR_UNSUPPORTED;
+  if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
+    return PKV_ERR_INVALID_ARG;
   if (!causal) return PKV_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   const bool paged = block_table != nullptr;
@@ -793,25 +926,33 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return PKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
 
-  CUtensorMap mq, mk, mv;
-  const int64_t kv_rows = paged ? (int64_t)num_blocks * block_size : (int64_t)total_k;
-  const int kv_box = paged ? (block_size < 128 ? block_size : 128) : 128;
-  // [rows, heads, dim] bf16, boxes of 64 elements x 1 head x box rows, 128-byte swizzle
-  if (!make_tmap_3d(&mq, q, 2, total_q, num_heads, head_dim, 64, 128, 128) ||
-      !make_tmap_3d(&mk, k, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128) ||
-      !make_tmap_3d(&mv, v, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128))
-    return PKV_ERR_CUDA;
-
   const bool route = routes_decode(paged, num_heads, num_kv_heads);
-  const VarlenWs wl = varlen_ws_layout(batch, num_heads, num_kv_heads, head_dim, max_len_k, route);
+  const bool gather = uses_gather(paged, kv_dtype, block_size, total_k);
+  const VarlenWs wl = varlen_ws_layout(batch, num_heads, num_kv_heads, head_dim, max_len_k, route, gather, total_k);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
                        (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
+  char* wsb = static_cast<char*>(workspace);
+
+  // Gathered mode runs the packed kernel on the gathered buffers, with the
+  // packed offsets cu_g in place of cu_seqlens_k (same lengths for the
+  // gathered sequences, zero for the ones the decode kernels take).
+  const bool packed_tiles = !paged || gather;
+  const void* kt = gather ? static_cast<const void*>(wsb + wl.gk_off) : k;
+  const void* vt = gather ? static_cast<const void*>(wsb + wl.gv_off) : v;
+  CUtensorMap mq, mk, mv;
+  const int64_t kv_rows = !paged ? (int64_t)total_k : gather ? (int64_t)total_k : (int64_t)num_blocks * block_size;
+  const int kv_box = packed_tiles ? 128 : (block_size < 128 ? block_size : 128);
+  // [rows, heads, dim] bf16, boxes of 64 elements x 1 head x box rows, 128-byte swizzle
+  if (!make_tmap_3d(&mq, q, 2, total_q, num_heads, head_dim, 64, 128, 128) ||
+      !make_tmap_3d(&mk, kt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128) ||
+      !make_tmap_3d(&mv, vt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128))
+    return PKV_ERR_CUDA;
 
   PrefillParams p{};
   p.cu_q = cu_seqlens_q;
-  p.cu_k = cu_seqlens_k;
-  p.block_table = block_table;
+  p.cu_k = gather ? reinterpret_cast<const int32_t*>(wsb + wl.cu_g_off) : cu_seqlens_k;
+  p.block_table = packed_tiles ? nullptr : block_table;
   p.max_blocks = max_blocks_per_seq;
   p.block_size = block_size;
   p.box_rows = kv_box;
@@ -821,7 +962,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.n_qtiles = (max_len_q + kBM - 1) / kBM;
   p.batch = batch;
   p.route_decode = route ? 1 : 0;
-  p.scale_log2 = scale * kLog2e;
+  // FP8: the gathered codes are exact bf16 values; k_scale joins the logit
+  // scale and v_scale the output factor
+  p.scale_log2 = scale * kLog2e * (fp8 ? k_scale : 1.f);
+  p.v_mul = fp8 ? v_scale : 1.f;
   p.total_q = total_q;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
@@ -834,15 +978,35 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
     count = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.count_off);
     items = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.items_off);
   }
-  varlen_prep_kernel<<<1, route ? 1024 : 32, 0, st>>>(cu_seqlens_q, batch, items, count, p.item_counter);
+  int32_t* cu_g = gather ? reinterpret_cast<int32_t*>(wsb + wl.cu_g_off) : nullptr;
+  varlen_prep_kernel<<<1, (route || gather) ? 1024 : 32, 0, st>>>(cu_seqlens_q, cu_seqlens_k, batch, items, count,
+                                                                  p.item_counter, cu_g, (int64_t)total_k, err_flag);
+  if (gather) {
+    const dim3 ggrid((unsigned)((max_len_k + 63) / 64 > 0 ? (max_len_k + 63) / 64 : 1), (unsigned)batch, 1);
+    const int row_elems = num_kv_heads * head_dim;
+    uint16_t* gk = reinterpret_cast<uint16_t*>(wsb + wl.gk_off);
+    uint16_t* gv = reinterpret_cast<uint16_t*>(wsb + wl.gv_off);
+    const auto* kc = static_cast<const uint8_t*>(k);
+    const auto* vc = static_cast<const uint8_t*>(v);
+    if (fp8)
+      gather_kv_kernel<true><<<ggrid, 256, 0, st>>>(kc, vc, cu_seqlens_q, cu_seqlens_k, cu_g, block_table,
+                                                     max_blocks_per_seq, block_size, num_blocks, row_elems,
+                                                     route ? 1 : 0, total_k, gk, gv, err_flag);
+    else
+      gather_kv_kernel<false><<<ggrid, 256, 0, st>>>(kc, vc, cu_seqlens_q, cu_seqlens_k, cu_g, block_table,
+                                                      max_blocks_per_seq, block_size, num_blocks, row_elems,
+                                                      route ? 1 : 0, total_k, gk, gv, err_flag);
+  }
   int rc;
   if (head_dim == 128)
-    rc = paged ? launch_prefill<128, true>(mq, mk, mv, p, batch, st) : launch_prefill<128, false>(mq, mk, mv, p, batch, st);
+    rc = packed_tiles ? launch_prefill<128, false>(mq, mk, mv, p, batch, st)
+                      : launch_prefill<128, true>(mq, mk, mv, p, batch, st);
   else
-    rc = paged ? launch_prefill<64, true>(mq, mk, mv, p, batch, st) : launch_prefill<64, false>(mq, mk, mv, p, batch, st);
+    rc = packed_tiles ? launch_prefill<64, false>(mq, mk, mv, p, batch, st)
+                      : launch_prefill<64, true>(mq, mk, mv, p, batch, st);
   if (rc != PKV_OK || !route) return rc;
   return launch_varlen_decode(q, k, v, items, count, cu_seqlens_q, cu_seqlens_k, block_table, max_blocks_per_seq,
                               batch, num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_len_k, total_q,
-                              scale, out, lse, static_cast<char*>(workspace) + wl.decode_off,
-                              wl.total - wl.decode_off, err_flag, st);
+                              scale, fp8, k_scale, v_scale, out, lse, wsb + wl.decode_off,
+                              (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, st);
 }

@@ -57,7 +57,7 @@ _SIGNATURES = {
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
         _i32, _i32, _i32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "pkv_paged_attn_decode_noalloc_max_scratch": (_sz, []),
-    "pkv_paged_attn_varlen_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pkv_paged_attn_varlen_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pkv_paged_attn_varlen": (ctypes.c_int, [
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
         _c_void_p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _f32, _f32, _c_void_p, _c_void_p,
@@ -326,13 +326,18 @@ def paged_attn_decode_noalloc(q, k_cache, v_cache, cache_seqlens, block_table, s
 
 def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_len_k: int, block_table=None,
                       scale: float = None, causal: bool = True, out=None, lse=None, return_lse=False,
-                      err_flag=None, workspace_buf=None, stream=None):
+                      err_flag=None, workspace_buf=None, stream=None, gather_k_tokens: int = 0,
+                      k_scale: float = 1.0, v_scale: float = 1.0):
     """Causal varlen attention; returns ``out [total_q, Hq, D]`` (and ``lse [Hq, total_q]``).
 
     Without ``block_table``: ``k``/``v`` are packed ``[total_k, Hkv, D]``.  With it:
     ``k``/``v`` are the paged caches ``[num_blocks, block_size, Hkv, D]`` and
     ``block_table`` is int32 ``[B, max_blocks_per_seq]``.  ``max_len_q`` /
     ``max_len_k`` are host upper bounds of the lengths (no device sync is made).
+    Paged mode: ``gather_k_tokens`` (a host bound on the summed keys of the
+    sequences with more than one query) lets the library gather their K/V into
+    a packed bf16 buffer first, which small blocks and FP8 caches (uint8 E4M3
+    codes, value = code * k_scale / v_scale) use.
     """
     _require_cuda(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table)
     T, Hq, D = q.shape
@@ -348,7 +353,7 @@ def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_l
         MB, bs, NB = 0, 0, 0
     else:
         NB, bs, Hkv, _ = k.shape
-        total_k = NB * bs
+        total_k = int(gather_k_tokens)
         if block_table.dtype != torch.int32 or not block_table.is_contiguous():
             raise ValueError("block_table must be contiguous int32")
         MB = block_table.shape[1]
@@ -360,12 +365,14 @@ def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_l
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
     L = lib()
     paged = 1 if block_table is not None else 0
-    need = L.pkv_paged_attn_varlen_workspace(B, T, Hq, Hkv, D, int(max_len_q), int(max_len_k), paged)
+    need = L.pkv_paged_attn_varlen_workspace(B, T, total_k, Hq, Hkv, D, int(max_len_q), int(max_len_k), paged,
+                                             _cache_dtype(k), bs)
     ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device) if need else None)
     st = L.pkv_paged_attn_varlen(_ptr(q), _ptr(k), _ptr(v), _cache_dtype(k), _ptr(cu_seqlens_q),
                                  _ptr(cu_seqlens_k), B, T, total_k, int(max_len_q), int(max_len_k),
                                  _ptr(block_table), MB, bs, NB, Hq, Hkv, D, float(scale), 1 if causal else 0,
-                                 1.0, 1.0, _ptr(out), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
+                                 float(k_scale), float(v_scale), _ptr(out), _ptr(lse), _ptr(ws),
+                                 0 if ws is None else ws.numel(),
                                  _ptr(err_flag), _stream(stream))
     _check(st)
     return (out, lse) if (return_lse or lse is not None) else out

@@ -325,6 +325,24 @@ def make_varlen_paged(q_lens, prefix_lens, num_heads, num_kv_heads, head_dim, bl
         slot_mapping=_as_i32(slots, device), extra={"prefix_lens": prefix_lens})
 
 
+def gather_tokens(wl: VarlenWorkload) -> int:
+    """Summed key counts of the sequences with more than one query (the prefill gather bound)."""
+    return int(np.sum(wl.k_lens[wl.q_lens > 1]))
+
+
+def to_fp8_cache(wl: VarlenWorkload) -> VarlenWorkload:
+    """The same paged workload with an FP8 E4M3 cache: per-tensor absmax/448 scales over the
+    history and the new tokens, history codes laid down with torch's float8 cast."""
+    ks, kinv = per_tensor_fp8_scales(torch.cat([wl.k_cache.reshape(-1), wl.k_new.reshape(-1)]))
+    vs, vinv = per_tensor_fp8_scales(torch.cat([wl.v_cache.reshape(-1), wl.v_new.reshape(-1)]))
+    out = VarlenWorkload(**{f: getattr(wl, f) for f in wl.__dataclass_fields__})
+    out.k_cache = fp8_codes_via_torch(wl.k_cache, kinv)
+    out.v_cache = fp8_codes_via_torch(wl.v_cache, vinv)
+    out.extra = dict(wl.extra, cache_dtype="fp8_e4m3", k_scale=ks, v_scale=vs, k_inv_scale=kinv, v_inv_scale=vinv)
+    out.name = wl.name + "_fp8"
+    return out
+
+
 def varlen_prefill(seed=1002, device="cpu", paged=False, batch=8, lo=128, hi=2048) -> VarlenWorkload:
     """8 sequences with q_len = k_len uniform in [128, 2048]; 32 q / 8 kv heads, d128.
 

@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 from paged_kv_cache_200_gb300 import workloads as W
-from _helpers import BF16_ATOL, BF16_RTOL, assert_close, bits, built_library, f64
+from _helpers import BF16_ATOL, BF16_RTOL, FP8_ATOL, FP8_RTOL, assert_close, bits, built_library, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -65,16 +65,19 @@ def test_varlen_packed_small(pkv, case):
 
 def _write_new_tokens(pkv, wl):
     kc, vc = wl.k_cache.clone(), wl.v_cache.clone()
-    pkv.kv_cache_write(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
+    pkv.kv_cache_write(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping, k_inv_scale=wl.extra.get("k_inv_scale", 1.0),
+                       v_inv_scale=wl.extra.get("v_inv_scale", 1.0))
     return kc, vc
 
 
-def _paged(pkv, wl, kc, vc):
+def _paged(pkv, wl, kc, vc, gather=False):
+    """Paged varlen; gather=True gives the library the bound that lets it gather K/V into a packed buffer."""
     shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = pkv.paged_attn_varlen(wl.q, kc.view(shape4), vc.view(shape4), wl.cu_seqlens_q, wl.cu_seqlens_k,
                                      wl.max_len_q, wl.max_len_k, block_table=wl.block_table, scale=wl.scale,
-                                     return_lse=True, err_flag=err)
+                                     return_lse=True, err_flag=err, gather_k_tokens=W.gather_tokens(wl) if gather else 0,
+                                     k_scale=wl.extra.get("k_scale", 1.0), v_scale=wl.extra.get("v_scale", 1.0))
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     return out, lse
@@ -93,13 +96,14 @@ PAGED = [
 ]
 
 
+@pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
 @pytest.mark.parametrize("case", PAGED, ids=[f"bs{c[5]}_{c[2]}q{c[3]}kv_d{c[4]}_{i}" for i, c in enumerate(PAGED)])
-def test_varlen_paged_small(pkv, case):
+def test_varlen_paged_small(pkv, case, gather):
     q_lens, prefix, Hq, Hkv, D, bs = case
     wl = W.make_varlen_paged(q_lens, prefix, Hq, Hkv, D, bs, seed=sum(q_lens) + sum(prefix) + bs, device="cuda",
                              extra_blocks=3)
     kc, vc = _write_new_tokens(pkv, wl)
-    out, lse = _paged(pkv, wl, kc, vc)
+    out, lse = _paged(pkv, wl, kc, vc, gather=gather)
     ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
                                        wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
                                        block_table=wl.block_table.cpu().numpy(), block_size=bs)
@@ -200,10 +204,11 @@ def test_varlen_prefill_full_size_packed(pkv):
     assert torch.isfinite(out.float()).all()
 
 
-def test_varlen_prefill_full_size_paged(pkv):
+@pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
+def test_varlen_prefill_full_size_paged(pkv, gather):
     wl = W.varlen_prefill(device="cuda", paged=True)
     kc, vc = _write_new_tokens(pkv, wl)
-    out, lse = _paged(pkv, wl, kc, vc)
+    out, lse = _paged(pkv, wl, kc, vc, gather=gather)
     seqs = [int(np.argmax(wl.q_lens)), 3]
     ks, vs, tsub = _sub_pool(wl, kc, vc, seqs)
     ref, ref_lse = O.paged_attn_varlen(bits(wl.q), ks, vs, wl.cu_seqlens_q.cpu().numpy(),
@@ -213,11 +218,12 @@ def test_varlen_prefill_full_size_paged(pkv):
     assert torch.isfinite(out.float()).all()
 
 
-def test_mixed_chunked_full_size(pkv):
+@pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
+def test_mixed_chunked_full_size(pkv, gather):
     """Four 512-query chunks over 0/2K/4K/8K prefixes (two sharing blocks) + 60 decode rows, one call."""
     wl = W.mixed_chunked(device="cuda")
     kc, vc = _write_new_tokens(pkv, wl)
-    out, lse = _paged(pkv, wl, kc, vc)
+    out, lse = _paged(pkv, wl, kc, vc, gather=gather)
     seqs = [0, 1, 2, 3, 4, 30, 63]
     ks, vs, tsub = _sub_pool(wl, kc, vc, seqs)
     ref, ref_lse = O.paged_attn_varlen(bits(wl.q), ks, vs, wl.cu_seqlens_q.cpu().numpy(),
@@ -225,3 +231,60 @@ def test_mixed_chunked_full_size(pkv):
                                        block_size=wl.block_size, seqs=seqs)
     _check_rows(out, lse, ref, ref_lse, rows=_rows_of(wl, seqs), what="mixed")
     assert torch.isfinite(out.float()).all()
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 cache in prefill (K/V gathered and widened, scales folded)
+# ---------------------------------------------------------------------------
+
+
+FP8_PAGED = [
+    # (q_lens, prefix_lens, Hq, Hkv, D, bs)
+    ([128, 50, 300], [0, 0, 0], 8, 2, 128, 16),
+    ([200, 1, 1, 64], [0, 700, 33, 900], 32, 8, 128, 16),
+    ([90, 260], [130, 0], 4, 1, 64, 64),
+    ([150, 150], [600, 5], 8, 2, 128, 256),
+]
+
+
+@pytest.mark.parametrize("case", FP8_PAGED, ids=[f"bs{c[5]}_{c[2]}q{c[3]}kv_d{c[4]}_{i}" for i, c in
+                                                 enumerate(FP8_PAGED)])
+def test_varlen_paged_fp8(pkv, case):
+    q_lens, prefix, Hq, Hkv, D, bs = case
+    wl = W.to_fp8_cache(W.make_varlen_paged(q_lens, prefix, Hq, Hkv, D, bs, seed=sum(q_lens) + 7, device="cuda",
+                                            extra_blocks=2))
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=True)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=bs,
+                                       kv_dtype="fp8_e4m3", k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+    assert_close(f64(out), ref, FP8_ATOL, FP8_RTOL, f"fp8 {case}")
+    assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"fp8 lse {case}")
+
+
+def test_varlen_prefill_full_size_paged_fp8(pkv):
+    wl = W.to_fp8_cache(W.varlen_prefill(device="cuda", paged=True))
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=True)
+    seqs = [int(np.argmax(wl.q_lens)), 3]
+    ks, vs, tsub = _sub_pool(wl, kc, vc, seqs)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), ks, vs, wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True, block_table=tsub,
+                                       block_size=wl.block_size, seqs=seqs, kv_dtype="fp8_e4m3",
+                                       k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+    rows = _rows_of(wl, seqs)
+    assert_close(f64(out)[rows], ref[rows], FP8_ATOL, FP8_RTOL, "prefill paged fp8")
+
+
+def test_gather_bound_too_small_is_flagged(pkv):
+    """Keys past the caller's gather bound are not gathered; the call flags it and faults nothing."""
+    wl = W.make_varlen_paged([300, 200], [100, 0], 8, 2, 128, 16, seed=99, device="cuda")
+    kc, vc = _write_new_tokens(pkv, wl)
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_attn_varlen(wl.q, kc.view(shape4), vc.view(shape4), wl.cu_seqlens_q, wl.cu_seqlens_k, wl.max_len_q,
+                          wl.max_len_k, block_table=wl.block_table, scale=wl.scale, err_flag=err,
+                          gather_k_tokens=W.gather_tokens(wl) - 100)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 4  # PKV_DEVERR_LENGTH
