@@ -750,7 +750,25 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
 // its cache slot to row cu_g[b] + j of a packed bf16 buffer, for K and V.  An
 // FP8 cache is widened exactly (every E4M3 value is a bf16 value; the scales
 // are applied by the attention).  Bad block ids are flagged and give zero rows;
-// rows at or past `cap` are not written.  CTA (t, b): positions [64 t, 64 t + 64).
+// rows at or past `cap` are not written.  CTA (t, b): positions
+// [kGatherPos t, kGatherPos (t + 1)), one warp per position at a time; a lane
+// issues all of its loads of a round (K and V) before its stores.
+constexpr int kGatherPos = 16;
+
+__device__ __forceinline__ uint4 widen8_e4m3(uint2 codes) {
+  const uint32_t cw[2] = {codes.x, codes.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t lo = e4m3x2_lo_to_f16x2(cw[h]), hi = e4m3x2_hi_to_f16x2(cw[h]);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    o[2 * h] = pack_bf16x2(a.x, a.y);
+    o[2 * h + 1] = pack_bf16x2(c.x, c.y);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 template <bool kFp8>
 __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restrict__ k_cache,
                                                         const uint8_t* __restrict__ v_cache,
@@ -761,6 +779,7 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restric
                                                         int32_t block_size, int32_t num_blocks, int32_t row_elems,
                                                         int route, int64_t cap, uint16_t* __restrict__ k_out,
                                                         uint16_t* __restrict__ v_out, int32_t* err) {
+  constexpr int kPer = 4;  // 16-byte output vectors per lane and tensor in one round
   const int b = blockIdx.y;
   const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
   if (lq <= 0 || (route && lq == 1)) return;
@@ -769,40 +788,43 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restric
     lk = max_blocks * block_size;
     if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, PKV_DEVERR_LENGTH);
   }
+  const int j0 = blockIdx.x * kGatherPos;
+  if (j0 >= lk) return;
   const int64_t g0 = __ldg(cu_g + b);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunks = row_elems >> 3;  // 16-byte bf16 vectors per row
-  for (int j = blockIdx.x * 64 + warp; j < min(lk, blockIdx.x * 64 + 64); j += 8) {
+  for (int j = j0 + warp; j < min(lk, j0 + kGatherPos); j += 8) {
     const int64_t row = g0 + j;
     if (row >= cap) break;
-    int blk = __ldg(block_table + (int64_t)b * max_blocks + j / block_size);
+    const int blk = __ldg(block_table + (int64_t)b * max_blocks + j / block_size);
     const bool bad = blk < 0 || blk >= num_blocks;
     if (bad && lane == 0) flag_error(err, PKV_DEVERR_BLOCK);
     const int64_t slot = bad ? 0 : (int64_t)blk * block_size + j % block_size;
-    for (int t = 0; t < 2; ++t) {
-      const uint8_t* src = t ? v_cache : k_cache;
-      uint4* dst = reinterpret_cast<uint4*>((t ? v_out : k_out) + row * row_elems);
-      for (int c = lane; c < chunks; c += 32) {
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (!bad) {
-          if constexpr (!kFp8) {
-            w = __ldg(reinterpret_cast<const uint4*>(src + slot * row_elems * 2) + c);
-          } else {
-            const uint2 codes = __ldg(reinterpret_cast<const uint2*>(src + slot * row_elems) + c);
-            const uint32_t cw[2] = {codes.x, codes.y};
-            uint32_t o[4];
+    uint4* kd = reinterpret_cast<uint4*>(k_out + row * row_elems);
+    uint4* vd = reinterpret_cast<uint4*>(v_out + row * row_elems);
+    for (int base = 0; base < chunks; base += 32 * kPer) {
+      uint4 kr[kPer], vr[kPer];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t lo = e4m3x2_lo_to_f16x2(cw[h]), hi = e4m3x2_hi_to_f16x2(cw[h]);
-              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-              const float2 bb = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-              o[2 * h] = pack_bf16x2(a.x, a.y);
-              o[2 * h + 1] = pack_bf16x2(bb.x, bb.y);
-            }
-            w = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int u = 0; u < kPer; ++u) {
+        const int c = base + u * 32 + lane;
+        kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < chunks && !bad) {
+          if constexpr (!kFp8) {
+            kr[u] = __ldg(reinterpret_cast<const uint4*>(k_cache + slot * row_elems * 2) + c);
+            vr[u] = __ldg(reinterpret_cast<const uint4*>(v_cache + slot * row_elems * 2) + c);
+          } else {
+            kr[u] = widen8_e4m3(__ldg(reinterpret_cast<const uint2*>(k_cache + slot * row_elems) + c));
+            vr[u] = widen8_e4m3(__ldg(reinterpret_cast<const uint2*>(v_cache + slot * row_elems) + c));
           }
         }
-        dst[c] = w;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int c = base + u * 32 + lane;
+        if (c < chunks) {
+          kd[c] = kr[u];
+          vd[c] = vr[u];
+        }
       }
     }
   }
@@ -982,7 +1004,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   varlen_prep_kernel<<<1, (route || gather) ? 1024 : 32, 0, st>>>(cu_seqlens_q, cu_seqlens_k, batch, items, count,
                                                                   p.item_counter, cu_g, (int64_t)total_k, err_flag);
   if (gather) {
-    const dim3 ggrid((unsigned)((max_len_k + 63) / 64 > 0 ? (max_len_k + 63) / 64 : 1), (unsigned)batch, 1);
+    const int gx = (max_len_k + kGatherPos - 1) / kGatherPos;
+    const dim3 ggrid((unsigned)(gx > 0 ? gx : 1), (unsigned)batch, 1);
     const int row_elems = num_kv_heads * head_dim;
     uint16_t* gk = reinterpret_cast<uint16_t*>(wsb + wl.gk_off);
     uint16_t* gv = reinterpret_cast<uint16_t*>(wsb + wl.gv_off);
