@@ -159,7 +159,8 @@ struct Smem {
   static constexpr int kNumBars = 28;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag, 4 ring slots
   static constexpr int kXchg = kMisc + 32;              // float m[2][128], l[2][128]
-  static constexpr int kTotal = kXchg + 4 * 128 * 4;
+  static constexpr int kStage = kXchg + 4 * 128 * 4;    // output staging: 8 softmax warps x 16 half rows
+  static constexpr int kTotal = kStage + 8 * 16 * D;
   static constexpr int kAlloc = kTotal + 1024;          // slack to align the base to 1024
 };
 
@@ -639,7 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = l0 * f0 + l1 * f1;
       const float inv = lt > 0.f ? p.v_mul / lt : 0.f;
       const float w0 = f0 * inv, w1 = f1 * inv;
-      // this half writes head dims [half*D/2, (half+1)*D/2)
+      // this half writes head dims [half*D/2, (half+1)*D/2) of every row
+      constexpr int kHalfRowBytes = D;           // D/2 bf16
+      constexpr int kCh = kHalfRowBytes / 16;    // 16-byte pieces of a half row
+      uint4 mine[kCh];
 #pragma unroll
       for (int ch = 0; ch < D / 64; ++ch) {
         const int col = half * (D / 2) + ch * 32;
@@ -647,20 +651,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         PKV_TMEM_LD32(tO(0) + lane_off + col, a);
         PKV_TMEM_LD32(tO(1) + lane_off + col, bb);
         tmem_wait_ld();
-        if (row_valid) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 8) {
-            float v[8];
+        for (int k = 0; k < 32; k += 8) {
+          float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(a[k + e]) * w0 + __uint_as_float(bb[k + e]) * w1;
-            uint4 o4;
-            o4.x = pack_bf16x2(v[0], v[1]);
-            o4.y = pack_bf16x2(v[2], v[3]);
-            o4.z = pack_bf16x2(v[4], v[5]);
-            o4.w = pack_bf16x2(v[6], v[7]);
-            *reinterpret_cast<uint4*>(orow + col + k) = o4;
+          for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(a[k + e]) * w0 + __uint_as_float(bb[k + e]) * w1;
+          mine[(ch * 32 + k) / 8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        }
+      }
+      // Rows of one head are num_heads*D elements apart, so a thread storing
+      // its own row would touch a separate line per 16 bytes.  Instead the
+      // warp passes 16 rows at a time through its staging rows in shared
+      // memory (16-byte pieces XOR-swizzled by row) and stores whole half rows.
+      uint8_t* stg = smem + L::kStage + (warp - 2) * 16 * kHalfRowBytes;
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        if ((lane >> 4) == pass) {
+          const int sr = lane & 15;
+#pragma unroll
+          for (int c = 0; c < kCh; ++c)
+            *reinterpret_cast<uint4*>(stg + sr * kHalfRowBytes + ((c ^ (sr & (kCh - 1))) * 16)) = mine[c];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16 * kCh / 32; ++i) {
+          const int idx = i * 32 + lane;
+          const int sr = idx / kCh, c = idx % kCh;
+          const int rr = quarter * 32 + pass * 16 + sr;  // row within the tile
+          if (rr < sq.rows) {
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + sr * kHalfRowBytes + ((c ^ (sr & (kCh - 1))) * 16));
+            uint16_t* dst = p.out + ((int64_t)(sq.q0 + sq.row0 + rr) * p.num_heads + x.head) * D + half * (D / 2) + c * 8;
+            *reinterpret_cast<uint4*>(dst) = val;
           }
         }
+        __syncwarp();
       }
       if (half == 0 && row_valid && p.lse != nullptr)
         p.lse[(int64_t)x.head * p.total_q + row] = lt > 0.f ? (ms + log2f(lt)) * kLn2 : -INFINITY;
