@@ -421,6 +421,7 @@ def extra_workloads(pkv, W, device, pk, args):
     if hasattr(pkv, "paged_attn_varlen") and hasattr(pkv.lib(), "pkv_paged_attn_varlen"):
         out.update(prefill_workload(pkv, W, device, pk, args))
     out.update(with_kvcache_workload(pkv, W, device, pk, args))
+    out.update(multi_query_workload(pkv, W, device, pk, args))
     out.update(copy_workload(pkv, W, device, pk, args))
     out.update(write_sweep(pkv, device, pk, args))
     return out
@@ -451,6 +452,35 @@ def with_kvcache_workload(pkv, W, device, pk, args):
         "GB_per_s": b / (ms_f * 1e-3) / 1e9, "frac_of_hbm_peak": b / (ms_f * 1e-3) / 1e9 / pk["hbm_gbs"],
         "tokens_per_s": wl.batch / (ms_f * 1e-3), "iters": iters}}
     del step, wl
+    torch.cuda.empty_cache()
+    return res
+
+
+def multi_query_workload(pkv, W, device, pk, args):
+    """Speculative verification: 64 sequences with 4 new tokens each over U[1024,16384] cached tokens, one varlen call."""
+    rng = np.random.default_rng(1008)
+    prefix = rng.integers(1024, 16384, size=64, endpoint=True)
+    wl = W.make_varlen_paged(np.full(64, 4), prefix, 32, 8, 128, 16, seed=1009, device=device)
+    sh = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    kc, vc = wl.k_cache.view(sh), wl.v_cache.view(sh)
+    need = pkv.lib().pkv_paged_attn_varlen_workspace(wl.batch, wl.total_q, 0, wl.num_heads, wl.num_kv_heads,
+                                                      wl.head_dim, wl.max_len_q, wl.max_len_k, 1, 0, wl.block_size)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(wl.q)
+    pkv.kv_cache_write(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+    iters = max(10, min(100, args.steps // 20))
+    ms = time_calls(lambda: pkv.paged_attn_varlen(wl.q, kc, vc, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.max_len_q,
+                                                  wl.max_len_k, block_table=wl.block_table, scale=wl.scale, out=out,
+                                                  workspace_buf=ws), iters)
+    row = wl.num_kv_heads * wl.head_dim * 2 * 2  # K and V bytes per position
+    once = int(wl.k_lens.sum()) * row            # each sequence's K/V read once
+    per_query = int(sum(int(lk) - 4 + i + 1 for lk in wl.k_lens for i in range(4))) * row  # what the rows read
+    res = {"multi_query_decode": {
+        "workload": "64 seqs x 4 new tokens over U[1024,16384] cached tokens, 32 q / 8 kv, d128, bs16; every query "
+                    "row served by the split-KV decode kernels (one varlen call)", "ms": ms,
+        "GB_per_s_read": per_query / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": per_query / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "kv_bytes_once": once, "kv_bytes_read": per_query, "tokens_per_s": wl.total_q / (ms * 1e-3), "iters": iters}}
+    del wl, kc, vc, out, ws
     torch.cuda.empty_cache()
     return res
 

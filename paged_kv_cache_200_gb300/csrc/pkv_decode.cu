@@ -89,20 +89,34 @@ struct DecodeParams {
   float k_inv, v_inv;                  // FP8: 1 / scale of each cache
 };
 
-// Sequence served by grid index z (or -1), its q/out row and its length source.
-__device__ __forceinline__ int item_sequence(const DecodeParams& p, int z) {
+// Sequence served by grid index z (or -1) and, in varlen mode, which of its
+// queries (qi): a routed item is b * kRouteCode + qi.
+__device__ __forceinline__ int item_sequence(const DecodeParams& p, int z, int& qi) {
+  qi = 0;
   if (p.items == nullptr) return z;
   if (z >= __ldg(p.item_count)) return -1;
-  return __ldg(p.items + z);
+  const int code = __ldg(p.items + z);
+  qi = code % kRouteCode;
+  return code / kRouteCode;
 }
-__device__ __forceinline__ int64_t item_row(const DecodeParams& p, int b) {
-  return p.cu_q != nullptr ? (int64_t)__ldg(p.cu_q + b) : (int64_t)b;
+__device__ __forceinline__ int64_t item_row(const DecodeParams& p, int b, int qi) {
+  return p.cu_q != nullptr ? (int64_t)__ldg(p.cu_q + b) + qi : (int64_t)b;
 }
 
-// Attended length of sequence b, clamped to what the block table and the
-// workspace can hold (violations are flagged by the caller thread).
-__device__ __forceinline__ int attended_length(const DecodeParams& p, int b, bool report) {
-  int len = p.cu_k != nullptr ? __ldg(p.cu_k + b + 1) - __ldg(p.cu_k + b) : __ldg(p.seqlens + b);
+// Attended length of sequence b (query qi of a varlen sequence sees the keys
+// up to qi + Lk - Lq, bottom-right causal), clamped to what the block table and
+// the workspace can hold (violations are flagged by the caller thread).
+__device__ __forceinline__ int attended_length(const DecodeParams& p, int b, int qi, bool report) {
+  int len;
+  if (p.cu_k != nullptr) {
+    const int lk = __ldg(p.cu_k + b + 1) - __ldg(p.cu_k + b);
+    const int lq = __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b);
+    len = qi + lk - lq + 1;
+    if (len < 0 && lk >= 0) len = 0;  // a query that sees no key (not an error)
+    if (len > lk) len = lk;
+  } else {
+    len = __ldg(p.seqlens + b);
+  }
   if (p.k_new != nullptr && len >= 0) len += 1;  // the appended token
   const int64_t cap_bt = (int64_t)p.max_blocks * p.block_size;
   const int64_t cap_ws = (int64_t)p.max_splits * p.split_tokens;
@@ -153,11 +167,12 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int z = blockIdx.z;
-  const int b = item_sequence(p, z);
+  int qi;
+  const int b = item_sequence(p, z, qi);
   if (b < 0) return;
-  const int64_t qrow_idx = item_row(p, b);
+  const int64_t qrow_idx = item_row(p, b, qi);
 
-  const int len = attended_length(p, b, split == 0 && kvh == 0 && threadIdx.x == 0);
+  const int len = attended_length(p, b, qi, split == 0 && kvh == 0 && threadIdx.x == 0);
   const int n_splits = (len + p.split_tokens - 1) / p.split_tokens;
   if (split >= (n_splits > 0 ? n_splits : 1)) return;
   const int t_begin = split * p.split_tokens;
@@ -506,10 +521,11 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   if (bh >= (int64_t)batch * p.num_heads) return;
   const int z = (int)(bh / p.num_heads);
   const int hq = (int)(bh % p.num_heads);
-  const int b = item_sequence(p, z);
+  int qi;
+  const int b = item_sequence(p, z, qi);
   if (b < 0) return;
-  const int64_t row = item_row(p, b);
-  const int len = attended_length(p, b, false);
+  const int64_t row = item_row(p, b, qi);
+  const int len = attended_length(p, b, qi, false);
   const int n = (len + p.split_tokens - 1) / p.split_tokens;
   if (n <= 1) return;
   const float* ls = p.ws_lse + bh * p.max_splits;

@@ -26,7 +26,16 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 bool make_tmap_3d(CUtensorMap* map, const void* base, int elt_bytes, int64_t rows, int heads, int dim,
                   int box_inner, int box_rows, int swizzle_bytes);
 
-// Decode kernels serving the single-query sequences of a paged varlen batch.
+// Varlen sequences with at most kRouteMaxQ queries are served by the decode
+// kernels, one item per query row (coded b * kRouteCode + qi); longer ones by
+// the prefill tiles.
+constexpr int kRouteMaxQ = 8;
+constexpr int kRouteCode = 16;
+static_assert(kRouteMaxQ < kRouteCode, "query index must fit the item code");
+
+// Decode kernels serving the routed query rows of a paged varlen batch
+// (`batch` is the bound on routed items).
+
 size_t varlen_decode_workspace(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k);
 int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* items,
                          const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,

@@ -221,7 +221,7 @@ __device__ __forceinline__ Seq seq_info(const PrefillParams& p, int b, int qtile
   s.row0 = qtile * kBM;
   s.rows = min(kBM, s.Lq - s.row0);
   s.diag = s.Lk - s.Lq;
-  s.skip = s.rows <= 0 || (p.route_decode && s.Lq == 1);
+  s.skip = s.rows <= 0 || (p.route_decode && s.Lq <= kRouteMaxQ);
   const int kmax = s.row0 + s.rows - 1 + s.diag;  // last key the last row sees
   const int kv_tiles = (s.Lk + kBN - 1) / kBN;
   s.n_kv = kmax < 0 ? 0 : min(kmax / kBN + 1, kv_tiles);
@@ -714,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __restrict__ cu_q,
                                                            const int32_t* __restrict__ cu_k, int batch,
                                                            int32_t* __restrict__ items, int32_t* __restrict__ count,
-                                                           int32_t* __restrict__ item_counter,
+                                                           int32_t* __restrict__ item_counter, int route_cap,
                                                            int32_t* __restrict__ cu_g, int64_t gather_cap,
                                                            int32_t* err) {
   __shared__ int n;
@@ -726,11 +726,18 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
   }
   __syncthreads();
   if (items != nullptr) {
+    // every query row of a sequence with 1..kRouteMaxQ queries (item codes
+    // b * kRouteCode + qi; the bound route_cap holds them all)
     for (int b = threadIdx.x; b < batch; b += blockDim.x) {
-      if (__ldg(cu_q + b + 1) - __ldg(cu_q + b) == 1) items[atomicAdd(&n, 1)] = b;
+      const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
+      if (lq >= 1 && lq <= kRouteMaxQ) {
+        const int base = atomicAdd(&n, lq);
+        for (int i = 0; i < lq; ++i)
+          if (base + i < route_cap) items[base + i] = b * kRouteCode + i;
+      }
     }
     __syncthreads();
-    if (threadIdx.x == 0) *count = n;
+    if (threadIdx.x == 0) *count = n < route_cap ? n : route_cap;
   }
   if (cu_g != nullptr) {
     // Packed offsets of the gathered sequences (those the prefill kernel
@@ -745,7 +752,7 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
       if (b < batch) {
         const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
         const int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
-        const bool gathered = lq > 0 && !(items != nullptr && lq == 1);
+        const bool gathered = lq > 0 && !(items != nullptr && lq <= kRouteMaxQ);
         v = gathered && lk > 0 ? lk : 0;
       }
       int64_t x = v;  // inclusive warp scan
@@ -807,7 +814,7 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restric
   constexpr int kPer = 4;  // 16-byte output vectors per lane and tensor in one round
   const int b = blockIdx.y;
   const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
-  if (lq <= 0 || (route && lq == 1)) return;
+  if (lq <= 0 || (route && lq <= kRouteMaxQ)) return;
   int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
   if ((int64_t)lk > (int64_t)max_blocks * block_size) {  // more keys than the table holds
     lk = max_blocks * block_size;
@@ -877,16 +884,23 @@ bool uses_gather(bool paged, int kv_dtype, int block_size, int64_t total_k) {
 // routed row list and the decode partials (paged mode), then, when K/V are
 // gathered, the packed offsets cu_g[batch+1] and the packed K and V buffers
 // of total_k rows each.
-VarlenWs varlen_ws_layout(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k, bool route,
-                          bool gather, int64_t total_k) {
+// Routed decode items: every query row of a sequence with at most
+// kRouteMaxQ queries, so at most min(total_q, kRouteMaxQ * batch).
+int route_items_bound(int batch, int total_q) {
+  const int64_t b = (int64_t)kRouteMaxQ * batch;
+  return (int)(b < total_q ? b : total_q);
+}
+
+VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
+                          bool route, bool gather, int64_t total_k) {
   VarlenWs w{0, 0, 0, 0, 0, 0, 256};
   if (batch <= 0) return w;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  if (route) {
+  if (route && route_items > 0) {
     w.count_off = 4;
     w.items_off = 256;
-    w.decode_off = w.items_off + up((size_t)batch * 4);
-    w.total = w.decode_off + varlen_decode_workspace(batch, num_heads, num_kv_heads, head_dim, max_len_k);
+    w.decode_off = w.items_off + up((size_t)route_items * 4);
+    w.total = w.decode_off + varlen_decode_workspace(route_items, num_heads, num_kv_heads, head_dim, max_len_k);
   }
   if (gather) {
     w.cu_g_off = up(w.total);
@@ -931,11 +945,13 @@ extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q
                                                   int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                                   int32_t max_len_q, int32_t max_len_k, int32_t paged,
                                                   int32_t kv_dtype, int32_t block_size) {
-  (void)total_q;
   (void)max_len_q;
-  if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_len_k < 0 || total_k < 0) return 0;
+  if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_len_k < 0 || total_k < 0 ||
+      total_q < 0)
+    return 0;
   const bool gather = pkv::uses_gather(paged != 0, kv_dtype, block_size, total_k);
-  return pkv::varlen_ws_layout(batch, num_heads, num_kv_heads, head_dim, max_len_k,
+  return pkv::varlen_ws_layout(batch, pkv::route_items_bound(batch, total_q), num_heads, num_kv_heads, head_dim,
+                               max_len_k,
                                routes_decode(paged != 0, num_heads, num_kv_heads), gather, total_k)
       .total;
 }
@@ -975,7 +991,9 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
 
   const bool route = routes_decode(paged, num_heads, num_kv_heads);
   const bool gather = uses_gather(paged, kv_dtype, block_size, total_k);
-  const VarlenWs wl = varlen_ws_layout(batch, num_heads, num_kv_heads, head_dim, max_len_k, route, gather, total_k);
+  const int route_items = route ? route_items_bound(batch, total_q) : 0;
+  const VarlenWs wl =
+      varlen_ws_layout(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, route, gather, total_k);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
                        (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
@@ -1021,13 +1039,13 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   int32_t* count = nullptr;
   int32_t* items = nullptr;
   p.item_counter = static_cast<int32_t*>(workspace);
-  if (route) {
+  if (route && route_items > 0) {
     count = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.count_off);
     items = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.items_off);
   }
   int32_t* cu_g = gather ? reinterpret_cast<int32_t*>(wsb + wl.cu_g_off) : nullptr;
-  varlen_prep_kernel<<<1, (route || gather) ? 1024 : 32, 0, st>>>(cu_seqlens_q, cu_seqlens_k, batch, items, count,
-                                                                  p.item_counter, cu_g, (int64_t)total_k, err_flag);
+  varlen_prep_kernel<<<1, (items != nullptr || gather) ? 1024 : 32, 0, st>>>(
+      cu_seqlens_q, cu_seqlens_k, batch, items, count, p.item_counter, route_items, cu_g, (int64_t)total_k, err_flag);
   if (gather) {
     const int gx = (max_len_k + kGatherPos - 1) / kGatherPos;
     const dim3 ggrid((unsigned)(gx > 0 ? gx : 1), (unsigned)batch, 1);
@@ -1052,9 +1070,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   else
     rc = packed_tiles ? launch_prefill<64, false>(mq, mk, mv, p, batch, st)
                       : launch_prefill<64, true>(mq, mk, mv, p, batch, st);
-  if (rc != PKV_OK || !route) return rc;
+  if (rc != PKV_OK || items == nullptr) return rc;
   return launch_varlen_decode(q, k, v, items, count, cu_seqlens_q, cu_seqlens_k, block_table, max_blocks_per_seq,
-                              batch, num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_len_k, total_q,
+                              route_items, num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_len_k,
+                              total_q,
                               scale, fp8, k_scale, v_scale, out, lse, wsb + wl.decode_off,
                               (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, st);
 }

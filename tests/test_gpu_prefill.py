@@ -288,3 +288,33 @@ def test_gather_bound_too_small_is_flagged(pkv):
                           gather_k_tokens=W.gather_tokens(wl) - 100)
     torch.cuda.synchronize()
     assert int(err.item()) & 4  # PKV_DEVERR_LENGTH
+
+
+# ---------------------------------------------------------------------------
+# several new tokens per sequence (speculative verification): each query row of
+# a sequence with up to 8 queries goes to the decode kernels
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
+def test_multi_query_decode_rows(pkv, dt, gather):
+    rng = np.random.default_rng(61)
+    q_lens = rng.integers(1, 9, size=12)            # 1..8 new tokens
+    q_lens[3] = 40                                  # and one longer chunk (prefill tiles)
+    prefix = rng.integers(0, 3000, size=12)
+    prefix[5] = 0                                   # a sequence that is only its new tokens
+    wl = W.make_varlen_paged(q_lens, prefix, 32, 8, 128, 16, seed=62, device="cuda")
+    if dt != "bf16":
+        wl = W.to_fp8_cache(wl)
+        if not gather:
+            pytest.skip("an FP8 cache is read through the gather")
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=gather)
+    kw = {} if dt == "bf16" else dict(kv_dtype="fp8_e4m3", k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=16, **kw)
+    atol, rtol = (BF16_ATOL, BF16_RTOL) if dt == "bf16" else (FP8_ATOL, FP8_RTOL)
+    assert_close(f64(out), ref, atol, rtol, f"multi-query {dt}")
+    assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"multi-query lse {dt}")
