@@ -11,6 +11,7 @@ softmax, no blocking: a reader can check each function against the pages.
 
 from .pkv_oracle import (  # noqa: F401
     E4M3_MAX,
+    INT8_MAX,
     attention_rows,
     bf16_bits_to_f64,
     cache_values_f64,
@@ -26,6 +27,7 @@ from .pkv_oracle import (  # noqa: F401
     paged_attn_decode_with_kvcache,
     paged_attn_varlen,
     quantize_to_e4m3,
+    quantize_to_int8,
     request_index,
     slot_of,
 )

@@ -132,12 +132,32 @@ def quantize_to_e4m3(x_bf16_bits, inv_scale) -> np.ndarray:
     return e4m3_encode_rne_satfinite(prod)
 
 
+INT8_MAX = 127
+
+
+def quantize_to_int8(x_bf16_bits, inv_scale) -> np.ndarray:
+    """INT8 KV quantisation: ``clamp(round_half_even(f32(x) * f32(inv_scale)), -127, 127)``.
+
+    [CH15] "KVキャッシュはどれくらいメモリを食う？" states that an INT8 cache, like FP8,
+    halves the KV size, and fixes nothing else.  Reading: symmetric codes with a
+    per-tensor scale (absmax / 127), one float32 multiply, round half to even,
+    saturation at +-127 (-128 unused so that the range is symmetric).  A NaN
+    input gives code 0.
+    """
+    x32 = (np.asarray(x_bf16_bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    prod = (x32 * np.float32(inv_scale)).astype(np.float32).astype(np.float64)
+    prod = np.where(np.isnan(prod), 0.0, prod)
+    return np.clip(np.rint(prod), -INT8_MAX, INT8_MAX).astype(np.int8)
+
+
 def cache_values_f64(cache, cache_dtype: str, scale: float = 1.0) -> np.ndarray:
-    """Values held by a cache (or K/V tensor) as fp64: bf16 bits or E4M3 codes * scale."""
+    """Values held by a cache (or K/V tensor) as fp64: bf16 bits, or E4M3 / INT8 codes * scale."""
     if cache_dtype == "bf16":
         return bf16_bits_to_f64(cache)
     if cache_dtype == "fp8_e4m3":
         return e4m3_decode(cache) * np.float64(np.float32(scale))
+    if cache_dtype == "int8":
+        return np.asarray(cache, dtype=np.int8).astype(np.float64) * np.float64(np.float32(scale))
     raise ValueError(f"unknown cache dtype {cache_dtype!r}")
 
 
@@ -228,6 +248,9 @@ def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, cache_dtype: str = "bf1
         elif cache_dtype == "fp8_e4m3":
             kc[s] = quantize_to_e4m3(k[t], k_inv_scale)
             vc[s] = quantize_to_e4m3(v[t], v_inv_scale)
+        elif cache_dtype == "int8":
+            kc[s] = quantize_to_int8(k[t], k_inv_scale)
+            vc[s] = quantize_to_int8(v[t], v_inv_scale)
         else:
             raise ValueError(cache_dtype)
     return kc, vc

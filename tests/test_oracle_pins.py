@@ -545,3 +545,30 @@ def test_decode_with_append_on_an_empty_cache_returns_the_new_value():
     out, _, _, _ = O.paged_attn_decode_with_kvcache(q, kn, vn, kc, vc, [0], np.array([[2, -1]]), 16, 0.5)
     assert np.array_equal(out[0, 0], O.bf16_bits_to_f64(vn[0, 0]))
     assert np.array_equal(out[0, 1], O.bf16_bits_to_f64(vn[0, 0]))
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV codes ([CH15] KV size: INT8 halves the cache; symmetric per-tensor reading)
+# ---------------------------------------------------------------------------
+
+
+def test_int8_quantiser_rounding_and_saturation():
+    vals = np.array([0.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, 127.0, 127.5, 300.0, -300.0, 3.25, -3.75],
+                    dtype=np.float32)
+    # every value above is exact in bf16; ties go to the even code, 127.5 saturates
+    codes = O.quantize_to_int8(_bf16_bits(vals), 1.0)
+    assert codes.tolist() == [0, 0, 2, 2, 0, -2, -2, 126, 127, 127, 127, -127, 3, -4]
+    inf = _bf16_bits(np.array([np.inf, -np.inf], dtype=np.float32))
+    assert O.quantize_to_int8(inf, 1.0).tolist() == [127, -127]
+
+
+def test_int8_codes_round_trip_and_dequantise():
+    codes = np.arange(-127, 128, dtype=np.int8)
+    vals = O.cache_values_f64(codes, "int8", 0.25)
+    assert np.array_equal(vals, codes.astype(np.float64) * 0.25)
+    # re-quantising the exact bf16 images of the values gives the codes back
+    back = O.quantize_to_int8(_bf16_bits(codes.astype(np.float32)), 1.0)
+    assert np.array_equal(back, codes)
+    # the scale is applied by one float32 multiply before the rounding
+    x = _bf16_bits(np.array([10.0], dtype=np.float32))
+    assert O.quantize_to_int8(x, np.float32(1.0 / 3.0)).tolist() == [3]
