@@ -169,7 +169,7 @@ def job_throughput_gbs(bytes_per_rank_step: int, ms_per_step_max: float, world: 
 
 def decode_bytes(wl):
     """Algorithmic HBM bytes of one decode call: attended K/V + Q + O."""
-    elt = 1 if wl.cache_dtype == "fp8_e4m3" else 2
+    elt = 1 if wl.cache_dtype in ("fp8_e4m3", "int8") else 2
     lens = wl.lens_before + 1
     kv = int(lens.sum()) * wl.num_kv_heads * wl.head_dim * elt * 2
     qo = 2 * wl.batch * wl.num_heads * wl.head_dim * 2
@@ -178,7 +178,7 @@ def decode_bytes(wl):
 
 def write_bytes(wl):
     """Algorithmic bytes of the KV write: new rows read (bf16) + stored (cache dtype), K and V."""
-    elt = 1 if wl.cache_dtype == "fp8_e4m3" else 2
+    elt = 1 if wl.cache_dtype in ("fp8_e4m3", "int8") else 2
     row = wl.num_kv_heads * wl.head_dim
     return wl.batch * row * (2 + elt) * 2
 
@@ -405,7 +405,7 @@ def run_pkv(args, rank, world, device):
 
 def extra_workloads(pkv, W, device, pk, args):
     out = {}
-    for dt in ("bf16", "fp8_e4m3"):
+    for dt in ("bf16", "fp8_e4m3", "int8"):
         wl = W.long_decode(device=device, cache_dtype=dt)
         step = DecodeStep(pkv, wl)
         steps = max(10, min(200, args.steps // 10))
@@ -516,8 +516,8 @@ def write_sweep(pkv, device, pk, args):
         k = torch.randn((T, 8, 128), generator=g, device=device).to(torch.bfloat16)
         v = torch.randn((T, 8, 128), generator=g, device=device).to(torch.bfloat16)
         slots = torch.randperm(T, generator=g, device=device).to(torch.int32)
-        for dt in ("bf16", "fp8_e4m3"):
-            cdt = torch.bfloat16 if dt == "bf16" else torch.uint8
+        for dt in ("bf16", "fp8_e4m3", "int8"):
+            cdt = {"bf16": torch.bfloat16, "fp8_e4m3": torch.uint8, "int8": torch.int8}[dt]
             kc = torch.empty((T, 8, 128), dtype=cdt, device=device)
             vc = torch.empty_like(kc)
             ms = time_calls(lambda: pkv.kv_cache_write(k, v, kc, vc, slots, k_inv_scale=0.25, v_inv_scale=0.25),

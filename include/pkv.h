@@ -71,8 +71,9 @@ typedef enum {
 } pkv_status;
 
 typedef enum {
-  PKV_BF16 = 0,     /* bfloat16 */
-  PKV_FP8_E4M3 = 2  /* OCP FP8 E4M3 (cache only), per-tensor scale */
+  PKV_BF16 = 0,      /* bfloat16 */
+  PKV_FP8_E4M3 = 2,  /* OCP FP8 E4M3 (cache only), per-tensor scale */
+  PKV_INT8 = 3       /* symmetric INT8 codes -127..127 (cache only), per-tensor scale */
 } pkv_dtype;
 
 /* bits of *err_flag */
@@ -103,10 +104,12 @@ PKV_API int pkv_abi_version(void);
  *                fused QKV projection) but must be multiples of 8 elements and
  *                the pointers 16-byte aligned.
  * k_cache, v_cache: [num_slots, num_kv_heads, head_dim] of cache_dtype, 16-byte aligned.
- * cache_dtype:   PKV_BF16 (bits copied) or PKV_FP8_E4M3: each element is stored as
+ * cache_dtype:   PKV_BF16 (bits copied), PKV_FP8_E4M3: each element is stored as
  *                e4m3_rne_satfinite(float(x) * inv_scale), one fp32 multiply
- *                and one round-to-nearest-even saturating conversion.
- * k_inv_scale, v_inv_scale: 1/scale of each FP8 cache (ignored for PKV_BF16).
+ *                and one round-to-nearest-even saturating conversion, or
+ *                PKV_INT8: clamp(round_half_even(float(x) * inv_scale), -127, 127)
+ *                ([CH15] KV size: FP8 or INT8 halve the cache; NaN stores 0).
+ * k_inv_scale, v_inv_scale: 1/scale of each FP8 / INT8 cache (ignored for PKV_BF16).
  * num_kv_heads*head_dim must be a multiple of 8.
  */
 PKV_API int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,

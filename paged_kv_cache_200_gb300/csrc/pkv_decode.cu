@@ -148,7 +148,8 @@ struct TileLayout {
   }
 };
 
-template <int D, bool kFp8, int kStages>
+// kFp8: one-byte codes (E4M3, or INT8 when kInt8) widened to f16 for f16 MMAs.
+template <int D, bool kFp8, int kStages, bool kInt8 = false>
 __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                               const DecodeParams p) {
@@ -159,6 +160,9 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
   constexpr int kWarpBytes = kStages * kStageBytes;
   constexpr int kDT = D / 16;
   constexpr int kBoxElems = TL::kBoxRow / (kFp8 ? 1 : 2);
+  // two one-byte codes (bytes 0..1, resp. 2..3, of a word) -> f16x2, exactly
+  auto code_lo = [](uint32_t w) { return kInt8 ? int8x2_lo_to_f16x2(w) : e4m3x2_lo_to_f16x2(w); };
+  auto code_hi = [](uint32_t w) { return kInt8 ? int8x2_hi_to_f16x2(w) : e4m3x2_hi_to_f16x2(w); };
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -296,7 +300,8 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
         uint8_t* row = const_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) +
                        (slot * p.num_kv_heads + kvh) * (int64_t)kRowBytes;
         if constexpr (kFp8)
-          reinterpret_cast<uint2*>(row)[c] = quantize8_e4m3(w, is_v ? p.v_inv : p.k_inv);
+          reinterpret_cast<uint2*>(row)[c] =
+              kInt8 ? quantize8_int8(w, is_v ? p.v_inv : p.k_inv) : quantize8_e4m3(w, is_v ? p.v_inv : p.k_inv);
         else
           reinterpret_cast<uint4*>(row)[c] = w;
         asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -353,10 +358,10 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
           for (int pp = 0; pp < kDT / 2; ++pp) {
             uint32_t r0, r1, r2, r3;
             ldmatrix_x4(ks + TL::offset(row, 2 * pp + csel), r0, r1, r2, r3);
-            mma_f16_16816(s, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
-                          e4m3x2_hi_to_f16x2(r1), qf[2 * pp][0], qf[2 * pp][1]);
-            mma_f16_16816(s2, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
-                          e4m3x2_hi_to_f16x2(r3), qf[2 * pp + 1][0], qf[2 * pp + 1][1]);
+            mma_f16_16816(s, code_lo(r0), code_lo(r1), code_hi(r0),
+                          code_hi(r1), qf[2 * pp][0], qf[2 * pp][1]);
+            mma_f16_16816(s2, code_lo(r2), code_lo(r3), code_hi(r2),
+                          code_hi(r3), qf[2 * pp + 1][0], qf[2 * pp + 1][1]);
           }
         }
 #pragma unroll
@@ -427,10 +432,10 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
             // (2j,2u), (2j+1,2u) | (2j,2u+1), (2j+1,2u+1) and widen: even dims, then odd dims
             const uint32_t t0 = prmt(r0, 0u, 0x3120u), t1 = prmt(r1, 0u, 0x3120u);
             const uint32_t t2 = prmt(r2, 0u, 0x3120u), t3 = prmt(r3, 0u, 0x3120u);
-            mma_f16_16816(o[2 * pp], e4m3x2_lo_to_f16x2(t0), e4m3x2_lo_to_f16x2(t1), e4m3x2_lo_to_f16x2(t2),
-                          e4m3x2_lo_to_f16x2(t3), pb0, pb1);
-            mma_f16_16816(o[2 * pp + 1], e4m3x2_hi_to_f16x2(t0), e4m3x2_hi_to_f16x2(t1), e4m3x2_hi_to_f16x2(t2),
-                          e4m3x2_hi_to_f16x2(t3), pb0, pb1);
+            mma_f16_16816(o[2 * pp], code_lo(t0), code_lo(t1), code_lo(t2),
+                          code_lo(t3), pb0, pb1);
+            mma_f16_16816(o[2 * pp + 1], code_hi(t0), code_hi(t1), code_hi(t2),
+                          code_hi(t3), pb0, pb1);
           }
         }
       }
@@ -599,7 +604,7 @@ SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, i
   return pl;
 }
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, bool kInt8 = false>
 int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t num_slots, cudaStream_t st) {
   constexpr int kStages = kFp8 ? 4 : 3;  // FP8: 3 CTAs (12 warps) per SM; bf16: 2 CTAs
   constexpr int kRowBytes = D * (kFp8 ? 1 : 2);
@@ -612,7 +617,7 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t
   if (!make_tmap_3d(&mk, p.k_cache, kFp8 ? 1 : 2, num_slots, p.num_kv_heads, D, box_elems, kGroupTok, TL::kSwizzle) ||
       !make_tmap_3d(&mv, p.v_cache, kFp8 ? 1 : 2, num_slots, p.num_kv_heads, D, box_elems, kGroupTok, TL::kSwizzle))
     return PKV_ERR_CUDA;
-  auto kern = paged_decode_split_kernel<D, kFp8, kStages>;
+  auto kern = paged_decode_split_kernel<D, kFp8, kStages, kInt8>;
   static bool attr_set[64] = {false};  // per instantiation and device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -629,6 +634,18 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t
     paged_decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p, batch);
   }
   return launch_status();
+}
+
+int dispatch_decode(int cache_dtype, int head_dim, const DecodeParams& p, int batch, const SplitPlan& pl,
+                    int64_t ns, cudaStream_t st) {
+  if (head_dim == 128) {
+    if (cache_dtype == PKV_FP8_E4M3) return launch_decode<128, true>(p, batch, pl, ns, st);
+    if (cache_dtype == PKV_INT8) return launch_decode<128, true, true>(p, batch, pl, ns, st);
+    return launch_decode<128, false>(p, batch, pl, ns, st);
+  }
+  if (cache_dtype == PKV_FP8_E4M3) return launch_decode<64, true>(p, batch, pl, ns, st);
+  if (cache_dtype == PKV_INT8) return launch_decode<64, true, true>(p, batch, pl, ns, st);
+  return launch_decode<64, false>(p, batch, pl, ns, st);
 }
 
 }  // namespace
@@ -665,10 +682,10 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
   if (num_heads / num_kv_heads > kMaxGroup) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
-  if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
-  if (cache_dtype == PKV_FP8_E4M3 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
-                                      !std::isfinite(v_scale)))
+  if (cache_dtype != PKV_BF16 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
+                                  !std::isfinite(v_scale)))
     return PKV_ERR_INVALID_ARG;
   if (batch == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !cache_seqlens || !block_table || !out) return PKV_ERR_INVALID_ARG;
@@ -695,9 +712,9 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
   p.num_blocks = num_blocks;
   p.split_tokens = pl.split_tokens;
   p.max_splits = pl.max_splits;
-  const bool fp8 = cache_dtype == PKV_FP8_E4M3;
-  p.scale_log2 = scale * kLog2e * (fp8 ? k_scale : 1.f);
-  p.v_mul = fp8 ? v_scale : 1.f;
+  const bool coded = cache_dtype != PKV_BF16;  // one-byte codes with per-tensor scales
+  p.scale_log2 = scale * kLog2e * (coded ? k_scale : 1.f);
+  p.v_mul = coded ? v_scale : 1.f;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   if (pl.max_splits > 1) {
@@ -718,9 +735,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
   }
   cudaStream_t st = as_stream(stream);
   const int64_t ns = (int64_t)num_blocks * block_size;
-  if (head_dim == 128)
-    return fp8 ? launch_decode<128, true>(p, batch, pl, ns, st) : launch_decode<128, false>(p, batch, pl, ns, st);
-  return fp8 ? launch_decode<64, true>(p, batch, pl, ns, st) : launch_decode<64, false>(p, batch, pl, ns, st);
+  return dispatch_decode(cache_dtype, head_dim, p, batch, pl, ns, st);
 }
 
 }  // namespace
@@ -767,23 +782,32 @@ extern "C" int pkv_paged_attn_decode_with_kvcache(const void* q, const void* k_n
 
 namespace pkv {
 
-size_t varlen_decode_workspace(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k) {
-  if (batch <= 0 || max_len_k <= 0) return 0;
-  return plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k).workspace;
+// Partials of `items` routed rows, split as a decode batch of `batch` sequences would be.
+size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k) {
+  if (batch <= 0 || items <= 0 || max_len_k <= 0) return 0;
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k);
+  if (pl.max_splits <= 1) return 0;
+  const size_t rows = (size_t)items * num_heads * pl.max_splits;
+  return rows * head_dim * sizeof(float) + ((rows * sizeof(float) + 255) / 256) * 256;
 }
 
-// Decode kernels over the single-query sequences of a paged varlen batch
-// (items[0..*item_count) on the device, at most `batch` of them).
+// Decode kernels over the routed query rows of a paged varlen batch
+// (items[0..*item_count) on the device, at most `items` of them); the split
+// size is planned for `batch` sequences.
 int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* items,
                          const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,
-                         const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
+                         const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t item_bound,
+                         int32_t num_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                         int32_t max_len_k, int64_t total_q, float scale, bool fp8, float k_scale, float v_scale,
-                         void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
-                         cudaStream_t st) {
+                         int32_t max_len_k, int64_t total_q, float scale, int cache_dtype, float k_scale,
+                         float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         int32_t* err_flag, cudaStream_t st) {
+  const bool fp8 = cache_dtype != PKV_BF16;  // one-byte codes
   if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
   const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1);
-  if (pl.workspace > workspace_bytes) return PKV_ERR_WORKSPACE;
+  if (varlen_decode_workspace(batch, item_bound, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1) >
+      workspace_bytes)
+    return PKV_ERR_WORKSPACE;
   DecodeParams p{};
   p.q = static_cast<const uint16_t*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
@@ -802,7 +826,7 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   if (pl.max_splits > 1) {
-    const size_t rows = (size_t)batch * num_heads * pl.max_splits;
+    const size_t rows = (size_t)item_bound * num_heads * pl.max_splits;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + rows * head_dim * sizeof(float));
   }
@@ -814,9 +838,7 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.lse_head_stride = total_q;
   p.lse_row_stride = 1;
   const int64_t ns = (int64_t)num_blocks * block_size;
-  if (head_dim == 128)
-    return fp8 ? launch_decode<128, true>(p, batch, pl, ns, st) : launch_decode<128, false>(p, batch, pl, ns, st);
-  return fp8 ? launch_decode<64, true>(p, batch, pl, ns, st) : launch_decode<64, false>(p, batch, pl, ns, st);
+  return dispatch_decode(cache_dtype, head_dim, p, item_bound, pl, ns, st);
 }
 
 }  // namespace pkv

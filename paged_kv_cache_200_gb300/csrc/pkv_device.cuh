@@ -114,6 +114,46 @@ __device__ __forceinline__ uint2 quantize8_e4m3(uint4 v, float inv) {
   return make_uint2(packed[0], packed[1]);
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Eight bf16 values -> eight INT8 codes, each
+// clamp(round_half_even(float(x) * inv), -127, 127); a NaN product gives 0
+// (the float-to-int conversion's rule), an infinity saturates.
+__device__ __forceinline__ uint2 quantize8_int8(uint4 v, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t word = w[e >> 1];
+    const float x = __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
+    int r = __float2int_rn(__fmul_rn(x, inv));
+    r = r > 127 ? 127 : (r < -127 ? -127 : r);
+    packed[e >> 2] |= ((uint32_t)r & 0xFFu) << (8 * (e & 3));
+  }
+  return make_uint2(packed[0], packed[1]);
+}
+
+// Two INT8 codes (bytes 0..1, resp. 2..3, of w) -> f16x2, exactly.  With the
+// sign bit flipped a code c becomes the unsigned byte c + 128; as the low
+// mantissa bits of an f16 whose exponent field gives 2^10 (high byte 0x64) it
+// reads 1024 + c + 128, and subtracting 1152 leaves c.
+__device__ __forceinline__ uint32_t int8x2_lo_to_f16x2(uint32_t w) {
+  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4140u);
+  uint32_t d;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
+  return d;
+}
+__device__ __forceinline__ uint32_t int8x2_hi_to_f16x2(uint32_t w) {
+  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4342u);
+  uint32_t d;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
+  return d;
+}
+
 // Packed fp32 pairs (sm_100+): two lanes of arithmetic per instruction.
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
   uint64_t r;
@@ -152,23 +192,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-// Two E4M3 codes placed in bits 8..15 and 24..31 of `t` (other bits zero) -> two
-// bfloat16 values equal to the codes' values times 2^-120, exactly.
-//
-// An E4M3 code s.eeee.mmm moved so that eeee lands in the low four bits of the
-// bf16 exponent field and mmm in the top three mantissa bits reads as
-// (1 + m/8) * 2^(e-127) for e > 0 and as the bf16 subnormal (m/8) * 2^-126 for
-// e == 0: in both cases the code's value (1+m/8)*2^(e-7), resp. (m/8)*2^-6,
-// times 2^-120.  Callers fold 2^120 into their fp32 scale factors.
-__device__ __forceinline__ uint32_t e4m3x2_hi_bytes_to_bf16x2_scaled(uint32_t t) {
-  return (t & 0x80008000u) | ((t & 0x7F007F00u) >> 4);
-}
 
 // ---------------------------------------------------------------------------
 // mbarrier, TMA and timer helpers

@@ -26,23 +26,25 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 bool make_tmap_3d(CUtensorMap* map, const void* base, int elt_bytes, int64_t rows, int heads, int dim,
                   int box_inner, int box_rows, int swizzle_bytes);
 
-// Varlen sequences with at most kRouteMaxQ queries are served by the decode
-// kernels, one item per query row (coded b * kRouteCode + qi); longer ones by
-// the prefill tiles.
+// Varlen sequences with few queries are served by the decode kernels, one
+// item per query row (coded b * kRouteCode + qi): those with one query always,
+// and those with up to kRouteMaxQ when no sequence of the batch has more
+// (speculative verification); longer ones by the prefill tiles.
 constexpr int kRouteMaxQ = 8;
 constexpr int kRouteCode = 16;
 static_assert(kRouteMaxQ < kRouteCode, "query index must fit the item code");
 
 // Decode kernels serving the routed query rows of a paged varlen batch
-// (`batch` is the bound on routed items).
+// (at most item_bound of them; splits planned for `batch` sequences).
 
-size_t varlen_decode_workspace(int batch, int num_heads, int num_kv_heads, int head_dim, int max_len_k);
+size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k);
 int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* items,
                          const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,
-                         const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t num_heads,
+                         const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t item_bound,
+                         int32_t num_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                         int32_t max_len_k, int64_t total_q, float scale, bool fp8, float k_scale, float v_scale,
-                         void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
-                         cudaStream_t st);
+                         int32_t max_len_k, int64_t total_q, float scale, int cache_dtype, float k_scale,
+                         float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         int32_t* err_flag, cudaStream_t st);
 
 }  // namespace pkv

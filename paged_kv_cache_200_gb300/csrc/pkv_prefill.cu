@@ -60,7 +60,7 @@ struct PrefillParams {
   int32_t group;
   int32_t n_qtiles;
   int32_t batch;
-  int32_t route_decode;  // sequences with exactly one query are left to the decode kernels
+  int32_t route_decode;  // sequences with at most this many queries are left to the decode kernels (0: none)
   int32_t* item_counter; // work-item counter, zero at launch
   float scale_log2;
   float v_mul;           // output factor (FP8 V scale of a gathered cache, else 1)
@@ -221,7 +221,7 @@ __device__ __forceinline__ Seq seq_info(const PrefillParams& p, int b, int qtile
   s.row0 = qtile * kBM;
   s.rows = min(kBM, s.Lq - s.row0);
   s.diag = s.Lk - s.Lq;
-  s.skip = s.rows <= 0 || (p.route_decode && s.Lq <= kRouteMaxQ);
+  s.skip = s.rows <= 0 || s.Lq <= p.route_decode;
   const int kmax = s.row0 + s.rows - 1 + s.diag;  // last key the last row sees
   const int kv_tiles = (s.Lk + kBN - 1) / kBN;
   s.n_kv = kmax < 0 ? 0 : min(kmax / kBN + 1, kv_tiles);
@@ -715,6 +715,7 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ cu_k, int batch,
                                                            int32_t* __restrict__ items, int32_t* __restrict__ count,
                                                            int32_t* __restrict__ item_counter, int route_cap,
+                                                           int route_max_q,
                                                            int32_t* __restrict__ cu_g, int64_t gather_cap,
                                                            int32_t* err) {
   __shared__ int n;
@@ -730,7 +731,7 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
     // b * kRouteCode + qi; the bound route_cap holds them all)
     for (int b = threadIdx.x; b < batch; b += blockDim.x) {
       const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
-      if (lq >= 1 && lq <= kRouteMaxQ) {
+      if (lq >= 1 && lq <= route_max_q) {
         const int base = atomicAdd(&n, lq);
         for (int i = 0; i < lq; ++i)
           if (base + i < route_cap) items[base + i] = b * kRouteCode + i;
@@ -752,7 +753,7 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
       if (b < batch) {
         const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
         const int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
-        const bool gathered = lq > 0 && !(items != nullptr && lq <= kRouteMaxQ);
+        const bool gathered = lq > route_max_q;
         v = gathered && lk > 0 ? lk : 0;
       }
       int64_t x = v;  // inclusive warp scan
@@ -801,7 +802,19 @@ __device__ __forceinline__ uint4 widen8_e4m3(uint2 codes) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-template <bool kFp8>
+__device__ __forceinline__ uint4 widen8_int8(uint2 codes) {
+  const uint32_t cw[2] = {codes.x, codes.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const int8_t c0 = (int8_t)(cw[e >> 2] >> (8 * (e & 3)));
+    const int8_t c1 = (int8_t)(cw[e >> 2] >> (8 * ((e & 3) + 1)));
+    o[e >> 1] = pack_bf16x2((float)c0, (float)c1);  // |c| <= 127: exact in bf16
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int kMode>  // 0: bf16 rows, 1: E4M3 codes, 2: INT8 codes
 __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restrict__ k_cache,
                                                         const uint8_t* __restrict__ v_cache,
                                                         const int32_t* __restrict__ cu_q,
@@ -814,7 +827,7 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restric
   constexpr int kPer = 4;  // 16-byte output vectors per lane and tensor in one round
   const int b = blockIdx.y;
   const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
-  if (lq <= 0 || (route && lq <= kRouteMaxQ)) return;
+  if (lq <= route) return;  // route: the routed query bound (0: none)
   int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
   if ((int64_t)lk > (int64_t)max_blocks * block_size) {  // more keys than the table holds
     lk = max_blocks * block_size;
@@ -841,12 +854,14 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restric
         const int c = base + u * 32 + lane;
         kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
         if (c < chunks && !bad) {
-          if constexpr (!kFp8) {
+          if constexpr (kMode == 0) {
             kr[u] = __ldg(reinterpret_cast<const uint4*>(k_cache + slot * row_elems * 2) + c);
             vr[u] = __ldg(reinterpret_cast<const uint4*>(v_cache + slot * row_elems * 2) + c);
           } else {
-            kr[u] = widen8_e4m3(__ldg(reinterpret_cast<const uint2*>(k_cache + slot * row_elems) + c));
-            vr[u] = widen8_e4m3(__ldg(reinterpret_cast<const uint2*>(v_cache + slot * row_elems) + c));
+            const uint2 kc2 = __ldg(reinterpret_cast<const uint2*>(k_cache + slot * row_elems) + c);
+            const uint2 vc2 = __ldg(reinterpret_cast<const uint2*>(v_cache + slot * row_elems) + c);
+            kr[u] = kMode == 1 ? widen8_e4m3(kc2) : widen8_int8(kc2);
+            vr[u] = kMode == 1 ? widen8_e4m3(vc2) : widen8_int8(vc2);
           }
         }
       }
@@ -877,18 +892,19 @@ struct VarlenWs {
 constexpr int kGatherBelowBlock = 64;
 
 bool uses_gather(bool paged, int kv_dtype, int block_size, int64_t total_k) {
-  return paged && total_k > 0 && (kv_dtype == PKV_FP8_E4M3 || block_size < kGatherBelowBlock);
+  return paged && total_k > 0 && (kv_dtype != PKV_BF16 || block_size < kGatherBelowBlock);
 }
 
 // [0, 256): the prefill work-item counter and the routed-row count; then the
 // routed row list and the decode partials (paged mode), then, when K/V are
 // gathered, the packed offsets cu_g[batch+1] and the packed K and V buffers
 // of total_k rows each.
-// Routed decode items: every query row of a sequence with at most
-// kRouteMaxQ queries, so at most min(total_q, kRouteMaxQ * batch).
-int route_items_bound(int batch, int total_q) {
-  const int64_t b = (int64_t)kRouteMaxQ * batch;
-  return (int)(b < total_q ? b : total_q);
+// Queries up to which a sequence is routed to the decode kernels: kRouteMaxQ
+// when no sequence of the batch has more (then every query row is routed and
+// there are total_q items), else 1 (then at most one item per sequence).
+int route_max_q(int max_len_q) { return max_len_q <= kRouteMaxQ ? kRouteMaxQ : 1; }
+int route_items_bound(int batch, int total_q, int max_len_q) {
+  return route_max_q(max_len_q) > 1 ? total_q : (batch < total_q ? batch : total_q);
 }
 
 VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
@@ -900,7 +916,7 @@ VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_
     w.count_off = 4;
     w.items_off = 256;
     w.decode_off = w.items_off + up((size_t)route_items * 4);
-    w.total = w.decode_off + varlen_decode_workspace(route_items, num_heads, num_kv_heads, head_dim, max_len_k);
+    w.total = w.decode_off + varlen_decode_workspace(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k);
   }
   if (gather) {
     w.cu_g_off = up(w.total);
@@ -945,12 +961,12 @@ extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q
                                                   int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                                   int32_t max_len_q, int32_t max_len_k, int32_t paged,
                                                   int32_t kv_dtype, int32_t block_size) {
-  (void)max_len_q;
   if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_len_k < 0 || total_k < 0 ||
       total_q < 0)
     return 0;
   const bool gather = pkv::uses_gather(paged != 0, kv_dtype, block_size, total_k);
-  return pkv::varlen_ws_layout(batch, pkv::route_items_bound(batch, total_q), num_heads, num_kv_heads, head_dim,
+  return pkv::varlen_ws_layout(batch, pkv::route_items_bound(batch, total_q, max_len_q), num_heads, num_kv_heads,
+                               head_dim,
                                max_len_k,
                                routes_decode(paged != 0, num_heads, num_kv_heads), gather, total_k)
       .total;
@@ -970,9 +986,9 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
     return PKV_ERR_INVALID_ARG;
   if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (head_dim != 128 && head_dim != 64) return PKV_ERR_UNSUPPORTED;
-  if (kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
-  const bool fp8 = kv_dtype == PKV_FP8_E4M3;
-  // an FP8 cache is read through the gather (paged mode, total_k > 0)
+  if (kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E4M3 && kv_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
+  const bool fp8 = kv_dtype != PKV_BF16;  // one-byte codes (E4M3 or INT8) with per-tensor scales
+  // a coded cache is read through the gather (paged mode, total_k > 0)
   if (fp8 && (block_table == nullptr || total_k <= 0)) return PKV_ERR_UNSUPPORTED;
   if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
     return PKV_ERR_INVALID_ARG;
@@ -991,7 +1007,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
 
   const bool route = routes_decode(paged, num_heads, num_kv_heads);
   const bool gather = uses_gather(paged, kv_dtype, block_size, total_k);
-  const int route_items = route ? route_items_bound(batch, total_q) : 0;
+  const int route_items = route ? route_items_bound(batch, total_q, max_len_q) : 0;
+  const int rmq = route ? route_max_q(max_len_q) : 0;  // queries up to which a sequence is routed
   const VarlenWs wl =
       varlen_ws_layout(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, route, gather, total_k);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
@@ -1026,7 +1043,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.group = num_heads / num_kv_heads;
   p.n_qtiles = (max_len_q + kBM - 1) / kBM;
   p.batch = batch;
-  p.route_decode = route ? 1 : 0;
+  p.route_decode = rmq;
   // FP8: the gathered codes are exact bf16 values; k_scale joins the logit
   // scale and v_scale the output factor
   p.scale_log2 = scale * kLog2e * (fp8 ? k_scale : 1.f);
@@ -1045,7 +1062,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   }
   int32_t* cu_g = gather ? reinterpret_cast<int32_t*>(wsb + wl.cu_g_off) : nullptr;
   varlen_prep_kernel<<<1, (items != nullptr || gather) ? 1024 : 32, 0, st>>>(
-      cu_seqlens_q, cu_seqlens_k, batch, items, count, p.item_counter, route_items, cu_g, (int64_t)total_k, err_flag);
+      cu_seqlens_q, cu_seqlens_k, batch, items, count, p.item_counter, route_items, rmq, cu_g, (int64_t)total_k,
+      err_flag);
   if (gather) {
     const int gx = (max_len_k + kGatherPos - 1) / kGatherPos;
     const dim3 ggrid((unsigned)(gx > 0 ? gx : 1), (unsigned)batch, 1);
@@ -1054,14 +1072,11 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
     uint16_t* gv = reinterpret_cast<uint16_t*>(wsb + wl.gv_off);
     const auto* kc = static_cast<const uint8_t*>(k);
     const auto* vc = static_cast<const uint8_t*>(v);
-    if (fp8)
-      gather_kv_kernel<true><<<ggrid, 256, 0, st>>>(kc, vc, cu_seqlens_q, cu_seqlens_k, cu_g, block_table,
-                                                     max_blocks_per_seq, block_size, num_blocks, row_elems,
-                                                     route ? 1 : 0, total_k, gk, gv, err_flag);
-    else
-      gather_kv_kernel<false><<<ggrid, 256, 0, st>>>(kc, vc, cu_seqlens_q, cu_seqlens_k, cu_g, block_table,
-                                                      max_blocks_per_seq, block_size, num_blocks, row_elems,
-                                                      route ? 1 : 0, total_k, gk, gv, err_flag);
+    auto gk_kern = kv_dtype == PKV_FP8_E4M3 ? gather_kv_kernel<1>
+                   : kv_dtype == PKV_INT8   ? gather_kv_kernel<2>
+                                            : gather_kv_kernel<0>;
+    gk_kern<<<ggrid, 256, 0, st>>>(kc, vc, cu_seqlens_q, cu_seqlens_k, cu_g, block_table, max_blocks_per_seq,
+                                   block_size, num_blocks, row_elems, rmq, total_k, gk, gv, err_flag);
   }
   int rc;
   if (head_dim == 128)
@@ -1072,8 +1087,9 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
                       : launch_prefill<64, true>(mq, mk, mv, p, batch, st);
   if (rc != PKV_OK || items == nullptr) return rc;
   return launch_varlen_decode(q, k, v, items, count, cu_seqlens_q, cu_seqlens_k, block_table, max_blocks_per_seq,
-                              route_items, num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_len_k,
+                              batch, route_items, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                              max_len_k,
                               total_q,
-                              scale, fp8, k_scale, v_scale, out, lse, wsb + wl.decode_off,
+                              scale, kv_dtype, k_scale, v_scale, out, lse, wsb + wl.decode_off,
                               (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, st);
 }

@@ -1,4 +1,4 @@
-// Slot-mapped KV-cache write (bf16 copy, or FP8 E4M3 quantise-on-write).
+// Slot-mapped KV-cache write (bf16 copy, or FP8 E4M3 / INT8 quantise-on-write).
 //
 // Source: "効率的な KV キャッシュ管理と Attention 計算" (itan.pw), section "Triton
 // カーネルによる KV キャッシュ書き込み": every new token's K and V row
@@ -23,7 +23,7 @@ namespace {
 constexpr int kWriteThreads = 256;
 constexpr int kWriteUnroll = 4;
 
-template <bool kFp8>
+template <int kMode>  // 0: bf16 copy, 1: FP8 E4M3, 2: INT8
 __global__ void __launch_bounds__(kWriteThreads) kv_cache_write_kernel(
     const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* __restrict__ v, int64_t v_stride,
     int32_t num_tokens, int32_t row_elems, void* __restrict__ k_cache, void* __restrict__ v_cache,
@@ -54,12 +54,12 @@ __global__ void __launch_bounds__(kWriteThreads) kv_cache_write_kernel(
       for (int u = 0; u < kWriteUnroll; ++u) {
         const int c = c0 + u * 32;
         if (c >= chunks) break;
-        if constexpr (!kFp8) {
+        if constexpr (kMode == 0) {
           uint4* dst = reinterpret_cast<uint4*>(is_v ? v_cache : k_cache) + (int64_t)slot * chunks + c;
           *dst = buf[u];
         } else {
           uint2* dst = reinterpret_cast<uint2*>(is_v ? v_cache : k_cache) + (int64_t)slot * chunks + c;
-          *dst = quantize8_e4m3(buf[u], inv);
+          *dst = kMode == 1 ? quantize8_e4m3(buf[u], inv) : quantize8_int8(buf[u], inv);
         }
       }
     }
@@ -76,7 +76,7 @@ extern "C" int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const voi
                                   int32_t* err_flag, void* stream) {
   using namespace pkv;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_slots <= 0) return PKV_ERR_INVALID_ARG;
-  if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
   const int64_t row_elems = (int64_t)num_kv_heads * head_dim;
   if (row_elems % 8 != 0 || row_elems > (1 << 20)) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
@@ -90,14 +90,11 @@ extern "C" int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const voi
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
   cudaStream_t st = as_stream(stream);
-  if (cache_dtype == PKV_BF16) {
-    kv_cache_write_kernel<false><<<(unsigned)blocks, kWriteThreads, 0, st>>>(
-        static_cast<const uint16_t*>(k), k_row_stride, static_cast<const uint16_t*>(v), v_row_stride, num_tokens,
-        (int32_t)row_elems, k_cache, v_cache, num_slots, slot_mapping, k_inv_scale, v_inv_scale, err_flag);
-  } else {
-    kv_cache_write_kernel<true><<<(unsigned)blocks, kWriteThreads, 0, st>>>(
-        static_cast<const uint16_t*>(k), k_row_stride, static_cast<const uint16_t*>(v), v_row_stride, num_tokens,
-        (int32_t)row_elems, k_cache, v_cache, num_slots, slot_mapping, k_inv_scale, v_inv_scale, err_flag);
-  }
+  auto kern = cache_dtype == PKV_BF16 ? kv_cache_write_kernel<0>
+               : cache_dtype == PKV_FP8_E4M3 ? kv_cache_write_kernel<1> : kv_cache_write_kernel<2>;
+  kern<<<(unsigned)blocks, kWriteThreads, 0, st>>>(static_cast<const uint16_t*>(k), k_row_stride,
+                                                   static_cast<const uint16_t*>(v), v_row_stride, num_tokens,
+                                                   (int32_t)row_elems, k_cache, v_cache, num_slots, slot_mapping,
+                                                   k_inv_scale, v_inv_scale, err_flag);
   return launch_status();
 }

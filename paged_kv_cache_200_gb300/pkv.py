@@ -26,6 +26,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "pkv.h")
 
 PKV_BF16 = 0
 PKV_FP8_E4M3 = 2
+PKV_INT8 = 3
 
 DEVERR_SLOT = 1
 DEVERR_BLOCK = 2
@@ -119,6 +120,8 @@ def _cache_dtype(cache: torch.Tensor) -> int:
         return PKV_BF16
     if cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
         return PKV_FP8_E4M3
+    if cache.dtype == torch.int8:
+        return PKV_INT8
     raise TypeError(f"unsupported cache dtype {cache.dtype}")
 
 

@@ -60,6 +60,22 @@ def per_tensor_fp8_scales(x: torch.Tensor):
     return float(scale), float(inv)
 
 
+def per_tensor_int8_scales(x: torch.Tensor):
+    """(scale, inv_scale) as float32: scale = absmax(x) / 127, inv_scale = 1 / scale."""
+    amax = np.float32(x.detach().abs().max().float().cpu().item())
+    scale = np.float32(amax / np.float32(127.0))
+    if scale == 0:
+        scale = np.float32(1.0)
+    inv = np.float32(np.float32(1.0) / scale)
+    return float(scale), float(inv)
+
+
+def int8_codes_via_torch(x: torch.Tensor, inv_scale: float) -> torch.Tensor:
+    """INT8 codes of ``x * inv_scale`` (torch's round half to even, clamped to +-127; input preparation only)."""
+    y = x.float() * torch.tensor(inv_scale, dtype=torch.float32, device=x.device)
+    return torch.round(y).clamp_(-127, 127).to(torch.int8)
+
+
 def fp8_codes_via_torch(x: torch.Tensor, inv_scale: float) -> torch.Tensor:
     """E4M3 codes of ``x * inv_scale`` using torch's float8 cast (input preparation only).
 
@@ -179,13 +195,15 @@ def make_decode(lens_before, num_heads, num_kv_heads, head_dim, block_size, seed
         lens_before=lens_before, cache_seqlens=_as_i32(total, device), block_table=_as_i32(table, device),
         slot_mapping=_as_i32(slots, device), q=q, k_new=k_new, v_new=v_new,
         k_cache=k_hist, v_cache=v_hist, cache_dtype="bf16")
-    if cache_dtype == "fp8_e4m3":
-        ks, kinv = per_tensor_fp8_scales(torch.cat([k_hist.reshape(-1), k_new.reshape(-1)]))
-        vs, vinv = per_tensor_fp8_scales(torch.cat([v_hist.reshape(-1), v_new.reshape(-1)]))
-        wl.k_cache = fp8_codes_via_torch(k_hist, kinv)
-        wl.v_cache = fp8_codes_via_torch(v_hist, vinv)
+    if cache_dtype in ("fp8_e4m3", "int8"):
+        scales = per_tensor_fp8_scales if cache_dtype == "fp8_e4m3" else per_tensor_int8_scales
+        codes = fp8_codes_via_torch if cache_dtype == "fp8_e4m3" else int8_codes_via_torch
+        ks, kinv = scales(torch.cat([k_hist.reshape(-1), k_new.reshape(-1)]))
+        vs, vinv = scales(torch.cat([v_hist.reshape(-1), v_new.reshape(-1)]))
+        wl.k_cache = codes(k_hist, kinv)
+        wl.v_cache = codes(v_hist, vinv)
         del k_hist, v_hist
-        wl.cache_dtype = "fp8_e4m3"
+        wl.cache_dtype = cache_dtype
         wl.k_scale, wl.k_inv_scale, wl.v_scale, wl.v_inv_scale = ks, kinv, vs, vinv
     return wl
 
@@ -330,16 +348,19 @@ def gather_tokens(wl: VarlenWorkload) -> int:
     return int(np.sum(wl.k_lens[wl.q_lens > 1]))
 
 
-def to_fp8_cache(wl: VarlenWorkload) -> VarlenWorkload:
-    """The same paged workload with an FP8 E4M3 cache: per-tensor absmax/448 scales over the
-    history and the new tokens, history codes laid down with torch's float8 cast."""
-    ks, kinv = per_tensor_fp8_scales(torch.cat([wl.k_cache.reshape(-1), wl.k_new.reshape(-1)]))
-    vs, vinv = per_tensor_fp8_scales(torch.cat([wl.v_cache.reshape(-1), wl.v_new.reshape(-1)]))
+def to_fp8_cache(wl: VarlenWorkload, cache_dtype: str = "fp8_e4m3") -> VarlenWorkload:
+    """The same paged workload with a coded cache (FP8 E4M3, or INT8 with cache_dtype="int8"):
+    per-tensor absmax/448 (absmax/127) scales over the history and the new tokens, history
+    codes laid down with torch casts."""
+    scales = per_tensor_fp8_scales if cache_dtype == "fp8_e4m3" else per_tensor_int8_scales
+    codes = fp8_codes_via_torch if cache_dtype == "fp8_e4m3" else int8_codes_via_torch
+    ks, kinv = scales(torch.cat([wl.k_cache.reshape(-1), wl.k_new.reshape(-1)]))
+    vs, vinv = scales(torch.cat([wl.v_cache.reshape(-1), wl.v_new.reshape(-1)]))
     out = VarlenWorkload(**{f: getattr(wl, f) for f in wl.__dataclass_fields__})
-    out.k_cache = fp8_codes_via_torch(wl.k_cache, kinv)
-    out.v_cache = fp8_codes_via_torch(wl.v_cache, vinv)
-    out.extra = dict(wl.extra, cache_dtype="fp8_e4m3", k_scale=ks, v_scale=vs, k_inv_scale=kinv, v_inv_scale=vinv)
-    out.name = wl.name + "_fp8"
+    out.k_cache = codes(wl.k_cache, kinv)
+    out.v_cache = codes(wl.v_cache, vinv)
+    out.extra = dict(wl.extra, cache_dtype=cache_dtype, k_scale=ks, v_scale=vs, k_inv_scale=kinv, v_inv_scale=vinv)
+    out.name = wl.name + "_" + cache_dtype
     return out
 
 

@@ -10,11 +10,11 @@ FP8_RTOL = 2e-2
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """bf16 tensor -> numpy uint16 bit patterns; uint8 tensor -> numpy uint8."""
+    """bf16 tensor -> numpy uint16 bit patterns; uint8 / int8 tensor -> numpy uint8 / int8."""
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
-    if t.dtype == torch.uint8:
+    if t.dtype in (torch.uint8, torch.int8):
         return t.numpy()
     raise TypeError(t.dtype)
 

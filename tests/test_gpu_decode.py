@@ -46,7 +46,7 @@ def _oracle(wl, kc_bits, vc_bits, seqs=None):
 
 
 def _tol(wl):
-    return (FP8_ATOL, FP8_RTOL) if wl.cache_dtype == "fp8_e4m3" else (BF16_ATOL, BF16_RTOL)
+    return (FP8_ATOL, FP8_RTOL) if wl.cache_dtype in ("fp8_e4m3", "int8") else (BF16_ATOL, BF16_RTOL)
 
 
 def _check(wl, out, lse, ref, ref_lse, seqs=None):
@@ -83,6 +83,8 @@ CASES = [
     ([5, 200, 1500, 47, 3000], 64, 8, 128, 32, "fp8_e4m3"),
     ([1, 31, 700, 2049], 4, 2, 64, 32, "fp8_e4m3"),
     ([0, 3, 63, 1000], 8, 1, 64, 16, "fp8_e4m3"),
+    ([5, 200, 1500, 47, 3000], 32, 8, 128, 16, "int8"),
+    ([1, 31, 700, 2049], 4, 2, 64, 32, "int8"),
 ]
 
 
@@ -203,8 +205,9 @@ def _full_size(pkv, wl, seqs):
         assert torch.equal(kc[slots], wl.k_new) and torch.equal(vc[slots], wl.v_new)
         kb, vb = kc, vc
     else:
-        kq = O.quantize_to_e4m3(bits(wl.k_new), np.float32(wl.k_inv_scale))
-        assert np.array_equal(bits(kc[slots]), kq)
+        quant = O.quantize_to_e4m3 if wl.cache_dtype == "fp8_e4m3" else O.quantize_to_int8
+        assert np.array_equal(bits(kc[slots]), quant(bits(wl.k_new), np.float32(wl.k_inv_scale)))
+        assert np.array_equal(bits(vc[slots]), quant(bits(wl.v_new), np.float32(wl.v_inv_scale)))
         kb, vb = kc, vc
     # copy only the sampled sequences' blocks to the host for the oracle
     table = wl.block_table.cpu().numpy()
@@ -233,7 +236,7 @@ def test_decode_batch64_full_size_sampled(pkv):
     _full_size(pkv, wl, seqs)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8"])
 def test_long_decode_full_size_sampled(pkv, dt):
     wl = W.long_decode(device="cuda", cache_dtype=dt)
     _full_size(pkv, wl, [0, 5])

@@ -296,12 +296,17 @@ def test_gather_bound_too_small_is_flagged(pkv):
 # ---------------------------------------------------------------------------
 
 
+@pytest.mark.parametrize("chunk", [False, True], ids=["verify_only", "with_chunk"])
 @pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
 @pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
-def test_multi_query_decode_rows(pkv, dt, gather):
+def test_multi_query_decode_rows(pkv, dt, gather, chunk):
+    """1..8 new tokens per sequence: every query row goes to the decode kernels when no
+    sequence has more than 8 queries; with a longer chunk in the batch only the
+    single-query rows do, and the rest run on the prefill tiles."""
     rng = np.random.default_rng(61)
     q_lens = rng.integers(1, 9, size=12)            # 1..8 new tokens
-    q_lens[3] = 40                                  # and one longer chunk (prefill tiles)
+    if chunk:
+        q_lens[3] = 40                              # and one longer chunk (prefill tiles)
     prefix = rng.integers(0, 3000, size=12)
     prefix[5] = 0                                   # a sequence that is only its new tokens
     wl = W.make_varlen_paged(q_lens, prefix, 32, 8, 128, 16, seed=62, device="cuda")
@@ -318,3 +323,19 @@ def test_multi_query_decode_rows(pkv, dt, gather):
     atol, rtol = (BF16_ATOL, BF16_RTOL) if dt == "bf16" else (FP8_ATOL, FP8_RTOL)
     assert_close(f64(out), ref, atol, rtol, f"multi-query {dt}")
     assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"multi-query lse {dt}")
+
+
+@pytest.mark.parametrize("case", FP8_PAGED[:3], ids=[f"bs{c[5]}_{c[2]}q{c[3]}kv_d{c[4]}_{i}" for i, c in
+                                                     enumerate(FP8_PAGED[:3])])
+def test_varlen_paged_int8(pkv, case):
+    q_lens, prefix, Hq, Hkv, D, bs = case
+    wl = W.to_fp8_cache(W.make_varlen_paged(q_lens, prefix, Hq, Hkv, D, bs, seed=sum(q_lens) + 9, device="cuda",
+                                            extra_blocks=2), "int8")
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=True)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=bs,
+                                       kv_dtype="int8", k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+    assert_close(f64(out), ref, FP8_ATOL, FP8_RTOL, f"int8 {case}")
+    assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"int8 lse {case}")

@@ -71,13 +71,14 @@ def test_with_kvcache_worked_example(pkv):
     ([1, 63, 64, 700, 2049], 4, 2, 64, 32, "fp8_e4m3"),
     ([0, 5, 3000], 64, 8, 128, 32, "fp8_e4m3"),
     ([9, 600, 1300], 3, 1, 64, 16, "bf16"),
+    ([0, 77, 2100], 16, 4, 128, 16, "int8"),
 ])
 def test_with_kvcache_small_cases(pkv, lens, Hq, Hkv, D, bs, dt):
     wl = W.make_decode(lens, Hq, Hkv, D, bs, seed=31 + len(lens), device="cuda", cache_dtype=dt)
     out, lse, kc, vc = _fused(pkv, wl)
     ref, ref_lse, rk, rv = _oracle(wl)
     assert np.array_equal(bits(kc), rk) and np.array_equal(bits(vc), rv)
-    atol, rtol = (FP8_ATOL, FP8_RTOL) if dt == "fp8_e4m3" else (BF16_ATOL, BF16_RTOL)
+    atol, rtol = (FP8_ATOL, FP8_RTOL) if dt in ("fp8_e4m3", "int8") else (BF16_ATOL, BF16_RTOL)
     assert_close(f64(out), ref, atol, rtol, "out")
     assert_close(f64(lse), ref_lse, 1e-3, 1e-3, "lse")
 

@@ -132,3 +132,33 @@ def test_zero_tokens_is_a_noop(pkv):
     pkv.kv_cache_write(k, k, kc, kc, torch.empty(0, dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert torch.count_nonzero(kc).item() == 0
+
+
+@pytest.mark.parametrize("inv", [1.0, 21.5, 1000.0])
+def test_write_int8_bit_exact(pkv, inv):
+    T, Hkv, D, NS = 500, 8, 128, 640
+    g = torch.Generator(device="cuda").manual_seed(int(inv) + 5)
+    k = (torch.randn(T, Hkv, D, device="cuda", generator=g) * 3).bfloat16()
+    v = torch.randn(T, Hkv, D, device="cuda", generator=g).bfloat16()
+    kc = torch.randint(-127, 128, (NS, Hkv, D), device="cuda", dtype=torch.int8, generator=g)
+    vc = kc.clone()
+    slots = np.random.default_rng(3).permutation(NS)[:T].astype(np.int32)
+    k_inv, v_inv = np.float32(inv), np.float32(inv / 3)
+    k2, v2 = _run_write(pkv, k, v, kc, vc, torch.from_numpy(slots).cuda(), k_inv_scale=float(k_inv),
+                        v_inv_scale=float(v_inv))
+    rk, rv = O.kv_cache_write(bits(k), bits(v), bits(kc), bits(vc), slots, cache_dtype="int8",
+                              k_inv_scale=k_inv, v_inv_scale=v_inv)
+    assert np.array_equal(bits(k2), rk) and np.array_equal(bits(v2), rv)
+
+
+def test_write_int8_special_values(pkv):
+    """Ties to even, saturation at +-127 and infinities, as the oracle."""
+    vals = np.array([0.0, -0.0, 0.5, 1.5, 2.5, -2.5, 126.5, 127.5, 300.0, -300.0, np.inf, -np.inf, 3.25, -3.75,
+                     64.0, -1.0] * 8, dtype=np.float32)
+    x = torch.from_numpy(vals).bfloat16().cuda().view(16, 1, 8)
+    kc = torch.zeros(16, 1, 8, dtype=torch.int8, device="cuda")
+    slots = torch.arange(16, dtype=torch.int32, device="cuda")
+    k2, _ = _run_write(pkv, x, x, kc, kc, slots, k_inv_scale=1.0, v_inv_scale=1.0)
+    rk, _ = O.kv_cache_write(bits(x), bits(x), bits(kc), bits(kc), np.arange(16), cache_dtype="int8",
+                             k_inv_scale=np.float32(1.0), v_inv_scale=np.float32(1.0))
+    assert np.array_equal(bits(k2), rk)
