@@ -5,7 +5,7 @@
 // one prompt share the blocks of their common part, and a shared block is
 // copied only once one of them has to write into it.  This call makes those
 // copies: for each (src, dst) pair, block dst of each cache becomes a copy of
-// block src, byte for byte (bf16 or FP8 codes alike).
+// block src, byte for byte (bf16, FP8 or INT8 codes alike).
 //
 // Design: an HBM-bound copy.  Each CTA takes whole pairs (grid-stride over the
 // pair list) and moves a block of each cache in 16-byte vectors, every thread

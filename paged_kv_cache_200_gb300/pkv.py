@@ -155,8 +155,9 @@ def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, k_inv_scale: float = 1.
     """Scatter each token's K/V row into the caches at ``slot_mapping[t]`` (negative = skip).
 
     ``k``, ``v``: ``[T, Hkv, D]`` bf16 with the inner two dims contiguous (any
-    row stride).  Caches: ``[..., Hkv, D]`` contiguous, bf16 or uint8 E4M3
-    codes; FP8 stores ``e4m3(x * inv_scale)``.
+    row stride).  Caches: ``[..., Hkv, D]`` contiguous: bf16, uint8 E4M3 codes
+    or int8 codes.  FP8 stores ``e4m3(x * inv_scale)``; INT8 stores
+    ``clamp(rint(x * inv_scale), -127, 127)`` with NaN stored as 0.
     """
     _require_cuda(k, v, k_cache, v_cache, slot_mapping)
     T, Hkv, D = k.shape
@@ -185,8 +186,8 @@ def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, k_inv_scale: float = 1.
 def copy_blocks(k_cache, v_cache, block_pairs, err_flag=None, stream=None):
     """Block ``dst`` of each cache becomes a copy of block ``src``, for each row of ``block_pairs``.
 
-    Caches: ``[num_blocks, block_size, Hkv, D]`` contiguous (bf16 or uint8 E4M3
-    codes); ``v_cache`` may be ``None``.  ``block_pairs``: int32 ``[n, 2]``
+    Caches: ``[num_blocks, block_size, Hkv, D]`` contiguous (bf16, E4M3 or
+    INT8 codes; the bytes are copied as they are); ``v_cache`` may be ``None``.  ``block_pairs``: int32 ``[n, 2]``
     ``(src, dst)`` on the device; no dst may also be a src of the same call.
     """
     _require_cuda(k_cache, block_pairs, *([] if v_cache is None else [v_cache]))
