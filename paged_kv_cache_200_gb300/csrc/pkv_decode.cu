@@ -45,6 +45,8 @@ constexpr int kDecWarps = 4;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kGroupTok = 16;       // positions per warp step
 constexpr int kMaxGroup = 8;        // query heads per kv head handled by one CTA
+constexpr int kResidentBf16 = 2;    // split-kernel CTAs per SM with a bf16 cache (3 stages)
+constexpr int kResidentCoded = 4;   // ... with one-byte codes (3 stages)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -150,7 +152,7 @@ struct TileLayout {
 
 // kFp8: one-byte codes (E4M3, or INT8 when kInt8) widened to f16 for f16 MMAs.
 template <int D, bool kFp8, int kStages, bool kInt8 = false>
-__global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
+__global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResidentBf16)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                               const DecodeParams p) {
   constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one position, one kv head
@@ -428,14 +430,20 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? 3 : 2)
           for (int pp = 0; pp < kDT / 2; ++pp) {
             uint32_t r0, r1, r2, r3;
             ldmatrix_x4_trans(vs + TL::offset(row, 2 * pp + csel), r0, r1, r2, r3);
-            // r: bytes (pos 2j, dim 2u), (2j, 2u+1), (2j+1, 2u), (2j+1, 2u+1); reorder to
-            // (2j,2u), (2j+1,2u) | (2j,2u+1), (2j+1,2u+1) and widen: even dims, then odd dims
-            const uint32_t t0 = prmt(r0, 0u, 0x3120u), t1 = prmt(r1, 0u, 0x3120u);
-            const uint32_t t2 = prmt(r2, 0u, 0x3120u), t3 = prmt(r3, 0u, 0x3120u);
-            mma_f16_16816(o[2 * pp], code_lo(t0), code_lo(t1), code_lo(t2),
-                          code_lo(t3), pb0, pb1);
-            mma_f16_16816(o[2 * pp + 1], code_hi(t0), code_hi(t1), code_hi(t2),
-                          code_hi(t3), pb0, pb1);
+            // r: bytes (pos 2j, dim 2u), (2j, 2u+1), (2j+1, 2u), (2j+1, 2u+1); widen
+            // bytes {0, 2} (even dim, both positions), then {1, 3} (odd dim).  INT8
+            // picks them in its widening permute; E4M3 reorders the word first.
+            if constexpr (kInt8) {
+              mma_f16_16816(o[2 * pp], int8x2_even_to_f16x2(r0), int8x2_even_to_f16x2(r1),
+                            int8x2_even_to_f16x2(r2), int8x2_even_to_f16x2(r3), pb0, pb1);
+              mma_f16_16816(o[2 * pp + 1], int8x2_odd_to_f16x2(r0), int8x2_odd_to_f16x2(r1),
+                            int8x2_odd_to_f16x2(r2), int8x2_odd_to_f16x2(r3), pb0, pb1);
+            } else {
+              const uint32_t t0 = prmt(r0, 0u, 0x3120u), t1 = prmt(r1, 0u, 0x3120u);
+              const uint32_t t2 = prmt(r2, 0u, 0x3120u), t3 = prmt(r3, 0u, 0x3120u);
+              mma_f16_16816(o[2 * pp], code_lo(t0), code_lo(t1), code_lo(t2), code_lo(t3), pb0, pb1);
+              mma_f16_16816(o[2 * pp + 1], code_hi(t0), code_hi(t1), code_hi(t2), code_hi(t3), pb0, pb1);
+            }
           }
         }
       }
@@ -579,22 +587,57 @@ struct SplitPlan {
   size_t workspace;
 };
 
-// Positions per CTA: enough CTAs to fill the GPU several times over at the
-// longest sequence, in multiples of 64 positions (4 warps x 16), at least 512.
-// With fewer (sequence, kv head) units than SMs all sequences are long and
-// alike, and 8 waves of 2 CTAs per SM cost less per-CTA overhead than 16
-// (long-context decode 6.33 -> 6.61 TB/s); many units of mixed lengths keep 16.
-SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seqlen_k) {
+// Positions per CTA (split_tokens), a multiple of 64 (4 warps x 16), at least
+// 512.  A resident slot is one CTA on one SM (SMs x CTAs per SM for the cache's
+// element size), and a wave fills every slot once.
+//  * Fewer (sequence, kv head) units than SMs: the sequences are few and long,
+//    taken as equally long.  Each candidate split count is costed as
+//    waves x (split_tokens + a fixed per-CTA cost), which favours splits that
+//    end on a whole wave and penalises many short CTAs (measured on 8 x 128K
+//    contexts: bf16 6.47 -> 6.64 TB/s, FP8 5.82 -> 5.88 TB/s against 8 waves of
+//    2 CTAs per SM).
+//  * Otherwise the lengths are mixed and unknown on the host: about 32 CTAs
+//    per SM at the longest length, which leaves the short sequences one CTA.
+constexpr int64_t kCtaOverheadPos = 96;  // prologue + merge of one CTA, in positions of streaming time
+constexpr int64_t kCtasPerSmMixed = 32;
+
+int resident_ctas(int cache_dtype) { return cache_dtype == PKV_BF16 ? kResidentBf16 : kResidentCoded; }
+
+SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seqlen_k, int cache_dtype) {
   SplitPlan pl{64, 1, 0};
   if (batch <= 0 || max_seqlen_k <= 0) return pl;
   const int64_t units = (int64_t)batch * num_kv_heads;
-  const int64_t waves = units < device_sm_count() ? 8 : 16;
-  const int64_t target = (int64_t)device_sm_count() * 2 * waves;
-  int64_t c = ((int64_t)max_seqlen_k * units + target - 1) / target;
-  c = ((c + 63) / 64) * 64;
-  if (c < 512) c = 512;
-  const int64_t whole = ((int64_t)max_seqlen_k + 63) / 64 * 64;
-  if (c > whole) c = whole;
+  const int64_t sms = device_sm_count();
+  const int64_t L = max_seqlen_k;
+  const int64_t whole = (L + 63) / 64 * 64;
+  auto clamp_split = [&](int64_t c) {  // multiple of 64, at least 512, at most the whole sequence
+    c = (c + 63) / 64 * 64;
+    if (c < 512) c = 512;
+    return c < whole ? c : whole;
+  };
+  int64_t c;
+  if (whole <= 512) {
+    c = whole;
+  } else if (units < sms) {
+    const int64_t slots = sms * resident_ctas(cache_dtype);
+    const int64_t n_max = 8 * slots / units + 1;  // beyond 8 waves' worth of splits nothing is gained
+    c = whole;
+    int64_t best = INT64_MAX;
+    for (int64_t n = 1; n <= n_max; ++n) {
+      const int64_t cn = clamp_split((L + n - 1) / n);
+      const int64_t splits = (L + cn - 1) / cn;
+      const int64_t waves = (units * splits + slots - 1) / slots;
+      const int64_t cost = waves * (cn + kCtaOverheadPos);
+      if (cost < best) {
+        best = cost;
+        c = cn;
+      }
+      if (cn == 512) break;  // every larger n gives the same split
+    }
+  } else {
+    const int64_t target = sms * kCtasPerSmMixed;
+    c = clamp_split((L * units + target - 1) / target);
+  }
   pl.split_tokens = (int)c;
   pl.max_splits = (int)((max_seqlen_k + c - 1) / c);
   if (pl.max_splits > 1) {
@@ -606,7 +649,7 @@ SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, i
 
 template <int D, bool kFp8, bool kInt8 = false>
 int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t num_slots, cudaStream_t st) {
-  constexpr int kStages = kFp8 ? 4 : 3;  // FP8: 3 CTAs (12 warps) per SM; bf16: 2 CTAs
+  constexpr int kStages = 3;  // shared memory for kResidentCoded (one-byte codes) or kResidentBf16 CTAs per SM
   constexpr int kRowBytes = D * (kFp8 ? 1 : 2);
   using TL = TileLayout<kRowBytes>;
   constexpr int kSmemPipe = kDecWarps * kStages * 2 * TL::kTileBytes + kDecWarps * kStages * 8;
@@ -654,7 +697,10 @@ int dispatch_decode(int cache_dtype, int head_dim, const DecodeParams& p, int ba
 extern "C" size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
                                                   int32_t head_dim, int32_t max_seqlen_k) {
   if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seqlen_k <= 0) return 0;
-  return pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k).workspace;
+  // enough for every cache element type (their plans differ in CTAs per SM)
+  const size_t a = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_BF16).workspace;
+  const size_t b = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_INT8).workspace;
+  return a > b ? a : b;
 }
 
 namespace pkv {
@@ -693,7 +739,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
       (reinterpret_cast<uintptr_t>(out) & 7u))
     return PKV_ERR_INVALID_ARG;
   const int mlen = max_seqlen_k > 0 ? max_seqlen_k : 1;
-  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, mlen);
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, mlen, cache_dtype);
   if (pl.workspace > 0 && (workspace == nullptr || workspace_bytes < pl.workspace ||
                            (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
@@ -783,9 +829,10 @@ extern "C" int pkv_paged_attn_decode_with_kvcache(const void* q, const void* k_n
 namespace pkv {
 
 // Partials of `items` routed rows, split as a decode batch of `batch` sequences would be.
-size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k) {
+size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
+                               int cache_dtype) {
   if (batch <= 0 || items <= 0 || max_len_k <= 0) return 0;
-  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k);
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k, cache_dtype);
   if (pl.max_splits <= 1) return 0;
   const size_t rows = (size_t)items * num_heads * pl.max_splits;
   return rows * head_dim * sizeof(float) + ((rows * sizeof(float) + 255) / 256) * 256;
@@ -804,9 +851,10 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          int32_t* err_flag, cudaStream_t st) {
   const bool fp8 = cache_dtype != PKV_BF16;  // one-byte codes
   if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
-  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1);
-  if (varlen_decode_workspace(batch, item_bound, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1) >
-      workspace_bytes)
+  const SplitPlan pl =
+      plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype);
+  if (varlen_decode_workspace(batch, item_bound, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1,
+                              cache_dtype) > workspace_bytes)
     return PKV_ERR_WORKSPACE;
   DecodeParams p{};
   p.q = static_cast<const uint16_t*>(q);

@@ -154,6 +154,20 @@ __device__ __forceinline__ uint32_t int8x2_hi_to_f16x2(uint32_t w) {
   return d;
 }
 
+// Bytes {0, 2}, resp. {1, 3}, of a word of INT8 codes -> f16x2 (same method).
+__device__ __forceinline__ uint32_t int8x2_even_to_f16x2(uint32_t w) {
+  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4240u);
+  uint32_t d;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
+  return d;
+}
+__device__ __forceinline__ uint32_t int8x2_odd_to_f16x2(uint32_t w) {
+  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4341u);
+  uint32_t d;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
+  return d;
+}
+
 // Packed fp32 pairs (sm_100+): two lanes of arithmetic per instruction.
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
   uint64_t r;

@@ -37,7 +37,8 @@ static_assert(kRouteMaxQ < kRouteCode, "query index must fit the item code");
 // Decode kernels serving the routed query rows of a paged varlen batch
 // (at most item_bound of them; splits planned for `batch` sequences).
 
-size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k);
+size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
+                               int cache_dtype);
 int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* items,
                          const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,
                          const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t item_bound,

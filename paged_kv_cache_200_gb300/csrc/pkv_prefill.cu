@@ -908,7 +908,7 @@ int route_items_bound(int batch, int total_q, int max_len_q) {
 }
 
 VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
-                          bool route, bool gather, int64_t total_k) {
+                          bool route, bool gather, int64_t total_k, int kv_dtype) {
   VarlenWs w{0, 0, 0, 0, 0, 0, 256};
   if (batch <= 0) return w;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -916,7 +916,8 @@ VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_
     w.count_off = 4;
     w.items_off = 256;
     w.decode_off = w.items_off + up((size_t)route_items * 4);
-    w.total = w.decode_off + varlen_decode_workspace(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k);
+    w.total = w.decode_off +
+              varlen_decode_workspace(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, kv_dtype);
   }
   if (gather) {
     w.cu_g_off = up(w.total);
@@ -968,7 +969,7 @@ extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q
   return pkv::varlen_ws_layout(batch, pkv::route_items_bound(batch, total_q, max_len_q), num_heads, num_kv_heads,
                                head_dim,
                                max_len_k,
-                               routes_decode(paged != 0, num_heads, num_kv_heads), gather, total_k)
+                               routes_decode(paged != 0, num_heads, num_kv_heads), gather, total_k, kv_dtype)
       .total;
 }
 
@@ -1010,7 +1011,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   const int route_items = route ? route_items_bound(batch, total_q, max_len_q) : 0;
   const int rmq = route ? route_max_q(max_len_q) : 0;  // queries up to which a sequence is routed
   const VarlenWs wl =
-      varlen_ws_layout(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, route, gather, total_k);
+      varlen_ws_layout(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, route, gather, total_k,
+                       kv_dtype);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
                        (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
