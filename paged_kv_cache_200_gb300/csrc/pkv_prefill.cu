@@ -157,8 +157,9 @@ struct Smem {
   static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
   static constexpr int kBar = kV + 2 * kTileBytes;
   static constexpr int kNumBars = 28;
-  static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag, 4 ring slots
-  static constexpr int kXchg = kMisc + 32;              // float m[2][128], l[2][128]
+  static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
+  static constexpr int kRingData = kMisc + 16;          // 4 ring slots x 8 ints (item, q0, Lq, k0, Lk)
+  static constexpr int kXchg = kRingData + 4 * 32;      // float m[2][128], l[2][128]
   static constexpr int kStage = kXchg + 4 * 128 * 4;    // output staging: 8 softmax warps x 16 half rows
   static constexpr int kTotal = kStage + 8 * 16 * D;
   static constexpr int kAlloc = kTotal + 1024;          // slack to align the base to 1024
@@ -199,17 +200,30 @@ static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kVFull0 == k
                   kPvDone0 == kPFull0 + 2 && kRingEmpty0 == kPvDone0 + 2 && kBarCount == kRingEmpty0 + kRing,
               "mbarrier index ranges must not overlap");
 
+// A sequence's query/key offsets and (checked) lengths.  The producer warp
+// reads them from global memory once per work item and hands them to the
+// other roles through the work-item ring, so only one warp waits on those loads.
+struct SeqBase {
+  int q0, Lq, k0, Lk;
+};
 struct Seq {
   int q0, Lq, k0, Lk, row0, rows, diag, n_kv;
   bool skip;
 };
 
-__device__ __forceinline__ Seq seq_info(const PrefillParams& p, int b, int qtile, bool report) {
-  Seq s;
-  s.q0 = __ldg(p.cu_q + b);
-  s.Lq = __ldg(p.cu_q + b + 1) - s.q0;
-  s.k0 = __ldg(p.cu_k + b);
-  s.Lk = __ldg(p.cu_k + b + 1) - s.k0;
+// Cumulative offsets of sequence b: q0, q1, k0, k1 (loads only; checked by seq_check).
+__device__ __forceinline__ void seq_load(const PrefillParams& p, int b, int (&raw)[4]) {
+  raw[0] = __ldg(p.cu_q + b);
+  raw[1] = __ldg(p.cu_q + b + 1);
+  raw[2] = __ldg(p.cu_k + b);
+  raw[3] = __ldg(p.cu_k + b + 1);
+}
+__device__ __forceinline__ SeqBase seq_check(const PrefillParams& p, const int (&raw)[4], bool report) {
+  SeqBase s;
+  s.q0 = raw[0];
+  s.Lq = raw[1] - raw[0];
+  s.k0 = raw[2];
+  s.Lk = raw[3] - raw[2];
   bool bad = false;
   if (s.Lq < 0) { s.Lq = 0; bad = true; }
   if (s.Lk < 0) { s.Lk = 0; bad = true; }
@@ -218,6 +232,14 @@ __device__ __forceinline__ Seq seq_info(const PrefillParams& p, int b, int qtile
     bad = true;
   }
   if (bad && report) flag_error(p.err, PKV_DEVERR_LENGTH);
+  return s;
+}
+__device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase& b0, int qtile) {
+  Seq s;
+  s.q0 = b0.q0;
+  s.Lq = b0.Lq;
+  s.k0 = b0.k0;
+  s.Lk = b0.Lk;
   s.row0 = qtile * kBM;
   s.rows = min(kBM, s.Lq - s.row0);
   s.diag = s.Lk - s.Lq;
@@ -309,12 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // them), through a global counter; the producer warp claims them and
   // publishes each one that has work into a 4-slot ring that the MMA and
   // softmax warps read in order.  -1 ends the list.
-  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);
-  // Consumer side: item of the u-th ring entry (or -1, also on timeout).
-  auto ring_get = [&](int u) -> int {
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRingData);
+  // Consumer side: item of the u-th ring entry (or -1, also on timeout) and its sequence.
+  auto ring_get = [&](int u, SeqBase& sb) -> int {
     const int slot = u & (kRing - 1);
     if (!mbar_wait(bar(kRingFull0 + slot), (u / kRing) & 1, abort_flag)) return -1;
-    const int it = ring[slot];
+    const volatile int* e = ring + 8 * slot;
+    const int it = e[0];
+    sb.q0 = e[1];
+    sb.Lq = e[2];
+    sb.k0 = e[3];
+    sb.Lk = e[4];
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kRingEmpty0 + slot));
     return it;
@@ -325,27 +352,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     int last_k[2] = {-1, -1}, last_v[2] = {-1, -1}, last_q[2] = {-1, -1};
     int g = 0, uq = 0, ur = 0;  // tiles, items with keys, ring entries
     bool ok = true;
-    auto publish = [&](int it) -> bool {
+    auto publish = [&](int it, const SeqBase& sb) -> bool {
       const int slot = ur & (kRing - 1);
       if (ur >= kRing && !mbar_wait(bar(kRingEmpty0 + slot), ((ur / kRing) - 1) & 1, abort_flag)) return false;
       if (lane == 0) {
-        ring[slot] = it;
+        volatile int* e = ring + 8 * slot;
+        e[0] = it;
+        e[1] = sb.q0;
+        e[2] = sb.Lq;
+        e[3] = sb.k0;
+        e[4] = sb.Lk;
         mbar_arrive(bar(kRingFull0 + slot));
       }
       __syncwarp();
       ++ur;
       return true;
     };
-    while (ok) {
-      int it = 0;
-      if (lane == 0) it = atomicAdd(p.item_counter, 1);
-      it = __shfl_sync(0xffffffffu, it, 0);
-      if (it >= n_items) break;
+    // The next item is claimed from the global counter a few tiles before
+    // the current one's last, and its offsets are loaded while those tiles
+    // are issued: neither latency then sits between two items, and a claimed
+    // item waits only a few tiles (dynamic balance is kept).  A skipped item
+    // (a sequence left to the decode kernels, or a query tile past its end)
+    // moves the counter past the other heads of its (tile, sequence), which
+    // are skipped too.
+    int claim = 0;  // lane 0: atomic result for the next item
+    bool claimed = false, resolved = false;
+    int it = 0, next = n_items;
+    int raw[4] = {0, 0, 0, 0};
+    auto claim_next = [&]() {
+      if (claimed) return;
+      if (lane == 0) claim = atomicAdd(p.item_counter, 1);
+      claimed = true;
+    };
+    auto resolve_next = [&]() {
+      claim_next();
+      if (resolved) return;
+      next = __shfl_sync(0xffffffffu, claim, 0);
+      if (next < n_items) seq_load(p, item_of(p, next).b, raw);
+      resolved = true;
+    };
+    resolve_next();
+    it = next;
+    while (ok && it < n_items) {
+      claimed = resolved = false;
       const Item x = item_of(p, it);
-      const Seq sq = seq_info(p, x.b, x.qtile, x.qtile == 0 && x.head == 0 && lane == 0);
-      if (sq.skip) continue;
-      if (!publish(it)) { ok = false; break; }
-      if (sq.n_kv == 0) continue;
+      const SeqBase si = seq_check(p, raw, x.qtile == 0 && x.head == 0 && lane == 0);
+      const Seq sq = seq_derive(p, si, x.qtile);
+      if (sq.skip) {
+        const int block_end = (it / p.num_heads + 1) * p.num_heads;  // first item of the next (tile, sequence)
+        if (lane == 0 && block_end < n_items) atomicMax(p.item_counter, block_end);
+        resolve_next();
+        it = next;
+        continue;
+      }
+      if (!publish(it, si)) { ok = false; break; }
+      if (sq.n_kv == 0) {
+        resolve_next();
+        it = next;
+        continue;
+      }
       const int kvh = x.head / p.group;
       const int32_t* bt = kPaged ? p.block_table + (int64_t)x.b * p.max_blocks : nullptr;
       const int qb = uq & 1, qu = uq >> 1;
@@ -416,7 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int slot_cur = tile_slot(0, tile_blk(0));
       int blk_next = tile_blk(1);
       if (!issue(0, 0, slot_cur)) { ok = false; break; }
+      const int claim_at = sq.n_kv > 3 ? sq.n_kv - 3 : 0;  // tiles ahead of the item's end
       for (int j = 0; j < sq.n_kv && ok; ++j) {
+        if (j == claim_at) claim_next();
+        if (j > claim_at && j == sq.n_kv - 1) resolve_next();
         const int blk_after = tile_blk(j + 2);
         const int slot_next = (j + 1 < sq.n_kv) ? tile_slot(j + 1, blk_next) : 0;
         if (j + 1 < sq.n_kv && !issue(0, j + 1, slot_next)) { ok = false; break; }
@@ -424,10 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         slot_cur = slot_next;
         blk_next = blk_after;
       }
+      if (!ok) break;
+      resolve_next();
+      it = next;
       g += sq.n_kv;
       ++uq;
     }
-    if (ok && !publish(-1)) ok = false;
+    if (ok && !publish(-1, SeqBase{0, 0, 0, 0})) ok = false;
     if (!ok) fail();
     // every copy this CTA issued has landed before shared memory is released
     for (int s = 0; s < 2; ++s) {
@@ -482,10 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     for (int u = 0; ok; ++u) {
-      const int it = ring_get(u);
+      SeqBase si;
+      const int it = ring_get(u, si);
       if (it < 0) break;
       const Item x = item_of(p, it);
-      const Seq sq = seq_info(p, x.b, x.qtile, false);
+      const Seq sq = seq_derive(p, si, x.qtile);
       if (sq.n_kv == 0) continue;
       const int qb = uq & 1;
       if (!mbar_wait(bar(kQFull0 + qb), (uq >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -534,10 +606,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0, ux = 0;  // tiles and work items (with keys) processed
     for (int u = 0; ok; ++u) {
-      const int it = ring_get(u);
+      SeqBase si;
+      const int it = ring_get(u, si);
       if (it < 0) break;
       const Item x = item_of(p, it);
-      const Seq sq = seq_info(p, x.b, x.qtile, false);
+      const Seq sq = seq_derive(p, si, x.qtile);
       const int qi = sq.row0 + r;
       const int64_t row = (int64_t)sq.q0 + qi;
       const bool row_valid = r < sq.rows;
