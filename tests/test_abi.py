@@ -66,3 +66,59 @@ def test_copy_blocks_host_validation():
     # no pairs: nothing to do; pairs without a cache: rejected
     assert lib.pkv_copy_blocks(nul, nul, 4096, 8, nul, 0, nul, nul) == 0
     assert lib.pkv_copy_blocks(nul, nul, 4096, 8, nul, 3, nul, nul) == 1
+
+
+def _split_plan(batch, num_kv_heads, max_len, sms, resident):
+    """The decode split plan as the library states it: positions per CTA (a multiple of 64,
+    at least 512, at most the whole sequence).  Few (sequence, kv head) units: the split
+    count with the fewest waves x (split + 96); otherwise about 32 CTAs per SM."""
+    whole = (max_len + 63) // 64 * 64
+
+    def clamp(c):
+        return min(max((c + 63) // 64 * 64, 512), whole)
+
+    if whole <= 512:
+        return whole
+    units = batch * num_kv_heads
+    if units < sms:
+        slots = sms * resident
+        best, best_c = None, whole
+        for n in range(1, 8 * slots // units + 2):
+            c = clamp(-(-max_len // n))
+            waves = -(-units * -(-max_len // c) // slots)
+            cost = waves * (c + 96)
+            if best is None or cost < best:
+                best, best_c = cost, c
+            if c == 512:
+                break
+        return best_c
+    return clamp(-(-max_len * units // (sms * 32)))
+
+
+@pytest.mark.parametrize("shape", [(8, 64, 8, 128, 131073), (64, 32, 8, 128, 16385), (1, 8, 8, 128, 32768),
+                                   (3, 4, 2, 64, 71), (2, 16, 2, 64, 600000)])
+def test_decode_workspace_follows_the_split_plan(shape):
+    """The workspace query sizes the larger of the bf16 (2 CTAs per SM) and one-byte (4 per SM) plans."""
+    import torch
+
+    pkv = built_library()
+    lib = pkv.lib()
+    B, Hq, Hkv, D, L = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+
+    def ws(res):
+        c = _split_plan(B, Hkv, L, sms, res)
+        splits = -(-L // c)
+        if splits <= 1:
+            return 0
+        rows = B * Hq * splits
+        return rows * D * 4 + (rows * 4 + 255) // 256 * 256
+
+    assert lib.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, L) == max(ws(2), ws(4))
+
+
+def test_split_plan_ends_long_contexts_on_whole_waves():
+    """8 x 128K tokens: 19 splits of 6912 positions, 1216 CTAs = 4 waves of 2 CTAs per SM on 152 SMs."""
+    c = _split_plan(8, 8, 131073, 152, 2)
+    assert c == 6912 and -(-131073 // c) == 19
+    assert (8 * 8 * 19) % (152 * 2) == 0
