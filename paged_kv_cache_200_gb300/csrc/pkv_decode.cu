@@ -166,6 +166,9 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   auto code_lo = [](uint32_t w) { return kInt8 ? int8x2_lo_to_f16x2(w) : e4m3x2_lo_to_f16x2(w); };
   auto code_hi = [](uint32_t w) { return kInt8 ? int8x2_hi_to_f16x2(w) : e4m3x2_hi_to_f16x2(w); };
 
+  // The combine kernel may be scheduled as soon as every CTA of this grid has
+  // started; it waits for this grid's completion before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -528,6 +531,9 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
 // One warp per (sequence, query head): merge the splits by log-sum-exp.
 template <int D>
 __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p, int batch) {
+  // launched as a programmatic dependent of the split kernel: wait until that
+  // grid has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t bh = (int64_t)blockIdx.x * 4 + warp;
@@ -673,8 +679,20 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t
   dim3 grid(pl.max_splits, p.num_kv_heads, batch);
   kern<<<grid, kDecThreads, kSmem, st>>>(mk, mv, p);
   if (pl.max_splits > 1) {
+    // programmatic dependent launch: the combine grid's launch overlaps the
+    // split kernel's last wave instead of following its completion
     const int64_t rows = (int64_t)batch * p.num_heads;
-    paged_decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p, batch);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_decode_combine_kernel<D>, p, batch) != cudaSuccess) return PKV_ERR_CUDA;
   }
   return launch_status();
 }
