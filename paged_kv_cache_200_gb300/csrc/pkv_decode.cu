@@ -25,12 +25,18 @@
 // * Online softmax in the log2 domain, fp32; the running max moves only when
 //   it grows by more than 2^8; masked positions get -inf (never
 //   multiply-by-zero, so stale or NaN cache rows cannot leak in).
-// * FP8 E4M3 cache: codes widen exactly to f16 with the hardware conversion
-//   and the MMAs run in f16; Q is scaled by a power of two into f16 range,
-//   k_scale folds into the logit scale and v_scale into the output.
+// * FP8 E4M3 or INT8 cache: codes widen exactly to f16 (the hardware
+//   conversion, resp. byte permutes and one f16 subtract) and the MMAs run in
+//   f16; Q is scaled by a power of two into f16 range, k_scale folds into the
+//   logit scale and v_scale into the output.  One-byte caches run 4 CTAs per
+//   SM (bf16: 2), which hides the widening work behind more warps.
+// * Split sizes come from the host: few long sequences are cut so that their
+//   CTAs fill whole waves of resident CTAs; mixed batches get about 32 CTAs
+//   per SM at the longest length.
 // * Per-CTA partials (O/l, log2-sum-exp) go to the caller's workspace; a
-//   second kernel merges the splits of each (seq, head).  A sequence that fits
-//   one split is written directly by the split kernel.
+//   second kernel, launched as a programmatic dependent of the first, merges
+//   the splits of each (seq, head).  A sequence that fits one split is written
+//   directly by the split kernel.
 // * Append mode (decode with the step's cache update): the warp whose copies
 //   read the new position stores the new K/V rows first.
 #include <cmath>
