@@ -10,8 +10,10 @@ step's algorithmic HBM bytes per second (attended K/V + Q + O of the decode,
 plus the written rows read and stored), i.e. paged-decode HBM GB/s.
 
 Also measured in the same run (``also``): the long-context decode workload
-(8 x 131072 tokens, 64 q / 8 kv heads) with a bf16 and an FP8-E4M3 cache, and
-the causal varlen prefill workload (TFLOP/s) when the library provides it.
+(8 x 131072 tokens, 64 q / 8 kv heads) with bf16, FP8-E4M3 and INT8 caches,
+the causal varlen prefill workload (TFLOP/s; packed, paged and paged FP8), the
+mixed chunked batch, the fused append + decode step, speculative verification,
+copy-on-write and a KV-write sweep.
 
 ``--impl reference`` times the CPU oracle (fp64 NumPy) on bounded samples of
 the same workload, as the reference arm.
@@ -283,6 +285,65 @@ def sampled_oracle_decode(wl, seqs):
     return O, q, kc, vc, lens, tsub
 
 
+def _oracle_worker(task):
+    """One process of the all-cores oracle timing: the oracle, as it stands, on a few
+    sequences of its own with the decode batch's shapes (32 q / 8 kv heads, d128,
+    block size 16) and length distribution (uniform in 1024..16384), seeded; so no
+    cache is copied between processes."""
+    seed, budget_s, n_seqs = task
+    import oracle as O
+    rng = np.random.default_rng(seed)
+    hq, hkv, d, bs = 32, 8, 128, 16
+    lens = rng.integers(1024, 16384, size=n_seqs, endpoint=True)
+    nblk = -(-lens // bs)
+    perm = rng.permutation(int(nblk.sum())).astype(np.int32)
+    table = np.full((n_seqs, int(nblk.max())), -1, np.int32)
+    off = 0
+    for i, n in enumerate(nblk):
+        table[i, :n] = perm[off:off + n]
+        off += n
+
+    def bf16_bits(shape):  # N(0,1) fp32 rounded to nearest-even bf16, as bit patterns
+        x = rng.standard_normal(int(np.prod(shape)), dtype=np.float32).view(np.uint32)
+        return ((x + 0x7FFF + ((x >> 16) & 1)) >> 16).astype(np.uint16).reshape(shape)
+
+    kc = bf16_bits((int(nblk.sum()) * bs, hkv, d))
+    vc = bf16_bits((int(nblk.sum()) * bs, hkv, d))
+    q = bf16_bits((n_seqs, hq, d))
+    done, count = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        s = count % n_seqs
+        O.paged_attn_decode(q, kc, vc, lens, table, bs, d ** -0.5, "bf16", 1.0, 1.0, seqs=[s])
+        done += int(lens[s]) * hkv * d * 2 * 2 + 2 * hq * d * 2
+        count += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return done, time.perf_counter() - t0, count
+
+
+def oracle_decode_rate_all_cores(budget_s, seqs_per_worker=2):
+    """Oracle throughput with one single-threaded process per host core (spawned, so no
+    process is forked after the CUDA context exists): summed bytes / longest worker window."""
+    import multiprocessing as mp
+    n = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_worker, [(2003 + w, budget_s, seqs_per_worker) for w in range(n)])
+    return sum(r[0] for r in res) / max(r[1] for r in res), n, sum(r[2] for r in res)
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def oracle_decode_rate(wl, budget_s, max_seqs=64):
     """Oracle throughput (algorithmic bytes/s): whole sampled sequences, cycled until the budget is spent."""
     order = [int(s) for s in np.random.default_rng(0).permutation(wl.batch)[:max_seqs]]
@@ -331,7 +392,18 @@ def run_pkv(args, rank, world, device):
         rate, nseq, ntok, dt = oracle_decode_rate(wl, budget_s=args.cpu_budget)
         cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{nseq} whole-sequence decodes drawn from the decode batch ({ntok} cached tokens, "
-                         f"all 32 heads), fp64 NumPy, single thread, {dt:.1f} s"}
+                         f"all 32 heads), fp64 NumPy, single thread, {dt:.1f} s",
+               "cpu_model": cpu_model()}
+        if args.cpu_all_cores_budget > 0:
+            try:
+                rate_n, ncores, nseq_n = oracle_decode_rate_all_cores(args.cpu_all_cores_budget)
+                cpu["all_cores"] = {
+                    "value": rate_n / 1e9, "unit": "GB/s", "cores": ncores,
+                    "sample": f"{nseq_n} whole-sequence decodes, one single-threaded oracle process per core, "
+                              f"each on 2 seeded sequences of the decode batch's shapes and length distribution, "
+                              f"{args.cpu_all_cores_budget:.0f} s"}
+            except Exception as e:  # the single-thread figure stands alone
+                cpu["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
 
     clocks = ClockSampler(device)
     if world > 1:
@@ -728,6 +800,8 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-all-cores-budget", type=float, default=8.0,
+                    help="seconds of the all-cores oracle timing (0: skip)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "prefill"], default=None,
