@@ -333,14 +333,22 @@ def oracle_decode_rate_all_cores(budget_s, seqs_per_worker=2):
 
 
 def cpu_model():
+    """The host CPU's model name (x86), or its implementer and part ids (Arm cpuinfo has no name)."""
+    import platform
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu model")):
-                    return line.split(":", 1)[1].strip()
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
     except OSError:
         pass
-    import platform
+    if fields.get("model name"):
+        return fields["model name"]
+    if fields.get("cpu implementer") and fields.get("cpu part"):
+        return (f"{platform.machine()} CPU implementer {fields['cpu implementer']} "
+                f"part {fields['cpu part']}")
     return platform.processor() or platform.machine()
 
 
