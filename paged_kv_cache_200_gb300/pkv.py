@@ -339,9 +339,10 @@ def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_l
     ``block_table`` is int32 ``[B, max_blocks_per_seq]``.  ``max_len_q`` /
     ``max_len_k`` are host upper bounds of the lengths (no device sync is made).
     Paged mode: ``gather_k_tokens`` (a host bound on the summed keys of the
-    sequences with more than one query) lets the library gather their K/V into
-    a packed bf16 buffer first, which small blocks and FP8 caches (uint8 E4M3
-    codes, value = code * k_scale / v_scale) use.
+    sequences the prefill tiles serve) lets the library gather their K/V into
+    a packed bf16 buffer first, which blocks under 64 tokens and one-byte
+    caches (uint8 E4M3 or int8 codes, value = code * k_scale / v_scale) use;
+    one-byte caches need it.
     """
     _require_cuda(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table)
     T, Hq, D = q.shape
