@@ -140,8 +140,10 @@ PKV_API int pkv_copy_blocks(void* k_cache, void* v_cache, int64_t block_bytes, i
                             const int32_t* block_pairs, int32_t num_pairs, int32_t* err_flag, void* stream);
 
 /*
- * Workspace bytes pkv_paged_attn_decode needs for these sizes on the current
- * device (0 is a valid answer).  max_seqlen_k is a host upper bound of
+ * Workspace bytes pkv_paged_attn_decode (and pkv_paged_attn_decode_with_kvcache)
+ * needs for these sizes on the current device, whatever the cache type (0 is a
+ * valid answer; the split plan depends on the SM count and on the cache type,
+ * and the larger plan is sized).  max_seqlen_k is a host upper bound of
  * cache_seqlens.  Returns 0 for invalid sizes as well; the call itself then
  * reports the error.
  */
