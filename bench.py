@@ -504,7 +504,45 @@ def extra_workloads(pkv, W, device, pk, args):
     out.update(multi_query_workload(pkv, W, device, pk, args))
     out.update(copy_workload(pkv, W, device, pk, args))
     out.update(write_sweep(pkv, device, pk, args))
+    try:  # last: a failed graph capture must not cost the legs above
+        out.update(example_latency(pkv, W, device))
+    except Exception as e:
+        out["decode_example_latency"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
     return out
+
+
+def example_latency(pkv, W, device, iters=200):
+    """The docs' worked example (3 sequences, 4 q / 2 kv heads, d64): one write + decode step is
+    latency-bound, so it is timed eagerly (two host calls per step) and as a replayed CUDA graph
+    (launch overhead hidden); no roofline applies at this size."""
+    wl = W.decode_example(device=device)
+    kc, vc = wl.k_cache.clone(), wl.v_cache.clone()
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    out = torch.empty_like(wl.q)
+    need = pkv.lib().pkv_paged_attn_decode_workspace(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim,
+                                                     wl.max_seqlen)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+
+    def step():
+        pkv.kv_cache_write(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
+        pkv.paged_attn_decode(wl.q, kc.view(shape4), vc.view(shape4), wl.cache_seqlens, wl.block_table, wl.scale,
+                              max_seqlen_k=wl.max_seqlen, out=out, workspace_buf=ws)
+
+    eager_ms = time_calls(step, iters)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph_ms = time_calls(graph.replay, iters)
+    return {"decode_example_latency": {
+        "workload": "docs' worked example: 3 seqs (30/32/70 cached + 1), 4 q / 2 kv heads, d64, block 32; "
+                    "write + decode per step",
+        "eager_us_per_step": eager_ms * 1e3, "graph_us_per_step": graph_ms * 1e3, "iters": iters}}
 
 
 def with_kvcache_workload(pkv, W, device, pk, args):
