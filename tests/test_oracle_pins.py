@@ -391,6 +391,33 @@ def test_decode_equals_varlen_with_one_query():
     assert np.array_equal(dec, var) and np.array_equal(dlse, vlse.T)
 
 
+def test_each_query_of_a_multi_query_sequence_is_a_decode_over_its_prefix():
+    """Speculative verification (several new tokens per sequence): under bottom-right
+    alignment, query i of a sequence with Lq queries and Lk keys is a one-query decode over
+    the first i + Lk - Lq + 1 keys.  This is the identity the decode kernels rely on when
+    they serve such rows one by one."""
+    rng = np.random.default_rng(31)
+    lk = [9, 14, 6]
+    lq = [3, 4, 1]
+    table, kc, vc, _, _ = _tiny_paged_case(rng, lk, 4, 2, 8, 4)
+    total_q = sum(lq)
+    q = _rand_bf16(rng, (total_q, 4, 8))
+    var, vlse = O.paged_attn_varlen(q, kc, vc, O.cu_seqlens_from_lens(lq), O.cu_seqlens_from_lens(lk), 0.3,
+                                    block_table=table, block_size=4)
+    row = 0
+    for b in range(len(lk)):
+        for i in range(lq[b]):
+            keys = i + lk[b] - lq[b] + 1
+            one = np.full(len(lk), 0)
+            one[b] = keys
+            dec, dlse = O.paged_attn_decode(q[row:row + 1].repeat(len(lk), axis=0), kc, vc, one, table, 4, 0.3,
+                                            seqs=[b])
+            # same terms, summed over a masked longer row on the varlen side: fp64 rounding only
+            assert np.allclose(dec[b], var[row], rtol=1e-12, atol=1e-13), (b, i)
+            assert np.allclose(dlse[b], vlse[:, row], rtol=1e-12, atol=1e-13), (b, i)
+            row += 1
+
+
 def test_chunked_prefill_equals_whole_prefill():
     """Prefix reuse: queries of a later chunk over prefix+chunk keys = the same rows of the whole prefill."""
     rng = np.random.default_rng(27)
