@@ -471,6 +471,25 @@ def test_fp8_attention_uses_dequantised_values():
         assert np.array_equal(out[b], o[0])
 
 
+def test_int8_attention_uses_dequantised_values():
+    """INT8 cache (A18): attention runs on code * scale, each code an exact integer in [-127, 127]."""
+    rng = np.random.default_rng(30)
+    lens = [5, 7]
+    table, kc, vc, _, _ = _tiny_paged_case(rng, lens, 2, 1, 8, 4)
+    kq = O.quantize_to_int8(kc, np.float32(40.0))
+    vq = O.quantize_to_int8(vc, np.float32(25.0))
+    q = _rand_bf16(rng, (2, 2, 8))
+    ks, vs = 1 / 40.0, 1 / 25.0
+    out, _ = O.paged_attn_decode(q, kq, vq, np.array(lens), table, 4, 0.3, "int8", ks, vs)
+    kd = kq.astype(np.float64) * np.float64(np.float32(ks))
+    vd = vq.astype(np.float64) * np.float64(np.float32(vs))
+    for b, L in enumerate(lens):
+        kr = np.stack([kd[table[b][p // 4] * 4 + p % 4] for p in range(L)])
+        vr = np.stack([vd[table[b][p // 4] * 4 + p % 4] for p in range(L)])
+        o, _ = O.attention_rows(O.bf16_bits_to_f64(q[b])[None], kr, vr, 0.3, True)
+        assert np.array_equal(out[b], o[0])
+
+
 # ---------------------------------------------------------------------------
 # copy-on-write of shared blocks ([CH15] "PagedAttention：メモリを「ページ」で貸し出す")
 # ---------------------------------------------------------------------------
