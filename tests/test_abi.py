@@ -68,6 +68,43 @@ def test_copy_blocks_host_validation():
     assert lib.pkv_copy_blocks(nul, nul, 4096, 8, nul, 3, nul, nul) == 1
 
 
+def test_empty_calls_do_nothing_and_invalid_sizes_are_rejected():
+    """Degenerate calls return before any launch: an empty batch is a no-op, while a bad
+    size is rejected even when there is nothing to compute."""
+    pkv = built_library()
+    lib = pkv.lib()
+    nul = ctypes.c_void_p(0)
+
+    def decode(batch, Hq=8, Hkv=2, D=128, bs=16, scale=0.1):
+        return lib.pkv_paged_attn_decode(nul, nul, nul, 0, nul, nul, 4, batch, Hq, Hkv, D, bs, 8, 64, scale, 1.0,
+                                         1.0, nul, nul, nul, 0, nul, nul)
+
+    assert decode(0) == 0                 # empty batch: nothing to do
+    assert decode(-1) == 1                # negative batch
+    assert decode(0, scale=0.0) == 1      # an invalid scale is rejected even with nothing to do
+    assert decode(3, scale=0.0) == 1
+    assert decode(3) == 1                 # null pointers with work to do
+
+    def varlen(batch, total_q, max_len_q, Hq=8, Hkv=2, D=128, causal=1):
+        return lib.pkv_paged_attn_varlen(nul, nul, nul, 0, nul, nul, batch, total_q, 0, max_len_q, 0, nul, 0, 0, 0,
+                                         Hq, Hkv, D, 0.1, causal, 1.0, 1.0, nul, nul, nul, 0, nul, nul)
+
+    assert varlen(0, 0, 0) == 0           # empty batch
+    assert varlen(4, 0, 0) == 0           # no queries
+    assert varlen(4, 10, 4) == 1          # null pointers with work to do
+    assert varlen(4, 10, 4, D=96) == 2    # unsupported head dim
+    assert varlen(4, 10, 4, causal=0) == 2  # only causal attention is provided
+    assert varlen(4, 10, 4, Hq=6, Hkv=4) == 1  # heads not a multiple of the kv heads
+
+    def append(batch):
+        return lib.pkv_paged_attn_decode_with_kvcache(nul, nul, 1024, nul, 1024, nul, nul, 0, nul, nul, 4, batch, 8,
+                                                      2, 128, 16, 8, 64, 0.1, 1.0, 1.0, 1.0, 1.0, nul, nul, nul, 0,
+                                                      nul, nul)
+
+    assert append(0) == 0
+    assert append(2) == 1
+
+
 def _split_plan(batch, num_kv_heads, max_len, sms, resident):
     """The decode split plan as the library states it: positions per CTA (a multiple of 64,
     at least 512, at most the whole sequence).  Few (sequence, kv head) units: the split
