@@ -44,6 +44,8 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attn HBM GB/s (% of peak) & tokens/s; varlen prefill TFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 7900.0       # GB300 datasheet HBM3e bandwidth (context beside the measured copy peak)
+NOMINAL_BF16_TFLOPS = 2250.0   # GB300 datasheet dense bf16 (context beside the measured cuBLAS peak)
 L2_BYTES = 126 * 2 ** 20
 
 
@@ -427,9 +429,9 @@ def run_pkv(args, rank, world, device):
     e2e_ms, h2d, d2h = time_e2e(step, max(1, min(args.steps, args.e2e_steps)), 3)
     e2e_ms = max_over_ranks(e2e_ms, device)
 
-    also = {}
+    also, legs = {}, {}
     if not args.no_extra:
-        also.update(extra_workloads(pkv, W, device, pk, args))
+        also, legs = extra_workloads(pkv, W, device, pk, args)
 
     dec_bytes = decode_bytes(wl)
     achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
@@ -470,21 +472,30 @@ def run_pkv(args, rank, world, device):
             "traffic": traffic,
             "algorithmic_bytes": dec_bytes,
             "launch_ms": dec_ms,
-            "peak_source": pk["source"],
+            "peak_source": pk["source"] + " copy bandwidth (hbm_gbs)",
+            "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
         },
         "e2e": {"value": job_throughput_gbs(nbytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": step.launches * args.steps,
         "clocks": clk,
-        "also": also,
     }
     if cpu is not None:
         result["cpu_baseline"] = cpu
+    result["also"] = also
+    # compact figures of the other workloads last, so that the end of the line carries them
+    result["legs"] = legs
     return result
 
 
+def _r(x, n=4):
+    """x rounded to n significant digits (keeps the compact figures short)."""
+    return float(f"{x:.{n}g}") if isinstance(x, float) else x
+
+
 def extra_workloads(pkv, W, device, pk, args):
-    out = {}
+    """The other workloads: full records (``also``) and compact figures (``legs``)."""
+    also, legs = {}, {}
     for dt in ("bf16", "fp8_e4m3", "int8"):
         wl = W.long_decode(device=device, cache_dtype=dt)
         step = DecodeStep(pkv, wl)
@@ -492,23 +503,39 @@ def extra_workloads(pkv, W, device, pk, args):
         ms, dec_ms = time_decode_steps(step, steps, 3)
         b = decode_bytes(wl)
         ach = b / (dec_ms * 1e-3) / 1e9
-        out[f"long_decode_{dt}"] = {
+        also[f"long_decode_{dt}"] = {
             "workload": "8 seqs x 131072 cached tokens (+1), 64 q / 8 kv heads, d128, block 32, " + dt + " cache",
             "decode_ms": dec_ms, "step_ms": ms, "GB_per_s": ach, "frac_of_hbm_peak": ach / pk["hbm_gbs"],
             "tokens_per_s": wl.batch / (ms * 1e-3), "steps": steps}
+        legs[f"long_decode_{dt}"] = {"ms": _r(dec_ms), "GB_s": _r(ach), "frac": _r(ach / pk["hbm_gbs"])}
         del step, wl
         torch.cuda.empty_cache()
-    if hasattr(pkv, "paged_attn_varlen") and hasattr(pkv.lib(), "pkv_paged_attn_varlen"):
-        out.update(prefill_workload(pkv, W, device, pk, args))
-    out.update(with_kvcache_workload(pkv, W, device, pk, args))
-    out.update(multi_query_workload(pkv, W, device, pk, args))
-    out.update(copy_workload(pkv, W, device, pk, args))
-    out.update(write_sweep(pkv, device, pk, args))
+    also.update(with_kvcache_workload(pkv, W, device, pk, args))
+    legs["decode_with_kvcache"] = {"ms": _r(also["decode_with_kvcache"]["step_ms"]),
+                                   "frac": _r(also["decode_with_kvcache"]["frac_of_hbm_peak"])}
+    also.update(copy_workload(pkv, W, device, pk, args))
+    also.update(write_sweep(pkv, device, pk, args))
+    mq = multi_query_workload(pkv, W, device, pk, args)["multi_query_decode"]
+    also["multi_query_decode"] = mq
+    legs["multi_query_decode"] = {"ms": _r(mq["ms"]), "GB_s_once": _r(mq["GB_per_s"]),
+                                  "frac": _r(mq["frac_of_hbm_peak"])}
+    pre = prefill_workload(pkv, W, device, pk, args)
+    also.update(pre)
+    for key in ("varlen_prefill_packed", "varlen_prefill_paged", "varlen_prefill_paged_direct",
+                "varlen_prefill_paged_fp8", "varlen_prefill_paged_int8"):
+        if key in pre:
+            e = pre[key]
+            legs[key] = {"ms": _r(e["ms"]), "TFLOP_s": _r(e["TFLOP_per_s"]), "frac": _r(e["frac_of_bf16_peak"])}
+    legs["varlen_prefill_packed"]["roofline"] = {k: _r(v) for k, v in pre["varlen_prefill_packed"]["roofline"].items()}
+    mc = pre["mixed_chunked"]
+    legs["mixed_chunked"] = {"ms": _r(mc["ms"]), "roof_ms": _r(mc["roofline_ms"]), "frac": _r(mc["frac_of_roofline"])}
     try:  # last: a failed graph capture must not cost the legs above
-        out.update(example_latency(pkv, W, device))
+        also.update(example_latency(pkv, W, device))
+        ex = also["decode_example_latency"]
+        legs["decode_example_us"] = {"eager": _r(ex["eager_us_per_step"]), "graph": _r(ex["graph_us_per_step"])}
     except Exception as e:
-        out["decode_example_latency"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
-    return out
+        also["decode_example_latency"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+    return also, legs
 
 
 def example_latency(pkv, W, device, iters=200):
@@ -596,8 +623,10 @@ def multi_query_workload(pkv, W, device, pk, args):
     res = {"multi_query_decode": {
         "workload": "64 seqs x 4 new tokens over U[1024,16384] cached tokens, 32 q / 8 kv, d128, bs16; every query "
                     "row served by the split-KV decode kernels (one varlen call)", "ms": ms,
-        "GB_per_s_read": per_query / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": per_query / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-        "kv_bytes_once": once, "kv_bytes_read": per_query, "tokens_per_s": wl.total_q / (ms * 1e-3), "iters": iters}}
+        "GB_per_s": once / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": once / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "GB_per_s_incl_L2_rereads": per_query / (ms * 1e-3) / 1e9,
+        "kv_bytes_once": once, "kv_bytes_read_per_query_rows": per_query, "tokens_per_s": wl.total_q / (ms * 1e-3),
+        "iters": iters}}
     del wl, kc, vc, out, ws
     torch.cuda.empty_cache()
     return res
@@ -686,7 +715,11 @@ def prefill_workload(pkv, W, device, pk, args):
         "workload": "8 seqs, q_len = k_len in U[128,2048] (" + ",".join(str(int(x)) for x in wl.q_lens) +
                     "), 32 q / 8 kv heads, d128, causal, packed K/V",
         "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "causal_flops": flops,
-        "iters": iters}
+        "iters": iters,
+        # the call is the prep kernel (a few microseconds) and the prefill kernel, timed alone: burst peak
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / pk["bf16_tflops"], "flops": flops, "launch_ms": ms,
+                     "frac_of_nominal": tf / NOMINAL_BF16_TFLOPS}}
     del wl, out
     wp = W.varlen_prefill(device=device, paged=True)
     shape4 = (wp.num_blocks, wp.block_size, wp.num_kv_heads, wp.head_dim)

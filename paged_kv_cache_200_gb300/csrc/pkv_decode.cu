@@ -834,15 +834,16 @@ extern "C" int pkv_paged_attn_decode_with_kvcache(const void* q, const void* k_n
                                                   void* workspace, size_t workspace_bytes, int32_t* err_flag,
                                                   void* stream) {
   using namespace pkv;
+  // a one-byte cache needs finite positive inverse scales, even when there is nothing to do
+  if (cache_dtype != PKV_BF16 && (!(k_inv_scale > 0.f) || !(v_inv_scale > 0.f) || !std::isfinite(k_inv_scale) ||
+                                  !std::isfinite(v_inv_scale)))
+    return PKV_ERR_INVALID_ARG;
   if (batch > 0) {
     const int64_t row = (int64_t)num_kv_heads * head_dim;
     if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
     if (k_new_row_stride < row || v_new_row_stride < row || k_new_row_stride % 8 || v_new_row_stride % 8)
       return PKV_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
-    if (cache_dtype == PKV_FP8_E4M3 && (!(k_inv_scale > 0.f) || !(v_inv_scale > 0.f) ||
-                                        !std::isfinite(k_inv_scale) || !std::isfinite(v_inv_scale)))
-      return PKV_ERR_INVALID_ARG;
   }
   const AppendArgs app{k_new, k_new_row_stride, v_new, v_new_row_stride, k_inv_scale, v_inv_scale};
   return decode_impl(q, k_cache, v_cache, cache_dtype, cache_seqlens, block_table, max_blocks_per_seq, batch,

@@ -14,6 +14,8 @@
 // hardware's round-to-nearest-even saturating conversion.
 #include <cuda_fp8.h>
 
+#include <cmath>
+
 #include "pkv_device.cuh"
 #include "pkv_host.h"
 
@@ -79,6 +81,11 @@ extern "C" int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const voi
   if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
   const int64_t row_elems = (int64_t)num_kv_heads * head_dim;
   if (row_elems % 8 != 0 || row_elems > (1 << 20)) return PKV_ERR_UNSUPPORTED;
+  // a one-byte cache needs finite positive inverse scales (0, a negative value, inf or NaN
+  // would store codes that stand for no value of the input)
+  if (cache_dtype != PKV_BF16 && (!(k_inv_scale > 0.f) || !(v_inv_scale > 0.f) || !std::isfinite(k_inv_scale) ||
+                                  !std::isfinite(v_inv_scale)))
+    return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
   if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
   if (k_row_stride < row_elems || v_row_stride < row_elems || k_row_stride % 8 || v_row_stride % 8)

@@ -3,10 +3,12 @@
 import numpy as np
 import torch
 
+# bf16 attention: |err| <= 2e-2 + 2e-2*|ref|.  One-byte KV caches (FP8 E4M3, and INT8 on the
+# same bound): |err| <= 6e-2, absolute only, against the oracle on the dequantised cache.
 BF16_ATOL = 2e-2
 BF16_RTOL = 2e-2
 FP8_ATOL = 6e-2
-FP8_RTOL = 2e-2
+FP8_RTOL = 0.0
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

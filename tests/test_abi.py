@@ -55,6 +55,40 @@ def test_host_side_argument_validation():
     assert lib.pkv_paged_attn_decode(*args(8, 3, 128, 16)) == 1
 
 
+def test_one_byte_caches_need_valid_inverse_scales():
+    """An FP8 or INT8 cache write (and the append of decode-with-append) refuses a zero, negative,
+    infinite or NaN inverse scale before any launch; a bf16 cache ignores the scales."""
+    pkv = built_library()
+    lib = pkv.lib()
+    nul = ctypes.c_void_p(0)
+    bad = (0.0, -1.0, float("inf"), float("nan"))
+    for dt in (2, 3):  # PKV_FP8_E4M3, PKV_INT8
+        for x in bad:
+            for ki, vi in ((x, 1.0), (1.0, x)):
+                assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 4, 1, 128, nul, nul, dt, 16, nul, ki, vi, nul,
+                                              nul) == 1
+                assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 0, 1, 128, nul, nul, dt, 16, nul, ki, vi, nul,
+                                              nul) == 1
+    # valid scales and zero tokens: nothing to do; bf16: the scales are not used
+    for dt in (2, 3):
+        assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 0, 1, 128, nul, nul, dt, 16, nul, 0.5, 2.0, nul, nul) == 0
+    assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 0, 1, 128, nul, nul, 0, 16, nul, 0.0, float("nan"), nul,
+                                  nul) == 0
+
+    # decode with append: an empty batch with valid scales is a no-op, with a bad one it is refused
+    def append(dt, ki, vi):
+        return lib.pkv_paged_attn_decode_with_kvcache(nul, nul, 1024, nul, 1024, nul, nul, dt, nul, nul, 4, 0, 8, 2,
+                                                      128, 16, 8, 64, 0.1, 1.0, 1.0, ki, vi, nul, nul, nul, 0, nul,
+                                                      nul)
+
+    for dt in (2, 3):
+        assert append(dt, 0.5, 0.25) == 0
+        for x in bad:
+            assert append(dt, x, 1.0) == 1
+            assert append(dt, 1.0, x) == 1
+    assert append(0, 0.0, float("nan")) == 0  # bf16 cache: the scales are not used
+
+
 def test_copy_blocks_host_validation():
     pkv = built_library()
     lib = pkv.lib()
