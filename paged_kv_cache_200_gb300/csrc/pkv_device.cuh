@@ -263,6 +263,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int c
       : "memory");
 }
 
+// Prefetch the box of a 3-D tensor map at these coordinates into L2 (no
+// shared memory written, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -11,26 +11,32 @@
 // Causal alignment: query i of a sequence with Lq queries and Lk keys sees key
 // j iff j <= i + Lk - Lq (the queries are the last Lq positions; prefix reuse).
 //
-// Persistent kernel, one 320-thread CTA per SM.  A work item is 128 query rows
-// of one (sequence, query head); items are claimed through a global counter,
-// longest first, and published to the CTA's warps through a shared ring.
-//   warp 0      producer: Q once per item (TMA), then K/V tiles of 128 keys
+// Persistent kernel, one 352-thread CTA per SM.  A work item is a pair of
+// adjacent 128-row query tiles (A, then B) of one (sequence, query head),
+// paired from the sequence's end; both tiles read the same K/V tiles (B's
+// keys: A's last step is masked), so each K/V tile is loaded once for 256
+// query rows.  Items are claimed through a global counter, longest first, and
+// published to the CTA's warps through a shared ring.
+//   warp 0      producer: Q of both tiles (TMA), then K/V tiles of 128 keys
 //               (2 stages each), K one tile ahead of V.  Packed K/V: one TMA
 //               box per head-dim half.  Paged K/V: one box per page and
 //               half, each issued by its own lane, the block ids read two
 //               tiles ahead.
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, then for each
-//               64-key half h of the tile O_h += P_h V_h with P read from TMEM.
-//   warps 2..9  softmax, two warps per 32 rows: warps 2..5 own keys 0..63 of
-//               every tile, warps 6..9 keys 64..127.  Each half is its own
-//               online-softmax stream with its own O accumulator, so the halves
-//               never synchronise inside the key loop; they are merged once in
-//               the epilogue (log2-sum-exp weights), like two KV splits.  The
-//               running max moves only when it grows by more than 2^8, so O is
-//               rescaled rarely.  P (bf16 pairs) overwrites its S columns.
-// TMEM (512 columns): S buffers [0,128) and [128,256); O_0 at 256, O_1 at 384.
+//   warps 1, 2  MMA issuers, one thread each: warp 1 for tile A, warp 2 for
+//               tile B.  Per K/V tile j a thread issues O += P(j-1) V(j-1),
+//               then S(j) = Q K(j)^T.  One thread issues an M=128 MMA only
+//               every ~120-140 cycles, whatever N is, so the two tiles' MMAs
+//               come from two threads and interleave in the tensor core.
+//   warps 3..6  softmax of tile A, warps 7..10 of tile B: one thread per query
+//               row, all 128 keys of each tile.  The running max moves only
+//               when it grows by more than 2^8, so O is rescaled rarely (by
+//               the same thread, in TMEM).  P (bf16 pairs) overwrites half
+//               of its S columns.  After the tile's last PV the group reads O,
+//               releases it, and stores the normalised rows.
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A at 256, O_B at 384.
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA flags
-// PKV_DEVERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+// PKV_DEVERR_TIMEOUT, waits (bounded) for its own copies and MMAs, frees TMEM
+// and returns.
 #include <cmath>
 
 #include "pkv_device.cuh"
@@ -39,10 +45,12 @@
 namespace pkv {
 namespace {
 
-constexpr int kBM = 128;          // query rows per CTA
-constexpr int kBN = 128;          // keys per tile
-constexpr int kThreads = 320;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kBM = 128;          // query rows per query tile
+constexpr int kPairRows = 2 * kBM;  // query rows per work item (tiles A and B)
+constexpr int kBN = 128;          // keys per K/V tile
+constexpr int kThreads = 352;     // producer warp, 2 MMA warps, 2 softmax warp groups
+constexpr int kSoftmaxWarp0 = 3;  // first softmax warp (tile A: warps 3..6, tile B: 7..10)
+constexpr int kGroupThreads = 128;  // a softmax warp group: one thread per row of its tile
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -58,7 +66,7 @@ struct PrefillParams {
   int32_t num_blocks;
   int32_t num_heads;
   int32_t group;
-  int32_t n_qtiles;
+  int32_t n_pairs;       // query-tile pairs of the longest sequence
   int32_t batch;
   int32_t route_decode;  // sequences with at most this many queries are left to the decode kernels (0: none)
   int32_t* item_counter; // work-item counter, zero at launch
@@ -66,6 +74,7 @@ struct PrefillParams {
   float v_mul;           // output factor (FP8 V scale of a gathered cache, else 1)
   int64_t total_q;
   uint16_t* out;
+  int32_t out_v8;        // out is 32-byte aligned: rows are stored 32 bytes per instruction
   float* lse;
   int32_t* err;
 };
@@ -143,6 +152,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+
 // ---------------------------------------------------------------------------
 // shared-memory plan
 // ---------------------------------------------------------------------------
@@ -152,53 +162,49 @@ struct Smem {
   static constexpr int kAtoms = D / 64;                 // 64-element (128-byte) column groups
   static constexpr int kTileBytes = 128 * D * 2;        // a [128 x D] bf16 tile
   static constexpr int kAtomBytes = 128 * 128;          // [128 rows x 128 B]
-  static constexpr int kQ = 0;                          // 2 buffers (by work item)
+  static constexpr int kQ = 0;                          // query tiles A and B
   static constexpr int kK = kQ + 2 * kTileBytes;        // 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
   static constexpr int kBar = kV + 2 * kTileBytes;
-  static constexpr int kNumBars = 28;
+  static constexpr int kNumBars = 32;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
   static constexpr int kRingData = kMisc + 16;          // 4 ring slots x 8 ints (item, q0, Lq, k0, Lk)
-  static constexpr int kXchg = kRingData + 4 * 32;      // float m[2][128], l[2][128]
-  static constexpr int kStage = kXchg + 4 * 128 * 4;    // output staging: 8 softmax warps x 16 half rows
-  static constexpr int kTotal = kStage + 8 * 16 * D;
+  static constexpr int kEpi = kRingData + 4 * 32;       // per softmax thread: output and lse offsets, rows (32 B)
+  static constexpr int kTotal = kEpi + 2 * kGroupThreads * 32;
   static constexpr int kAlloc = kTotal + 1024;          // slack to align the base to 1024
 };
+static_assert(Smem<128>::kAlloc <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
 
 constexpr int kRing = 4;  // work-item ring slots
 
-// mbarrier indices (each one distinct; checked below).  K and V stages have
-// no "empty" barriers of their own: a K stage is free once S of its tile is
-// done (kSFull), a V stage once the tile's PV is (kPvDone).  Fewer commits
-// and waits keep the MMA thread, which runs nearly in step with the tensor
-// core, issuing MMAs.
+// mbarrier indices (each one distinct; checked below).  "X" is the query
+// tile of the pair (0: A, 1: B).  Every barrier below can only be one phase
+// ahead of its waiter (each role's next arrival depends on the waiter having
+// seen the previous one), so single parity waits are unambiguous.
 enum Bar {
-  kQFull0 = 0,       // +buffer (2)
-  kQEmpty0 = 2,      // +buffer (2)
-  kKFull0 = 4,       // +stage (2)
-  kVFull0 = 6,       // +stage (2)
-  kSFull0 = 8,       // +S buffer (2)
-  kRingFull0 = 10,   // +slot (4): a work item index published by the producer
-  kDrain = 14,
-  kXchgA = 15,       // softmax threads: (m, l) of both halves published
-  kXchgB = 16,       // softmax threads have read O and the exchange slots (MMA waits before the next item's PV)
-  // The next two sets have one barrier per S buffer, i.e. per tile parity.
-  // A parity wait can only tell "phase k done" from "phase k pending" when
-  // the barrier is never two phases away from the waiter; with one barrier
-  // per tile parity, tile t's phase has tile t-2's before it (known complete:
-  // S(t) was issued after PV(t-2)) and tile t+2's after it (cannot have
-  // started), so every wait below is unambiguous even when skipped tiles'
-  // phases were never waited on.
-  kPFull0 = 17,      // +buffer (2): P of that tile written, both halves (softmax -> MMA)
-  kPvDone0 = 19,     // +buffer (2): O += P V of that tile landed (MMA -> softmax, producer)
-  kRingEmpty0 = 21,  // +slot (4): the MMA warp and the 8 softmax warps have read the slot
-  kBarCount = 25
+  kQFull0 = 0,       // +X: Q tile landed (producer -> MMA)
+  kQEmpty0 = 2,      // +X: last S of the item's tile X done, Q buffer free (MMA -> producer)
+  kKFull0 = 4,       // +stage: K tile landed
+  kKEmpty0 = 6,      // +stage: every S reading the K stage done (one arrival per MMA thread)
+  kVFull0 = 8,       // +stage: V tile landed
+  kVEmpty0 = 10,     // +stage: every PV reading the V stage done (one arrival per MMA thread)
+  kSFull0 = 12,      // +X: S of the next tile done (MMA -> softmax X); also means PV_X of the tile before is done
+  kPFull0 = 14,      // +X: P of that tile written (softmax X, 128 arrivals -> MMA)
+  kODone0 = 16,      // +X: the item's last PV_X done (MMA -> softmax X epilogue)
+  kOFree0 = 18,      // +X: softmax X has read O_X (128 arrivals -> MMA, before the next item's first PV_X)
+  kRingFull0 = 20,   // +slot (4): a work item index published by the producer
+  kRingEmpty0 = 24,  // +slot (4): both MMA threads and the 8 softmax warps have read the slot
+  kDrain0 = 28,      // +X: every MMA of issuer X done (end of the kernel)
+  kTurn0 = 30,       // +X: the other softmax group finished its tile; group X may start its next one
+  kBarCount = 32
 };
-static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kVFull0 == kKFull0 + 2 &&
-                  kSFull0 == kVFull0 + 2 && kRingFull0 == kSFull0 + 2 && kDrain == kRingFull0 + kRing &&
-                  kXchgA == kDrain + 1 && kXchgB == kXchgA + 1 && kPFull0 == kXchgB + 1 &&
-                  kPvDone0 == kPFull0 + 2 && kRingEmpty0 == kPvDone0 + 2 && kBarCount == kRingEmpty0 + kRing,
+static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kKEmpty0 == kKFull0 + 2 &&
+                  kVFull0 == kKEmpty0 + 2 && kVEmpty0 == kVFull0 + 2 && kSFull0 == kVEmpty0 + 2 &&
+                  kPFull0 == kSFull0 + 2 && kODone0 == kPFull0 + 2 && kOFree0 == kODone0 + 2 &&
+                  kRingFull0 == kOFree0 + 2 && kRingEmpty0 == kRingFull0 + kRing && kDrain0 == kRingEmpty0 + kRing &&
+                  kTurn0 == kDrain0 + 2 && kBarCount == kTurn0 + 2,
               "mbarrier index ranges must not overlap");
+static_assert(Smem<128>::kNumBars >= kBarCount && Smem<64>::kNumBars >= kBarCount, "too few mbarrier slots");
 
 // A sequence's query/key offsets and (checked) lengths.  The producer warp
 // reads them from global memory once per work item and hands them to the
@@ -206,8 +212,12 @@ static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kVFull0 == k
 struct SeqBase {
   int q0, Lq, k0, Lk;
 };
+// One work item: the pair's two query tiles X = 0 (A), 1 (B), each with its
+// first row, rows inside the sequence and K/V tiles it attends (n[X]).
 struct Seq {
-  int q0, Lq, k0, Lk, row0, rows, diag, n_kv;
+  int q0, Lq, k0, Lk, diag;
+  int row0[2], rows[2], n[2];
+  int n_kv;  // K/V tiles the pair reads: max(n[0], n[1])
   bool skip;
 };
 
@@ -234,43 +244,66 @@ __device__ __forceinline__ SeqBase seq_check(const PrefillParams& p, const int (
   if (bad && report) flag_error(p.err, PKV_DEVERR_LENGTH);
   return s;
 }
-__device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase& b0, int qtile) {
+// Pair pe of a sequence, counted from its end, holds query tiles T-2-2pe (A)
+// and T-1-2pe (B), T = ceil(Lq/128): the last tiles, which see the most keys,
+// pair up, and a sequence with an odd tile count leaves tile 0 alone (it sees
+// one K/V tile).  Both tiles run the same K/V steps (tile A's step past its
+// diagonal is fully masked), so the two softmax groups alternate to the end.
+__device__ __forceinline__ void pair_tiles(int Lq, int pe, int& tA, int& tB) {
+  const int T = (Lq + kBM - 1) / kBM;
+  tB = T - 1 - 2 * pe;
+  tA = tB - 1;
+}
+__device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase& b0, int pair) {
   Seq s;
   s.q0 = b0.q0;
   s.Lq = b0.Lq;
   s.k0 = b0.k0;
   s.Lk = b0.Lk;
-  s.row0 = qtile * kBM;
-  s.rows = min(kBM, s.Lq - s.row0);
   s.diag = s.Lk - s.Lq;
-  s.skip = s.rows <= 0 || s.Lq <= p.route_decode;
-  const int kmax = s.row0 + s.rows - 1 + s.diag;  // last key the last row sees
   const int kv_tiles = (s.Lk + kBN - 1) / kBN;
-  s.n_kv = kmax < 0 ? 0 : min(kmax / kBN + 1, kv_tiles);
+  int t[2];
+  pair_tiles(s.Lq, pair, t[0], t[1]);
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if (t[x] < 0) {
+      s.row0[x] = 0;
+      s.rows[x] = 0;
+      s.n[x] = 0;
+    } else {
+      s.row0[x] = t[x] * kBM;
+      s.rows[x] = min(kBM, s.Lq - s.row0[x]);
+      const int kmax = s.row0[x] + s.rows[x] - 1 + s.diag;  // last key the tile's last row sees
+      s.n[x] = kmax < 0 ? 0 : min(kmax / kBN + 1, kv_tiles);
+    }
+  }
+  // tile B's rows see more keys than tile A's; both run B's K/V steps
+  s.n_kv = max(s.n[0], s.n[1]);
+  if (s.rows[0] > 0) s.n[0] = s.n_kv;
+  s.skip = s.rows[1] <= 0 || s.Lq <= p.route_decode;
   return s;
 }
 
-static_assert(Smem<128>::kNumBars >= kBarCount && Smem<64>::kNumBars >= kBarCount, "too few mbarrier slots");
-
-// Work item -> (sequence, query tile, head).  Items are ordered by query tile,
-// last tiles (most keys under causal masking) first, then sequence, then head,
-// so CTAs running side by side share K/V through L2.
+// Work item -> (sequence, query-tile pair, head).  Items are ordered by pair
+// (counted from each sequence's end: the pairs with the most keys under
+// causal masking first), then sequence, then head, so CTAs running side by
+// side share K/V through L2.
 struct Item {
-  int b, qtile, head;
+  int b, pair, head;
 };
 __device__ __forceinline__ Item item_of(const PrefillParams& p, int it) {
   const int per = p.batch * p.num_heads;
   Item x;
-  x.qtile = p.n_qtiles - 1 - it / per;
+  x.pair = it / per;
   const int rem = it % per;
   x.b = rem / p.num_heads;
   x.head = rem % p.num_heads;
   return x;
 }
 
-// Persistent kernel: one CTA per SM walks the work items blockIdx.x,
-// blockIdx.x + gridDim.x, ...  All roles walk the same list and keep running
-// counters (item, tile) so the barriers' phases continue across items.
+// Persistent kernel: one CTA per SM takes work items from the global counter.
+// All roles walk the same published list and keep running counters (items,
+// tiles) so the barriers' phases continue across items.
 template <int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -281,29 +314,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_items = p.n_qtiles * p.batch * p.num_heads;
+  const int n_items = p.n_pairs * p.batch * p.num_heads;
 
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kQFull0 + s), 1);
-      mbar_init(bar(kQEmpty0 + s), 1);
-      mbar_init(bar(kKFull0 + s), 1);
-      mbar_init(bar(kVFull0 + s), 1);
-      mbar_init(bar(kSFull0 + s), 1);
-      mbar_init(bar(kPFull0 + s), kSoftmaxThreads);
-      mbar_init(bar(kPvDone0 + s), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(kQFull0 + x), 1);
+      mbar_init(bar(kQEmpty0 + x), 1);
+      mbar_init(bar(kKFull0 + x), 1);
+      mbar_init(bar(kKEmpty0 + x), 2);
+      mbar_init(bar(kVFull0 + x), 1);
+      mbar_init(bar(kVEmpty0 + x), 2);
+      mbar_init(bar(kSFull0 + x), 1);
+      mbar_init(bar(kPFull0 + x), kGroupThreads);
+      mbar_init(bar(kODone0 + x), 1);
+      mbar_init(bar(kOFree0 + x), kGroupThreads);
     }
-    mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kDrain0), 1);
+    mbar_init(bar(kDrain0 + 1), 1);
+    mbar_init(bar(kTurn0), kGroupThreads / 32);
+    mbar_init(bar(kTurn0 + 1), kGroupThreads / 32);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(bar(kRingFull0 + r), 1);
-      mbar_init(bar(kRingEmpty0 + r), 1 + (kSoftmaxThreads / 32));
+      mbar_init(bar(kRingEmpty0 + r), 2 + 2 * kGroupThreads / 32);
     }
-    mbar_init(bar(kXchgA), kSoftmaxThreads);
-    mbar_init(bar(kXchgB), kSoftmaxThreads);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -318,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // TMEM columns: S buffers [0,128) and [128,256); O halves [256, 256+D) and [384, 384+D).
-  // P of a tile (bf16 pairs) overwrites the first 32 columns of each half's S columns.
-  auto tS = [&](int sb) -> uint32_t { return tmem + 128 * sb; };
-  auto tO = [&](int h) -> uint32_t { return tmem + 256 + 128 * h; };
+  // TMEM columns: S of tile X at 128 X (P of that tile, bf16 pairs: keys 0..63
+  // over its columns 0..31, keys 64..127 over 64..95), O of tile X at 256 + 128 X.
+  auto tS = [&](int x) -> uint32_t { return tmem + 128 * x; };
+  auto tO = [&](int x) -> uint32_t { return tmem + 256 + 128 * x; };
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -332,8 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // publishes each one that has work into a 4-slot ring that the MMA and
   // softmax warps read in order.  -1 ends the list.
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRingData);
-  // Consumer side: item of the u-th ring entry (or -1, also on timeout) and its sequence.
-  auto ring_get = [&](int u, SeqBase& sb) -> int {
+  // Consumer side: item of the u-th ring entry (or -1, also on timeout), its
+  // pair and head (decoded by the producer) and its sequence.
+  auto ring_get = [&](int u, SeqBase& sb, Item& x) -> int {
     const int slot = u & (kRing - 1);
     if (!mbar_wait(bar(kRingFull0 + slot), (u / kRing) & 1, abort_flag)) return -1;
     const volatile int* e = ring + 8 * slot;
@@ -342,6 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sb.Lq = e[2];
     sb.k0 = e[3];
     sb.Lk = e[4];
+    x.pair = e[5];
+    x.head = e[6];
+    x.b = 0;
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kRingEmpty0 + slot));
     return it;
@@ -350,9 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     int last_k[2] = {-1, -1}, last_v[2] = {-1, -1}, last_q[2] = {-1, -1};
-    int g = 0, uq = 0, ur = 0;  // tiles, items with keys, ring entries
+    int g = 0, ur = 0;        // K/V tiles, ring entries
+    int qc[2] = {0, 0};       // Q loads per tile slot
     bool ok = true;
-    auto publish = [&](int it, const SeqBase& sb) -> bool {
+    auto publish = [&](int it, const SeqBase& sb, const Item& x) -> bool {
       const int slot = ur & (kRing - 1);
       if (ur >= kRing && !mbar_wait(bar(kRingEmpty0 + slot), ((ur / kRing) - 1) & 1, abort_flag)) return false;
       if (lane == 0) {
@@ -362,6 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         e[2] = sb.Lq;
         e[3] = sb.k0;
         e[4] = sb.Lk;
+        e[5] = x.pair;
+        e[6] = x.head;
         mbar_arrive(bar(kRingFull0 + slot));
       }
       __syncwarp();
@@ -372,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the current one's last, and its offsets are loaded while those tiles
     // are issued: neither latency then sits between two items, and a claimed
     // item waits only a few tiles (dynamic balance is kept).  A skipped item
-    // (a sequence left to the decode kernels, or a query tile past its end)
-    // moves the counter past the other heads of its (tile, sequence), which
-    // are skipped too.
+    // (a sequence left to the decode kernels, or a pair past its end) moves
+    // the counter past the other heads of its (pair, sequence), which are
+    // skipped too.
     int claim = 0;  // lane 0: atomic result for the next item
     bool claimed = false, resolved = false;
     int it = 0, next = n_items;
@@ -396,16 +440,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && it < n_items) {
       claimed = resolved = false;
       const Item x = item_of(p, it);
-      const SeqBase si = seq_check(p, raw, x.qtile == 0 && x.head == 0 && lane == 0);
-      const Seq sq = seq_derive(p, si, x.qtile);
+      const SeqBase si = seq_check(p, raw, x.pair == 0 && x.head == 0 && lane == 0);
+      const Seq sq = seq_derive(p, si, x.pair);
       if (sq.skip) {
-        const int block_end = (it / p.num_heads + 1) * p.num_heads;  // first item of the next (tile, sequence)
+        const int block_end = (it / p.num_heads + 1) * p.num_heads;  // first item of the next (pair, sequence)
         if (lane == 0 && block_end < n_items) atomicMax(p.item_counter, block_end);
         resolve_next();
         it = next;
         continue;
       }
-      if (!publish(it, si)) { ok = false; break; }
+      if (!publish(it, si, x)) { ok = false; break; }
       if (sq.n_kv == 0) {
         resolve_next();
         it = next;
@@ -413,15 +457,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int kvh = x.head / p.group;
       const int32_t* bt = kPaged ? p.block_table + (int64_t)x.b * p.max_blocks : nullptr;
-      const int qb = uq & 1, qu = uq >> 1;
-      if (qu > 0 && !mbar_wait(bar(kQEmpty0 + qb), (qu - 1) & 1, abort_flag)) { ok = false; break; }
-      if (lane == 0) {
-        mbar_expect_tx(bar(kQFull0 + qb), L::kTileBytes);
-        for (int a = 0; a < L::kAtoms; ++a)
-          tma_load_3d(sbase + L::kQ + qb * L::kTileBytes + a * L::kAtomBytes, &tm_q, a * 64, x.head,
-                      sq.q0 + sq.row0, bar(kQFull0 + qb));
-      }
-      last_q[qb] = qu;
+      // Q of tile X (only when it attends keys), into its buffer once the
+      // previous item's last S of that tile is done
+      auto load_q = [&](int xq) -> bool {
+        if (sq.n[xq] == 0) return true;
+        if (qc[xq] > 0 && !mbar_wait(bar(kQEmpty0 + xq), (qc[xq] - 1) & 1, abort_flag)) return false;
+        if (lane == 0) {
+          mbar_expect_tx(bar(kQFull0 + xq), L::kTileBytes);
+          for (int a = 0; a < L::kAtoms; ++a)
+            tma_load_3d(sbase + L::kQ + xq * L::kTileBytes + a * L::kAtomBytes, &tm_q, a * 64, x.head,
+                        sq.q0 + sq.row0[xq], bar(kQFull0 + xq));
+        }
+        last_q[xq] = qc[xq];
+        ++qc[xq];
+        return true;
+      };
       const int br = kPaged ? p.box_rows : kBN;
       const int npages = kBN / br;
       // Paged tiles: lane (page pg, head-dim atom at) issues one box; at most
@@ -450,8 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue = [&](int t, int j, int my_slot) -> bool {  // t = 0: K, 1: V; local tile j
         const int gg = g + j;
         const int s = gg & 1, u = gg >> 1;
-        // the stage is free once the MMAs that read it are done: S(gg-2) for K, PV(gg-2) for V
-        const uint32_t empty = t ? bar(kPvDone0 + s) : bar(kSFull0 + s);
+        const uint32_t empty = bar((t ? kVEmpty0 : kKEmpty0) + s);
         const uint32_t full = bar((t ? kVFull0 : kKFull0) + s);
         if (u > 0 && !mbar_wait(empty, (u - 1) & 1, abort_flag)) return false;
         const uint32_t dst = sbase + (t ? L::kV : L::kK) + s * L::kTileBytes;
@@ -477,18 +526,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         (t ? last_v : last_k)[s] = u;
         return true;
       };
-      // K runs one tile ahead of V within the item
+      // The next item's Q rows, prefetched into L2 once it is known, so that
+      // its Q loads (which wait for this item's last S of each tile) hit L2.
+      auto prefetch_next_q = [&]() {
+        if (lane != 0 || next >= n_items) return;
+        const Item y = item_of(p, next);
+        const int lq = raw[1] - raw[0];
+        if (lq <= p.route_decode) return;
+        int tq[2];
+        pair_tiles(lq, y.pair, tq[0], tq[1]);
+        for (int xq = 0; xq < 2; ++xq)
+          if (tq[xq] >= 0)
+            for (int a = 0; a < L::kAtoms; ++a) tma_prefetch_3d(&tm_q, a * 64, y.head, raw[0] + tq[xq] * kBM);
+      };
+      // K(0), Q_A, Q_B (the K stage frees up before the Q buffers do), then K
+      // one tile ahead of V
       int slot_cur = tile_slot(0, tile_blk(0));
       int blk_next = tile_blk(1);
       if (!issue(0, 0, slot_cur)) { ok = false; break; }
+      if (!load_q(0) || !load_q(1)) { ok = false; break; }
       const int claim_at = sq.n_kv > 3 ? sq.n_kv - 3 : 0;  // tiles ahead of the item's end
+      const int resolve_at = min(claim_at + 1, sq.n_kv - 1);
       for (int j = 0; j < sq.n_kv && ok; ++j) {
         if (j == claim_at) claim_next();
-        if (j > claim_at && j == sq.n_kv - 1) resolve_next();
         const int blk_after = tile_blk(j + 2);
         const int slot_next = (j + 1 < sq.n_kv) ? tile_slot(j + 1, blk_next) : 0;
         if (j + 1 < sq.n_kv && !issue(0, j + 1, slot_next)) { ok = false; break; }
         if (!issue(1, j, slot_cur)) { ok = false; break; }
+        if (j == resolve_at) {
+          resolve_next();
+          prefetch_next_q();
+        }
         slot_cur = slot_next;
         blk_next = blk_after;
       }
@@ -496,155 +564,217 @@ __global__ void __launch_bounds__(kThreads, 1)
       resolve_next();
       it = next;
       g += sq.n_kv;
-      ++uq;
     }
-    if (ok && !publish(-1, SeqBase{0, 0, 0, 0})) ok = false;
+    if (ok && !publish(-1, SeqBase{0, 0, 0, 0}, Item{0, 0, 0})) ok = false;
     if (!ok) fail();
-    // every copy this CTA issued has landed before shared memory is released
+    // Every copy this CTA issued has landed before shared memory is released.
+    // These waits ignore the abort flag (a copy in flight always lands); a
+    // copy that was never issued leaves its phase pending until the deadline.
     for (int s = 0; s < 2; ++s) {
-      if (last_q[s] >= 0) mbar_wait(bar(kQFull0 + s), last_q[s] & 1, abort_flag);
-      if (last_k[s] >= 0) mbar_wait(bar(kKFull0 + s), last_k[s] & 1, abort_flag);
-      if (last_v[s] >= 0) mbar_wait(bar(kVFull0 + s), last_v[s] & 1, abort_flag);
+      if (last_q[s] >= 0) mbar_wait(bar(kQFull0 + s), last_q[s] & 1, nullptr);
+      if (last_k[s] >= 0) mbar_wait(bar(kKFull0 + s), last_k[s] & 1, nullptr);
+      if (last_v[s] >= 0) mbar_wait(bar(kVFull0 + s), last_v[s] & 1, nullptr);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);
-    constexpr uint32_t kIdescPV = make_idesc(kBM, D, true);
-    bool ok = true, issued = false;
-    int g = 0, uq = 0;
-    // O_h += P_h V_h for global tile t (local index jt within its item, whose keys end at Lk)
-    auto issue_pv = [&](int t, int jt, int Lk) -> bool {
-      if (!mbar_wait(bar(kVFull0 + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
-      // the first PV of an item overwrites O: the previous item's epilogue must have read it
-      if (jt == 0 && uq > 0 && !mbar_wait(bar(kXchgB), (uq - 1) & 1, abort_flag)) return false;
-      const uint32_t vbase = sbase + L::kV + (t & 1) * L::kTileBytes;
-      // keys at or beyond Lk: zero their V rows (stale or foreign data must not meet P = 0)
-      const int valid = Lk - jt * kBN;
-      if (valid < kBN) {
-        uint8_t* vs = smem + L::kV + (t & 1) * L::kTileBytes;
-        const int first = valid > 0 ? valid : 0;
-        const int nchunks = (kBN - first) * 8;  // 16-byte chunks per atom
-        for (int a = 0; a < L::kAtoms; ++a)
-          for (int c = lane; c < nchunks; c += 32)
-            *reinterpret_cast<uint4*>(vs + a * L::kAtomBytes + (first + c / 8) * 128 + (c % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      // descriptors differ only in their start-address field (bits 0..13, address >> 4)
-      const uint64_t vdesc = sw128_desc(vbase, L::kAtomBytes, 1024);
-      // both halves' P, then all eight PV MMAs and one commit: every wait and
-      // commit the MMA thread runs between MMAs leaves the tensor core idle
-      if (!mbar_wait(bar(kPFull0 + (t & 1)), (t >> 1) & 1, abort_flag)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t acc = jt > 0 ? 1u : 0u;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t pa = tS(t & 1) + 64 * h;  // P_h: 32 columns of bf16 pairs = 64 keys
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tO(h), pa + 8 * kk, vdesc + (uint64_t)(((64 * h + 16 * kk) * 128) >> 4), kIdescPV,
-                        kk > 0 ? 1u : acc);
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Thread 0 of warp 1 issues tile A's MMAs, thread 0 of warp 2 tile B's.
+    // One thread issues an M=128 MMA only every ~120-140 cycles (its own
+    // issue latency, whatever N is), well below the tensor core's rate, so
+    // the two tiles' MMAs come from two threads and interleave in the tensor
+    // core.  Each thread runs its own tile's S and PV in issue order; the K/V
+    // stages are released by one arrival of each thread.  Lanes 1..31 idle.
+    const int xq = warp - 1;
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);
+      constexpr uint32_t kIdescPV = make_idesc(kBM, D, true);
+      bool ok = true, issued = false;
+      int g = 0;   // K/V tiles consumed
+      int qc = 0;  // items whose tile attends keys (Q buffer uses)
+      int pc = 0;  // P tiles consumed
+      int oc = 0;  // O accumulations completed (items)
+      for (int u = 0; ok; ++u) {
+        const int slot = u & (kRing - 1);
+        if (!mbar_wait(bar(kRingFull0 + slot), (u / kRing) & 1, abort_flag)) break;
+        const volatile int* e = ring + 8 * slot;
+        const int it = e[0];
+        const SeqBase si{e[1], e[2], e[3], e[4]};
+        const int pair = e[5];
+        mbar_arrive(bar(kRingEmpty0 + slot));
+        if (it < 0) break;
+        const Seq sq = seq_derive(p, si, pair);
+        const int nkv = sq.n_kv;
+        if (nkv == 0) continue;
+        const int nx = xq ? sq.n[1] : sq.n[0];  // 0 or nkv (the tiles run in lockstep)
+        if (nx == 0) {
+          // this tile has no rows: release each K/V stage of the item once it is loaded
+          for (int j = 0; j < nkv && ok; ++j) {
+            const int gg = g + j, s = gg & 1;
+            if (!mbar_wait(bar(kKFull0 + s), (gg >> 1) & 1, abort_flag) ||
+                !mbar_wait(bar(kVFull0 + s), (gg >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive(bar(kKEmpty0 + s));
+            mbar_arrive(bar(kVEmpty0 + s));
+          }
+          g += nkv;
+          continue;
         }
-        mma_commit(bar(kPvDone0 + (t & 1)));  // also frees V stage t & 1
-      }
-      __syncwarp();
-      return true;
-    };
-    for (int u = 0; ok; ++u) {
-      SeqBase si;
-      const int it = ring_get(u, si);
-      if (it < 0) break;
-      const Item x = item_of(p, it);
-      const Seq sq = seq_derive(p, si, x.qtile);
-      if (sq.n_kv == 0) continue;
-      const int qb = uq & 1;
-      if (!mbar_wait(bar(kQFull0 + qb), (uq >> 1) & 1, abort_flag)) { ok = false; break; }
-      for (int j = 0; j < sq.n_kv; ++j) {
-        const int gg = g + j, s = gg & 1;
-        if (!mbar_wait(bar(kKFull0 + s), (gg >> 1) & 1, abort_flag)) { ok = false; break; }
-        // S(gg) overwrites buffer s, whose P(gg-2) the PV issued just before
-        // reads: tcgen05.mma operations from one thread execute in issue
-        // order, so no wait for that PV's completion is needed here.
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t qdesc = sw128_desc(sbase + L::kQ + qb * L::kTileBytes, 16, 1024);
+        // S(j) = Q K(j)^T overwrites the S/P columns that the PV issued just
+        // before reads: tcgen05.mma operations from one thread execute in issue
+        // order, so no wait for that PV's completion is needed; the softmax
+        // threads' reads of S(j-1) were ordered before that PV by its P wait.
+        auto issue_s = [&](int j) -> bool {
+          const int gg = g + j, s = gg & 1;
+          if (!mbar_wait(bar(kKFull0 + s), (gg >> 1) & 1, abort_flag)) return false;
+          if (j == 0 && !mbar_wait(bar(kQFull0 + xq), qc & 1, abort_flag)) return false;
+          const uint64_t qdesc = sw128_desc(sbase + L::kQ + xq * L::kTileBytes, 16, 1024);
           const uint64_t kdesc = sw128_desc(sbase + L::kK + s * L::kTileBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t off = (uint64_t)(((kk >> 2) * L::kAtomBytes + (kk & 3) * 32) >> 4);
-            mma_bf16(tS(s), qdesc + off, kdesc + off, kIdescQK, kk > 0 ? 1u : 0u);
+            mma_bf16(tS(xq), qdesc + off, kdesc + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(kSFull0 + s));  // also frees K stage s
-          if (j == sq.n_kv - 1) mma_commit(bar(kQEmpty0 + qb));
+          mma_commit(bar(kSFull0 + xq));
+          mma_commit(bar(kKEmpty0 + s));
+          if (j == nx - 1) mma_commit(bar(kQEmpty0 + xq));
+          issued = true;
+          return true;
+        };
+        // O += P(jt) V(jt)
+        auto issue_pv = [&](int jt) -> bool {
+          const int gg = g + jt, s = gg & 1;
+          if (!mbar_wait(bar(kVFull0 + s), (gg >> 1) & 1, abort_flag)) return false;
+          // keys at or beyond Lk (only in a sequence's last K/V tile): zero their
+          // V rows, so that stale or foreign data never meets P = 0.  Both MMA
+          // threads do this, each before its own PV; they only ever write zeros.
+          const int valid = sq.Lk - jt * kBN;
+          if (valid < kBN) {
+            uint8_t* vs = smem + L::kV + s * L::kTileBytes;
+            const int first = valid > 0 ? valid : 0;
+            for (int a = 0; a < L::kAtoms; ++a)
+              for (int row = first; row < kBN; ++row) {
+                uint4* dst = reinterpret_cast<uint4*>(vs + a * L::kAtomBytes + row * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+              }
+            fence_proxy_async_smem();
+          }
+          // the item's first PV overwrites O: the previous item's epilogue must have read it
+          if (jt == 0 && oc > 0 && !mbar_wait(bar(kOFree0 + xq), (oc - 1) & 1, abort_flag)) return false;
+          if (!mbar_wait(bar(kPFull0 + xq), pc & 1, abort_flag)) return false;
+          tc_fence_after();  // P written (and O read) by the softmax threads before these MMAs
+          // descriptors differ only in their start-address field (bits 0..13, address >> 4)
+          const uint64_t vdesc = sw128_desc(sbase + L::kV + s * L::kTileBytes, L::kAtomBytes, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)  // P: 8 columns of bf16 pairs per 16 keys, keys 64.. at column 64
+            mma_bf16_ts(tO(xq), tS(xq) + 8 * kk + (kk >= 4 ? 32 : 0), vdesc + (uint64_t)((16 * kk * 128) >> 4),
+                        kIdescPV, (jt > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(kVEmpty0 + s));
+          if (jt == nx - 1) mma_commit(bar(kODone0 + xq));
+          ++pc;
+          if (jt == nx - 1) ++oc;
+          return true;
+        };
+        for (int j = 0; j <= nkv && ok; ++j) {
+          if (j >= 1 && !issue_pv(j - 1)) ok = false;
+          if (ok && j < nkv && !issue_s(j)) ok = false;
         }
-        __syncwarp();
-        issued = true;
-        if (j > 0 && !issue_pv(gg - 1, j - 1, sq.Lk)) { ok = false; break; }
+        if (!ok) break;
+        ++qc;
+        g += nkv;
       }
-      if (ok && !issue_pv(g + sq.n_kv - 1, sq.n_kv - 1, sq.Lk)) ok = false;
-      g += sq.n_kv;
-      ++uq;
+      if (!ok) fail();
+      // drain: all MMAs this thread issued have completed before TMEM is
+      // released (an issued MMA always completes, so the abort flag is ignored)
+      if (issued) {
+        mma_commit(bar(kDrain0 + xq));
+        mbar_wait(bar(kDrain0 + xq), 0, nullptr);
+      }
     }
-    if (!ok) fail();
-    // drain: all MMAs this thread issued have completed before TMEM is released
-    if (issued) {
-      if (lane == 0) mma_commit(bar(kDrain));
-      __syncwarp();
-      mbar_wait(bar(kDrain), 0, abort_flag);
-    }
+    __syncwarp();  // the warp reconverges before the CTA barrier below
   } else {
     // ------------------------------------------------------------------ softmax warps
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;   // keys [64*half, 64*half + 64) of every tile
+    const int xq = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warp group
+    const int quarter = warp & 3;       // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;  // TMEM lane == query row in the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float c = p.scale_log2;
-    float* xm = reinterpret_cast<float*>(smem + L::kXchg);
-    float* xl = xm + 256;
     bool ok = true;
-    int g = 0, ux = 0;  // tiles and work items (with keys) processed
+    int sc = 0, oc = 0;  // S tiles and items (with keys) processed
+    int tc = 0;          // tiles processed in turn with the other group
     for (int u = 0; ok; ++u) {
       SeqBase si;
-      const int it = ring_get(u, si);
+      Item x;
+      const int it = ring_get(u, si, x);
       if (it < 0) break;
-      const Item x = item_of(p, it);
-      const Seq sq = seq_derive(p, si, x.qtile);
-      const int qi = sq.row0 + r;
-      const int64_t row = (int64_t)sq.q0 + qi;
-      const bool row_valid = r < sq.rows;
-      uint16_t* orow = p.out + (row * p.num_heads + x.head) * D;
-      if (sq.n_kv == 0) {
+      // Only a few values live across the tile loop (the 128 scores need the
+      // registers): the output offsets, the row limits and the loop counts.
+      int rows, nkv, vis0, jm;
+      int64_t obase, lse_idx;  // this tile's first output element; this row's lse index
+      bool turns;
+      {
+        const Seq sq = seq_derive(p, si, x.pair);
+        // (selects, not an indexed load: xq differs between warps but the arrays stay in registers)
+        rows = xq ? sq.rows[1] : sq.rows[0];
+        const int row0 = xq ? sq.row0[1] : sq.row0[0];
+        nkv = xq ? sq.n[1] : sq.n[0];
+        obase = ((int64_t)(sq.q0 + row0) * p.num_heads + x.head) * D;
+        lse_idx = (int64_t)x.head * p.total_q + sq.q0 + row0 + r;
+        // key limit of this row (bottom-right causal, inside the keys); tiles
+        // before jm need no mask for any row of the tile (its first row has
+        // the smallest limit)
+        vis0 = min(row0 + r + sq.diag, sq.Lk - 1);
+        const int first = row0 + sq.diag;  // limit of the tile's first row
+        jm = min(first < kBN - 1 ? 0 : (first + 1) / kBN, sq.Lk / kBN);
+        // When both tiles have rows, the two groups take turns, tile by tile
+        // (A0, B0, A1, B1, ...): each softmax then has the SM's sub-partitions
+        // to itself, and while one group works the other tile's MMAs run.
+        turns = sq.rows[0] > 0;
+      }
+      if (rows <= 0) continue;
+      // the offsets wait in shared memory while the tile loop runs (registers)
+      int64_t* epi = reinterpret_cast<int64_t*>(smem + L::kEpi) + 4 * (threadIdx.x - kSoftmaxWarp0 * 32);
+      epi[0] = obase;
+      epi[1] = lse_idx;
+      epi[2] = rows;
+      if (nkv == 0) {
+        const bool row_valid = r < rows;
         // rows that see no key: zeros and lse = -inf
         if (row_valid) {
-          for (int cc = half * (D / 16); cc < (half + 1) * (D / 16); ++cc)
-            reinterpret_cast<uint4*>(orow)[cc] = make_uint4(0, 0, 0, 0);
-          if (half == 0 && p.lse) p.lse[(int64_t)x.head * p.total_q + row] = -INFINITY;
+          uint16_t* orow = p.out + obase + (int64_t)r * p.num_heads * D;
+          for (int cc = 0; cc < D / 8; ++cc) reinterpret_cast<uint4*>(orow)[cc] = make_uint4(0, 0, 0, 0);
+          if (p.lse) p.lse[lse_idx] = -INFINITY;
         }
         continue;
       }
-      const int lim = qi + sq.diag;  // last visible key of this row
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < sq.n_kv; ++j) {
-        const int gg = g + j, sb = gg & 1;
-        if (!mbar_wait(bar(kSFull0 + sb), (gg >> 1) & 1, abort_flag)) { ok = false; break; }
+      for (int j = 0; j < nkv; ++j) {
+        if (!mbar_wait(bar(kSFull0 + xq), sc & 1, abort_flag)) { ok = false; break; }
+        ++sc;
+        if (turns) {  // tile A waits for B's previous tile, tile B for A's current one
+          const int need = xq == 0 ? tc - 1 : tc;
+          if (need >= 0 && !mbar_wait(bar(kTurn0 + xq), need & 1, abort_flag)) { ok = false; break; }
+        }
         tc_fence_after();
-        uint32_t sr[64];
-        PKV_TMEM_LD32(tS(sb) + lane_off + 64 * half, (sr + 0));
-        PKV_TMEM_LD32(tS(sb) + lane_off + 64 * half + 32, (sr + 32));
+        // All 128 scores of the row in one TMEM round trip; P of keys 64..127
+        // goes to columns 64..95 and of keys 0..63 to columns 0..31 (each half
+        // over S columns already read; columns 32..63 and 96..127 are unused).
+        const int key0 = j * kBN;
+        uint32_t sr[kBN];
+        PKV_TMEM_LD32(tS(xq) + lane_off + 0, (sr + 0));
+        PKV_TMEM_LD32(tS(xq) + lane_off + 32, (sr + 32));
+        PKV_TMEM_LD32(tS(xq) + lane_off + 64, (sr + 64));
+        PKV_TMEM_LD32(tS(xq) + lane_off + 96, (sr + 96));
         tmem_wait_ld();
-
-        const int key0 = j * kBN + 64 * half;
-        const bool need_mask = (key0 + 63 > sq.row0 + sq.diag) || (key0 + 64 > sq.Lk);
-        if (need_mask) {
-          const int vis = min(lim, sq.Lk - 1) - key0;  // columns 0..vis are visible
+        if (j >= jm) {
+          const int vis = vis0 - key0;  // columns 0..vis are visible
 #pragma unroll
-          for (int k = 0; k < 64; ++k) sr[k] = (k <= vis) ? sr[k] : __float_as_uint(-INFINITY);
+          for (int k = 0; k < kBN; ++k) sr[k] = (k <= vis) ? sr[k] : __float_as_uint(-INFINITY);
         }
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 64; k += 2)
+        for (int k = 0; k < kBN; k += 2)
           mx4[(k >> 1) & 3] = fmax3(mx4[(k >> 1) & 3], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
         const float mt = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c;
         float m_use = m;
@@ -656,118 +786,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float nm = live ? -m_use : -INFINITY;
         const uint64_t c2 = f32x2_pack(c, c), nm2 = f32x2_pack(nm, nm);
         uint64_t sum2[2] = {0ull, 0ull};
-        uint32_t pk[32];
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          float x0, x1;
-          f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nm2), x0, x1);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          sum2[(k >> 1) & 1] = fadd2(sum2[(k >> 1) & 1], f32x2_pack(p0, p1));
-          pk[k >> 1] = pack_bf16x2(p0, p1);
+        for (int h = 1; h >= 0; --h) {
+          // P of keys 64h..64h+63 as bf16 pairs, packed in place over the scores just used
+          uint32_t* pk = sr + 64 * h;
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            float x0, x1;
+            f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(pk[k]), __uint_as_float(pk[k + 1])), c2, nm2), x0, x1);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            sum2[(k >> 1) & 1] = fadd2(sum2[(k >> 1) & 1], f32x2_pack(p0, p1));
+            pk[k >> 1] = pack_bf16x2(p0, p1);
+          }
+          PKV_TMEM_ST32(tS(xq) + lane_off + 64 * h, pk);
         }
         float s00, s01, s10, s11;
         f32x2_unpack(sum2[0], s00, s01);
         f32x2_unpack(sum2[1], s10, s11);
         l = l * alpha + ((s00 + s01) + (s10 + s11));
         m = m_use;
-
-        // rescale O_half when this row's reference max moved (warp-collective TMEM access);
-        // the previous tile's PV must have landed first
+        // rescale O_X when this row's reference max moved (warp-collective TMEM
+        // access).  PV_X of the previous tile is done: it was issued before this
+        // tile's S, whose completion was just waited for.
         if (j > 0 && __any_sync(0xffffffffu, moved && alpha != 1.f)) {
-          const int tp = gg - 1;  // previous tile
-          if (!mbar_wait(bar(kPvDone0 + (tp & 1)), (tp >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
-            PKV_TMEM_LD32(tO(half) + lane_off + ch * 32, o);
+            PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            PKV_TMEM_ST32(tO(half) + lane_off + ch * 32, o);
+            PKV_TMEM_ST32(tO(xq) + lane_off + ch * 32, o);
           }
         }
-        // P_half (bf16 pairs) over the first 32 of this half's S columns
-        PKV_TMEM_ST32(tS(sb) + lane_off + 64 * half, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(kPFull0 + sb));
+        mbar_arrive(bar(kPFull0 + xq));
+        if (turns) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kTurn0 + (xq ^ 1)));
+          ++tc;
+        }
       }
       if (!ok) break;
-      const int glast = g + sq.n_kv - 1;
-      if (!mbar_wait(bar(kPvDone0 + (glast & 1)), (glast >> 1) & 1, abort_flag)) {
+      // ---- epilogue: O_X / l, released as soon as it is read, then stored ----
+      if (!mbar_wait(bar(kODone0 + xq), oc & 1, abort_flag)) {
         ok = false;
         break;
       }
+      ++oc;
       tc_fence_after();
-      // exchange (m, l) between the two halves of each row
-      xm[half * 128 + r] = m;
-      xl[half * 128 + r] = l;
-      mbar_arrive(bar(kXchgA));
-      if (!mbar_wait(bar(kXchgA), ux & 1, abort_flag)) { ok = false; break; }
-      const float m0 = xm[r], m1 = xm[128 + r];
-      const float l0 = xl[r], l1 = xl[128 + r];
-      const float ms = fmaxf(m0, m1);
-      const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - ms);
-      const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - ms);
-      const float lt = l0 * f0 + l1 * f1;
-      const float inv = lt > 0.f ? p.v_mul / lt : 0.f;
-      const float w0 = f0 * inv, w1 = f1 * inv;
-      // this half writes head dims [half*D/2, (half+1)*D/2) of every row
-      constexpr int kHalfRowBytes = D;           // D/2 bf16
-      constexpr int kCh = kHalfRowBytes / 16;    // 16-byte pieces of a half row
-      uint4 mine[kCh];
+      const float inv = l > 0.f ? p.v_mul / l : 0.f;
+      obase = epi[0];
+      lse_idx = epi[1];
+      const bool row_valid = r < (int)epi[2];
+      // O in 32-column chunks: read, normalise, pack to bf16 and store this
+      // thread's row piece (64 bytes) straight away, so no whole row is held in
+      // registers.  O is released after its last chunk is read.
+      uint4* orow = reinterpret_cast<uint4*>(p.out + obase + (int64_t)r * p.num_heads * D);
 #pragma unroll
-      for (int ch = 0; ch < D / 64; ++ch) {
-        const int col = half * (D / 2) + ch * 32;
-        uint32_t a[32], bb[32];
-        PKV_TMEM_LD32(tO(0) + lane_off + col, a);
-        PKV_TMEM_LD32(tO(1) + lane_off + col, bb);
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o);
         tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; k += 8) {
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(a[k + e]) * w0 + __uint_as_float(bb[k + e]) * w1;
-          mine[(ch * 32 + k) / 8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        if (ch == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(kOFree0 + xq));
         }
-      }
-      // Rows of one head are num_heads*D elements apart, so a thread storing
-      // its own row would touch a separate line per 16 bytes.  Instead the
-      // warp passes 16 rows at a time through its staging rows in shared
-      // memory (16-byte pieces XOR-swizzled by row) and stores whole half rows.
-      uint8_t* stg = smem + L::kStage + (warp - 2) * 16 * kHalfRowBytes;
+        if (row_valid) {
+          uint32_t w[16];
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
-        if ((lane >> 4) == pass) {
-          const int sr = lane & 15;
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+          if (p.out_v8) {  // whole 32-byte sectors, half the store instructions
 #pragma unroll
-          for (int c = 0; c < kCh; ++c)
-            *reinterpret_cast<uint4*>(stg + sr * kHalfRowBytes + ((c ^ (sr & (kCh - 1))) * 16)) = mine[c];
-        }
-        __syncwarp();
+            for (int h = 0; h < 2; ++h)
+              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + ch * 4 + 2 * h),
+                           "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
+                           "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                           : "memory");
+          } else {
 #pragma unroll
-        for (int i = 0; i < 16 * kCh / 32; ++i) {
-          const int idx = i * 32 + lane;
-          const int sr = idx / kCh, c = idx % kCh;
-          const int rr = quarter * 32 + pass * 16 + sr;  // row within the tile
-          if (rr < sq.rows) {
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + sr * kHalfRowBytes + ((c ^ (sr & (kCh - 1))) * 16));
-            uint16_t* dst = p.out + ((int64_t)(sq.q0 + sq.row0 + rr) * p.num_heads + x.head) * D + half * (D / 2) + c * 8;
-            *reinterpret_cast<uint4*>(dst) = val;
+            for (int q = 0; q < 4; ++q) orow[ch * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
         }
-        __syncwarp();
       }
-      if (half == 0 && row_valid && p.lse != nullptr)
-        p.lse[(int64_t)x.head * p.total_q + row] = lt > 0.f ? (ms + log2f(lt)) * kLn2 : -INFINITY;
-      // this thread has read O and the exchange slots; the MMA thread waits for all of them
-      // before the next item's first PV (so the softmax warps do not wait here)
-      tc_fence_before();
-      mbar_arrive(bar(kXchgB));
-      g += sq.n_kv;
-      ++ux;
+      if (row_valid && p.lse != nullptr) p.lse[lse_idx] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
     if (!ok) fail();
     tc_fence_before();
@@ -1016,7 +1120,7 @@ int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int64_t items = (int64_t)p.n_qtiles * batch * p.num_heads;
+  const int64_t items = (int64_t)p.n_pairs * batch * p.num_heads;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
   kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, p);
   return launch_status();
@@ -1116,7 +1220,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.num_blocks = num_blocks;
   p.num_heads = num_heads;
   p.group = num_heads / num_kv_heads;
-  p.n_qtiles = (max_len_q + kBM - 1) / kBM;
+  p.n_pairs = (max_len_q + kPairRows - 1) / kPairRows;
   p.batch = batch;
   p.route_decode = rmq;
   // FP8: the gathered codes are exact bf16 values; k_scale joins the logit
@@ -1125,6 +1229,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.v_mul = fp8 ? v_scale : 1.f;
   p.total_q = total_q;
   p.out = static_cast<uint16_t*>(out);
+  p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.lse = lse;
   p.err = err_flag;
   cudaStream_t st = as_stream(stream);
