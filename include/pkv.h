@@ -109,7 +109,8 @@ PKV_API int pkv_abi_version(void);
  *                and one round-to-nearest-even saturating conversion, or
  *                PKV_INT8: clamp(round_half_even(float(x) * inv_scale), -127, 127)
  *                ([CH15] KV size: FP8 or INT8 halve the cache; NaN stores 0).
- * k_inv_scale, v_inv_scale: 1/scale of each FP8 / INT8 cache (ignored for PKV_BF16).
+ * k_inv_scale, v_inv_scale: 1/scale of each FP8 / INT8 cache, finite and positive
+ *                (checked even when num_tokens == 0; ignored for PKV_BF16).
  * num_kv_heads*head_dim must be a multiple of 8.
  */
 PKV_API int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
@@ -162,9 +163,12 @@ PKV_API size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_heads,
  * with k_p, v_p taken from kv head h/(num_heads/num_kv_heads).  A sequence
  * with cache_seqlens[b] == 0 outputs zeros and lse = -inf.
  *
- * cache_dtype PKV_BF16, or PKV_FP8_E4M3 where the cached code c stands for
- * float(c)*k_scale (resp. v_scale).  Long sequences are split across CTAs and
- * merged by log-sum-exp; workspace holds the partial results.
+ * cache_dtype PKV_BF16, or a one-byte cache where the cached code c stands for
+ * c's value times k_scale (resp. v_scale): PKV_FP8_E4M3 (OCP E4M3) or
+ * PKV_INT8 (symmetric codes -127..127).  k_scale and v_scale must be finite
+ * and positive for a one-byte cache (ignored for PKV_BF16).  Long sequences
+ * are split across CTAs and merged by log-sum-exp; workspace holds the
+ * partial results.
  * max_seqlen_k: host upper bound of cache_seqlens (it sizes the split).
  */
 PKV_API int pkv_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, int32_t cache_dtype,
@@ -191,7 +195,9 @@ PKV_API int pkv_paged_attn_decode(const void* q, const void* k_cache, const void
  *
  * k_new, v_new:  bf16 [batch, num_kv_heads, head_dim] rows at k_new_row_stride /
  *                v_new_row_stride elements (multiples of 8), 16-byte aligned.
- * k_inv_scale, v_inv_scale: 1/scale of each FP8 cache (ignored for PKV_BF16).
+ * cache_dtype:   PKV_BF16, PKV_FP8_E4M3 or PKV_INT8 (stored as pkv_kv_cache_write does).
+ * k_inv_scale, v_inv_scale: 1/scale of each one-byte cache, finite and positive
+ *                (checked even when batch == 0; ignored for PKV_BF16).
  * max_seqlen_k:  host upper bound of cache_seqlens + 1 (the attended length);
  *                the workspace is pkv_paged_attn_decode_workspace(..., max_seqlen_k).
  * Other arguments as for pkv_paged_attn_decode.  A position whose block id is
@@ -242,19 +248,26 @@ PKV_API size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, i
  *
  * max_len_q, max_len_k: host upper bounds of the lengths (grid sizing).
  * total_k: packed mode: rows of the packed k/v.  Paged mode: 0, or an upper
- *          bound on the summed key counts of the sequences with more than one
- *          query.  With total_k > 0 and an FP8 cache or block_size < 64, those
- *          sequences' K/V are first gathered through the block table into a
- *          packed bf16 buffer in the workspace (FP8 codes widened exactly), and
- *          the packed tile loop runs on it: one small copy box per page and
- *          head-dim half would bound the paged loop.  Keys past the bound are
- *          not gathered and flagged (PKV_DEVERR_LENGTH).
- * kv_dtype: PKV_BF16, or PKV_FP8_E4M3 (paged mode with total_k > 0 only) where a
- *          cached code c stands for float(c)*k_scale (resp. v_scale).
+ *          bound on the summed key counts of the sequences the prefill tiles
+ *          serve (see routing below).  With total_k > 0 and a one-byte cache or
+ *          block_size < 64, those sequences' K/V are first gathered through the
+ *          block table into a packed bf16 buffer in the workspace (one-byte
+ *          codes widened exactly), and the packed tile loop runs on it: one
+ *          small copy box per page and head-dim half would bound the paged
+ *          loop.  Keys past the bound are not gathered and flagged
+ *          (PKV_DEVERR_LENGTH).
+ * kv_dtype: PKV_BF16; or, in paged mode, PKV_FP8_E4M3 or PKV_INT8, where a
+ *          cached code c stands for c's value times k_scale (resp. v_scale).
+ *          A one-byte cache needs total_k > 0 when some sequence has more
+ *          queries than the routing bound below (its tiles read the gathered
+ *          copy); otherwise the call returns PKV_ERR_UNSUPPORTED.
  * Supported: head_dim 64 or 128, causal != 0; paged block_size a multiple of 16
  * that divides 128 or is a multiple of 128.  All of q, k, v, out 16-byte aligned.
- * In paged mode sequences with exactly one query are computed by the decode
- * kernels (split-KV over the GQA group) instead of a 128-row tile.
+ * Routing (paged mode, num_heads/num_kv_heads <= 8): when no sequence has more
+ * than 8 queries, every query row is computed by the decode kernels over its
+ * own causal prefix (split-KV over the GQA group; speculative verification);
+ * otherwise only the sequences with exactly one query are, and the others by
+ * the 128-row tiles.
  */
 PKV_API int pkv_paged_attn_varlen(const void* q, const void* k, const void* v, int32_t kv_dtype,
                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
@@ -284,6 +297,10 @@ PKV_API int pkv_paged_attn_varlen(const void* q, const void* k, const void* v, i
  * - Every GPU that loads the library holds the 32 MiB array until the process exits.
  * - The first call on each device looks up the array's device address once
  *   (with that device current); make that first call before any stream capture.
+ *   The address is kept for the life of the process and stays valid while the
+ *   device's primary context lives: after a cudaDeviceReset (or anything else
+ *   that destroys and recreates that context) do not call this entry point again
+ *   in the same process.
  * - All calls share the array.  Nothing in it must start at zero, but calls that
  *   overlap on the GPU (e.g. on two streams) race on it and corrupt each other.
  * The caller still passes inputs and outputs (q, caches, metadata, out, lse).

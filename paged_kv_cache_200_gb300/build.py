@@ -44,16 +44,31 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
-    """Compile and link libpkv.so; return its path."""
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _newest_input() and not extra_flags:
-        return LIB_PATH
+TEST_BUILD_DIR = os.path.join(BUILD_DIR, "test")
+TEST_LIB_PATH = os.path.join(TEST_BUILD_DIR, "libpkv_test.so")
+# Test-only variant: every bounded wait inside a kernel gives up after 1 ms
+# instead of 2 s, and host-set hooks can withhold one TMA copy so that a wait
+# runs out (the failure-detection tests).  Never the product library.
+TEST_FLAGS = ["-DPKV_TEST_HOOKS", "-DPKV_TEST_WAIT_NS=1000000ull"]
+
+
+def build_test_library(verbose: bool = False) -> str:
+    """Compile the test-only variant of the library (see TEST_FLAGS); return its path."""
+    return build(verbose=verbose, extra_flags=TEST_FLAGS, out_path=TEST_LIB_PATH, build_dir=TEST_BUILD_DIR)
+
+
+def build(verbose: bool = False, force: bool = False, extra_flags=None, out_path: str = LIB_PATH,
+          build_dir: str = BUILD_DIR) -> str:
+    """Compile and link libpkv.so (or a variant at out_path); return its path."""
+    if not force and os.path.exists(out_path) and os.path.getmtime(out_path) >= _newest_input():
+        if not extra_flags or out_path != LIB_PATH:
+            return out_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
@@ -64,13 +79,13 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB_PATH + ".tmp"
+    tmp = out_path + ".tmp"
     cmd = [nvcc] + ARCH_FLAGS + ["-shared", "-o", tmp] + objs
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out_path)
+    return out_path
 
 
 if __name__ == "__main__":

@@ -95,6 +95,9 @@ struct DecodeParams {
   const uint16_t* v_new;
   int64_t k_new_stride, v_new_stride;  // elements between rows
   float k_inv, v_inv;                  // FP8: 1 / scale of each cache
+#ifdef PKV_TEST_HOOKS
+  int32_t test_skip_group;             // test builds: CTA (0,0,0), warp 0 withholds this group's copies (-1: none)
+#endif
 };
 
 // Sequence served by grid index z (or -1) and, in varlen mode, which of its
@@ -191,6 +194,9 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   const int n_splits = (len + p.split_tokens - 1) / p.split_tokens;
   if (split >= (n_splits > 0 ? n_splits : 1)) return;
   const int t_begin = split * p.split_tokens;
+#ifdef PKV_TEST_HOOKS
+  const bool skip_lane = p.test_skip_group >= 0 && split == 0 && kvh == 0 && z == 0;
+#endif
   const int t_end = min(t_begin + p.split_tokens, len);
   const int n_groups = t_end > t_begin ? (t_end - t_begin + kGroupTok - 1) / kGroupTok : 0;
   const int my_groups = n_groups > warp ? (n_groups - warp + kDecWarps - 1) / kDecWarps : 0;
@@ -275,6 +281,10 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
       const uint32_t bar = bar0 + 8 * st;
       const uint32_t dst = wsm_u32 + st * kStageBytes;
       fence_proxy_async_smem();  // order earlier generic writes (V tail zeroing) before the async copies
+#ifdef PKV_TEST_HOOKS
+      // test builds only: withhold this stage's copies and arrival, so that its wait runs out
+      if (skip_lane && warp == 0 && i == p.test_skip_group) return;
+#endif
       if (blk >= 0) {
         const int slot0 = blk * p.block_size + pos0 % p.block_size;
         mbar_expect_tx(bar, kStageBytes);
@@ -460,9 +470,13 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
     __syncwarp();  // every lane is done with this stage before it is refilled
     issue(i + kStages - 1);
   }
-  // copies issued but never consumed (only after a timeout) land before the CTA exits
+  // copies issued but never consumed (only after a timeout) land before the
+  // shared memory is reused; if one of them does not land in time either, the
+  // CTA writes nothing (its results are undefined, PKV_DEVERR_TIMEOUT is set)
+  bool drained = true;
   for (int i = consumed; i < min(my_groups, consumed + kStages - 1); ++i)
-    mbar_wait(bar0 + 8 * (i % kStages), (i / kStages) & 1, nullptr);
+    if (!mbar_wait(bar0 + 8 * (i % kStages), (i / kStages) & 1, nullptr)) drained = false;
+  if (__syncthreads_or(!drained)) return;
 
   // ---- merge the four warps of the CTA ----
 #pragma unroll
@@ -730,6 +744,10 @@ extern "C" size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_hea
 namespace pkv {
 namespace {
 
+#ifdef PKV_TEST_HOOKS
+int g_test_skip_group = -1;
+#endif
+
 struct AppendArgs {
   const void* k_new;
   int64_t k_new_stride;
@@ -805,6 +823,9 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
   }
   cudaStream_t st = as_stream(stream);
   const int64_t ns = (int64_t)num_blocks * block_size;
+#ifdef PKV_TEST_HOOKS
+  p.test_skip_group = g_test_skip_group;
+#endif
   return dispatch_decode(cache_dtype, head_dim, p, batch, pl, ns, st);
 }
 
@@ -923,7 +944,9 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
 // instead of a caller workspace.  Every GPU that loads this library holds the
 // array until the process exits.  Its device address is looked up once per
 // device (cudaGetSymbolAddress, with that device current) by the first call
-// made on that device; make that first call before any stream capture.
+// made on that device; make that first call before any stream capture.  The
+// cached address is valid while the device's primary context lives (a
+// cudaDeviceReset ends it, and the module may then load at another address).
 // Every call shares the array and finds the previous call's partials in it;
 // nothing in it needs to start at zero (each call writes every partial it
 // reads), but two calls that overlap on the GPU, on different streams,
@@ -974,3 +997,10 @@ extern "C" int pkv_paged_attn_decode_noalloc(const void* q, const void* k_cache,
                                batch, num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_seqlen_k, scale,
                                k_scale, v_scale, out, lse, scratch, kPkvFixedScratchBytes, err_flag, stream);
 }
+
+#ifdef PKV_TEST_HOOKS
+// Test builds only: the next decode calls withhold the copies of 16-position
+// group `group` of warp 0 in CTA (split 0, kv head 0, sequence 0), so that its
+// bounded wait runs out (-1 restores normal operation).
+extern "C" PKV_API void pkv_test_decode_skip_group(int group) { pkv::g_test_skip_group = group; }
+#endif

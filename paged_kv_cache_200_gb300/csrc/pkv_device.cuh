@@ -211,7 +211,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // mbarrier, TMA and timer helpers
 // ---------------------------------------------------------------------------
 
+#ifdef PKV_TEST_WAIT_NS
+constexpr uint64_t kWaitNs = PKV_TEST_WAIT_NS;  // test builds: a short limit
+#else
 constexpr uint64_t kWaitNs = 2000000000ull;  // every bounded wait gives up after 2 s
+#endif
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;

@@ -75,6 +75,9 @@ struct PrefillParams {
   int64_t total_q;
   uint16_t* out;
   int32_t out_v8;        // out is 32-byte aligned: rows are stored 32 bytes per instruction
+#ifdef PKV_TEST_HOOKS
+  int32_t test_skip_k;   // test builds: CTA 0 withholds the copy of this K tile (its count in the CTA; -1: none)
+#endif
   float* lse;
   int32_t* err;
 };
@@ -506,6 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = sbase + (t ? L::kV : L::kK) + s * L::kTileBytes;
         const CUtensorMap* map = t ? &tm_v : &tm_k;
         const int key0 = j * kBN;
+#ifdef PKV_TEST_HOOKS
+        // test builds only: withhold this K tile's copy and arrival, so that the waits on it run out
+        if (t == 0 && blockIdx.x == 0 && gg == p.test_skip_k) {
+          last_k[s] = u;
+          return true;
+        }
+#endif
         if constexpr (!kPaged) {
           if (lane == 0) {
             mbar_expect_tx(full, L::kTileBytes);
@@ -1058,6 +1068,10 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restric
 // host side
 // ---------------------------------------------------------------------------
 
+#ifdef PKV_TEST_HOOKS
+int g_test_skip_k = -1;
+#endif
+
 struct VarlenWs {
   size_t count_off, items_off, decode_off, cu_g_off, gk_off, gv_off, total;
 };
@@ -1166,13 +1180,17 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   if (head_dim != 128 && head_dim != 64) return PKV_ERR_UNSUPPORTED;
   if (kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E4M3 && kv_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
   const bool fp8 = kv_dtype != PKV_BF16;  // one-byte codes (E4M3 or INT8) with per-tensor scales
-  // a coded cache is read through the gather (paged mode, total_k > 0)
-  if (fp8 && (block_table == nullptr || total_k <= 0)) return PKV_ERR_UNSUPPORTED;
+  const bool paged = block_table != nullptr;
+  const bool route = routes_decode(paged, num_heads, num_kv_heads);
+  // no sequence has more queries than the routing bound: every query row goes
+  // to the decode kernels and no prefill tile runs
+  const bool all_routed = route && max_len_q <= kRouteMaxQ;
+  // the prefill tiles read a one-byte cache only through the gather (paged mode, total_k > 0)
+  if (fp8 && !all_routed && (!paged || total_k <= 0)) return PKV_ERR_UNSUPPORTED;
   if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
     return PKV_ERR_INVALID_ARG;
   if (!causal) return PKV_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
-  const bool paged = block_table != nullptr;
   if (paged) {
     if (block_size <= 0 || block_size % 16 != 0 || (block_size < 128 && 128 % block_size != 0) ||
         (block_size > 128 && block_size % 128 != 0))
@@ -1183,7 +1201,6 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return PKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
 
-  const bool route = routes_decode(paged, num_heads, num_kv_heads);
   const bool gather = uses_gather(paged, kv_dtype, block_size, total_k);
   const int route_items = route ? route_items_bound(batch, total_q, max_len_q) : 0;
   const int rmq = route ? route_max_q(max_len_q) : 0;  // queries up to which a sequence is routed
@@ -1205,9 +1222,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   const int64_t kv_rows = !paged ? (int64_t)total_k : gather ? (int64_t)total_k : (int64_t)num_blocks * block_size;
   const int kv_box = packed_tiles ? 128 : (block_size < 128 ? block_size : 128);
   // [rows, heads, dim] bf16, boxes of 64 elements x 1 head x box rows, 128-byte swizzle
-  if (!make_tmap_3d(&mq, q, 2, total_q, num_heads, head_dim, 64, 128, 128) ||
-      !make_tmap_3d(&mk, kt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128) ||
-      !make_tmap_3d(&mv, vt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128))
+  // (not needed when every query row goes to the decode kernels)
+  if (!all_routed && (!make_tmap_3d(&mq, q, 2, total_q, num_heads, head_dim, 64, 128, 128) ||
+                      !make_tmap_3d(&mk, kt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128) ||
+                      !make_tmap_3d(&mv, vt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128)))
     return PKV_ERR_CUDA;
 
   PrefillParams p{};
@@ -1232,6 +1250,9 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.lse = lse;
   p.err = err_flag;
+#ifdef PKV_TEST_HOOKS
+  p.test_skip_k = g_test_skip_k;
+#endif
   cudaStream_t st = as_stream(stream);
   int32_t* count = nullptr;
   int32_t* items = nullptr;
@@ -1258,8 +1279,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
     gk_kern<<<ggrid, 256, 0, st>>>(kc, vc, cu_seqlens_q, cu_seqlens_k, cu_g, block_table, max_blocks_per_seq,
                                    block_size, num_blocks, row_elems, rmq, total_k, gk, gv, err_flag);
   }
-  int rc;
-  if (head_dim == 128)
+  int rc = PKV_OK;
+  if (all_routed)
+    rc = launch_status();
+  else if (head_dim == 128)
     rc = packed_tiles ? launch_prefill<128, false>(mq, mk, mv, p, batch, st)
                       : launch_prefill<128, true>(mq, mk, mv, p, batch, st);
   else
@@ -1273,3 +1296,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
                               scale, kv_dtype, k_scale, v_scale, out, lse, wsb + wl.decode_off,
                               (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, st);
 }
+
+#ifdef PKV_TEST_HOOKS
+// Test builds only: the next varlen calls withhold, in CTA 0 of the prefill
+// kernel, the copy of its `tile`-th K tile, so that the waits on it run out
+// (-1 restores normal operation).
+extern "C" PKV_API void pkv_test_prefill_skip_k(int tile) { pkv::g_test_skip_k = tile; }
+#endif

@@ -134,10 +134,20 @@ def _require_cuda(*ts):
 _workspaces = {}
 
 
-def workspace(nbytes: int, device) -> torch.Tensor:
-    """A cached per-device scratch buffer of at least ``nbytes`` (grows, never shrinks)."""
+def workspace(nbytes: int, device, stream=None) -> torch.Tensor:
+    """A cached scratch buffer of at least ``nbytes`` (grows, never shrinks), one per
+    (device, stream).
+
+    Calls on one stream run in order, so they can share a buffer; calls on two
+    streams may overlap on the GPU and get separate buffers (the varlen call also
+    keeps its work counter in there).  A caller that passes ``workspace_buf``
+    itself must not share one buffer between calls that can overlap.
+    """
     dev = torch.device(device)
-    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    index = dev.index if dev.index is not None else torch.cuda.current_device()
+    if stream is None:
+        stream = torch.cuda.current_stream(index)
+    key = (index, int(stream.cuda_stream))
     buf = _workspaces.get(key)
     if buf is None or buf.numel() < nbytes:
         buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
@@ -240,7 +250,7 @@ def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale: fl
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     L = lib()
     need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
-    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device) if need else None)
+    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device, stream) if need else None)
     st = L.pkv_paged_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _cache_dtype(k_cache),
                                  _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB,
                                  int(max_seqlen_k), float(scale), float(k_scale), float(v_scale), _ptr(out),
@@ -287,7 +297,7 @@ def paged_attn_decode_with_kvcache(q, k_new, v_new, k_cache, v_cache, cache_seql
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     L = lib()
     need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
-    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device) if need else None)
+    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device, stream) if need else None)
     st = L.pkv_paged_attn_decode_with_kvcache(
         _ptr(q), _ptr(k_new), k_new.stride(0), _ptr(v_new), v_new.stride(0), _ptr(k_cache), _ptr(v_cache),
         _cache_dtype(k_cache), _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB, int(max_seqlen_k),
@@ -341,8 +351,10 @@ def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_l
     Paged mode: ``gather_k_tokens`` (a host bound on the summed keys of the
     sequences the prefill tiles serve) lets the library gather their K/V into
     a packed bf16 buffer first, which blocks under 64 tokens and one-byte
-    caches (uint8 E4M3 or int8 codes, value = code * k_scale / v_scale) use;
-    one-byte caches need it.
+    caches (uint8 E4M3 or int8 codes, value = code * k_scale / v_scale) use.
+    A one-byte cache needs it unless no sequence has more than 8 queries (then
+    every query row runs on the decode kernels).  Without ``workspace_buf`` the
+    scratch comes from a buffer cached per (device, stream).
     """
     _require_cuda(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table)
     T, Hq, D = q.shape
@@ -372,7 +384,7 @@ def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_l
     paged = 1 if block_table is not None else 0
     need = L.pkv_paged_attn_varlen_workspace(B, T, total_k, Hq, Hkv, D, int(max_len_q), int(max_len_k), paged,
                                              _cache_dtype(k), bs)
-    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device) if need else None)
+    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device, stream) if need else None)
     st = L.pkv_paged_attn_varlen(_ptr(q), _ptr(k), _ptr(v), _cache_dtype(k), _ptr(cu_seqlens_q),
                                  _ptr(cu_seqlens_k), B, T, total_k, int(max_len_q), int(max_len_k),
                                  _ptr(block_table), MB, bs, NB, Hq, Hkv, D, float(scale), 1 if causal else 0,

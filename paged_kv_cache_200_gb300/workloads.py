@@ -2,8 +2,12 @@
 
 This module only draws inputs: sequence lengths, block pools, block tables,
 the scheduler's slot mapping and cumulative lengths, and N(0,1) bf16 values.
-It holds none of the attention or quantisation arithmetic; both the CUDA path
-and the CPU oracle receive the same tensors from here.
+It holds no attention arithmetic.  The one piece of quantisation here lays
+down the pre-existing history of a one-byte cache (``fp8_codes_via_torch``,
+``int8_codes_via_torch``) with torch's own conversions, as input preparation:
+the oracle dequantises whatever codes it is given, and the rows the library
+writes are checked against the oracle's own quantiser.  Both the CUDA path and
+the CPU oracle receive the same tensors from here.
 
 Lengths and block permutations come from ``numpy.random.default_rng(seed)``
 (integers uniform, inclusive bounds).  Values are drawn as float32 N(0,1) by a

@@ -1,22 +1,34 @@
-"""The decode entry point that allocates nothing, against the workspace entry point.
+"""The decode entry point that allocates nothing, against the workspace entry point and the oracle.
 
-For callers that cannot allocate device memory (an engine that owns all of
-it, or a loop that must not synchronise on cudaMalloc), the library offers a
-decode call whose split-KV partials live in a fixed device array.  These
-tests call it directly through the C ABI and compare it with the regular
-entry point on consecutive calls, and check that a request too large for the
-fixed array is refused before anything runs.  This file is collected last.
+Some callers cannot allocate device memory: an engine that has reserved all of
+it for its own pool, or a loop that must not take cudaMalloc's implicit device
+synchronisation.  For them the library offers a decode call whose split-KV
+partials live in a fixed device array inside the library.  These tests call it
+directly through the C ABI on several calls in a row (bf16, FP8 and INT8 caches,
+and a later call whose split plan is longer than the earlier ones, so stale
+partials left in the shared array must never be read) and check that
+
+* its output and lse are bit for bit those of the regular entry point, which
+  runs the same kernels on the same split plan with a caller workspace;
+* both are within the parity tolerance of the fp64 oracle;
+* a request too large for the fixed array is refused before anything runs.
+
+This file is collected last.
 """
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from paged_kv_cache_200_gb300 import workloads as W
-from _helpers import BF16_ATOL, BF16_RTOL, FP8_ATOL, FP8_RTOL, assert_close, built_library, f64
+from _helpers import BF16_ATOL, BF16_RTOL, FP8_ATOL, FP8_RTOL, assert_close, bits, built_library, f64
 
 pytestmark = pytest.mark.gpu
+
+_DTYPE_CODE = {"bf16": 0, "fp8_e4m3": 2, "int8": 3}
 
 
 def _c_noalloc(lib, wl, out, lse):
@@ -24,20 +36,30 @@ def _c_noalloc(lib, wl, out, lse):
     kc, vc = wl.k_cache.view(shape4), wl.v_cache.view(shape4)
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     return lib.pkv_paged_attn_decode_noalloc(
-        p(wl.q), p(kc), p(vc), 2 if wl.cache_dtype == "fp8_e4m3" else 0, p(wl.cache_seqlens), p(wl.block_table),
+        p(wl.q), p(kc), p(vc), _DTYPE_CODE[wl.cache_dtype], p(wl.cache_seqlens), p(wl.block_table),
         wl.block_table.shape[1], wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
         wl.num_blocks, wl.max_seqlen, wl.scale, wl.k_scale, wl.v_scale, p(out), p(lse), None,
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
+def _partials_per_row(lib, wl):
+    """Workspace bytes of the call's split plan per (sequence, query head): grows with its split count."""
+    need = lib.pkv_paged_attn_decode_workspace(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.max_seqlen)
+    return need / (wl.batch * wl.num_heads)
+
+
+def test_noalloc_decode_is_the_workspace_decode_on_consecutive_calls():
     pkv = built_library()
     lib = pkv.lib()
     cases = [
         W.make_decode([3000, 17, 9000, 512], 32, 8, 128, 16, seed=101, device="cuda"),            # several splits
         W.make_decode([40, 2500, 700], 16, 4, 64, 32, seed=102, device="cuda", cache_dtype="fp8_e4m3"),
-        W.make_decode([3000, 17, 9000, 512], 32, 8, 128, 16, seed=101, device="cuda"),            # again
+        W.make_decode([5000, 600, 3100], 32, 8, 128, 16, seed=103, device="cuda", cache_dtype="int8"),
+        # few sequences, one long: more splits per (sequence, head) than every call above
+        W.make_decode([30000, 100], 32, 8, 128, 16, seed=104, device="cuda"),
+        W.make_decode([3000, 17, 9000, 512], 32, 8, 128, 16, seed=101, device="cuda"),            # the first again
     ]
+    assert _partials_per_row(lib, cases[3]) > max(_partials_per_row(lib, c) for c in cases[:3])
     for wl in cases:
         shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
         ref, ref_lse = pkv.paged_attn_decode(wl.q, wl.k_cache.view(shape4), wl.v_cache.view(shape4),
@@ -48,9 +70,16 @@ def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
         lse = torch.full_like(ref_lse, float("nan"))
         assert _c_noalloc(lib, wl, out, lse) == 0
         torch.cuda.synchronize()
-        atol, rtol = (FP8_ATOL, FP8_RTOL) if wl.cache_dtype == "fp8_e4m3" else (BF16_ATOL, BF16_RTOL)
-        assert_close(f64(out), f64(ref), atol, rtol, "noalloc out")
-        assert_close(f64(lse), f64(ref_lse), 1e-3, 1e-3, "noalloc lse")
+        # same kernels, same split plan: identical bits
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"{wl.cache_dtype}: out differs"
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), f"{wl.cache_dtype}: lse differs"
+        # and both match the oracle
+        oref, oref_lse = O.paged_attn_decode(bits(wl.q), bits(wl.k_cache), bits(wl.v_cache),
+                                             wl.cache_seqlens.cpu().numpy(), wl.block_table.cpu().numpy(),
+                                             wl.block_size, wl.scale, wl.cache_dtype, wl.k_scale, wl.v_scale)
+        atol, rtol = (FP8_ATOL, FP8_RTOL) if wl.cache_dtype != "bf16" else (BF16_ATOL, BF16_RTOL)
+        assert_close(f64(out), oref, atol, rtol, f"noalloc {wl.cache_dtype} out")
+        assert_close(f64(lse), oref_lse, 1e-3, 1e-3, f"noalloc {wl.cache_dtype} lse")
 
 
 def test_noalloc_rejects_requests_beyond_its_fixed_scratch():
