@@ -621,8 +621,9 @@ def multi_query_workload(pkv, W, device, pk, args):
     once = int(wl.k_lens.sum()) * row            # each sequence's K/V read once
     per_query = int(sum(int(lk) - 4 + i + 1 for lk in wl.k_lens for i in range(4))) * row  # what the rows read
     res = {"multi_query_decode": {
-        "workload": "64 seqs x 4 new tokens over U[1024,16384] cached tokens, 32 q / 8 kv, d128, bs16; every query "
-                    "row served by the split-KV decode kernels (one varlen call)", "ms": ms,
+        "workload": "64 seqs x 4 new tokens over U[1024,16384] cached tokens, 32 q / 8 kv, d128, bs16; each "
+                    "sequence's 4 x 4 (query, head) rows in one split-KV decode pass, K/V read once (one varlen "
+                    "call)", "ms": ms,
         "GB_per_s": once / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": once / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
         "GB_per_s_incl_L2_rereads": per_query / (ms * 1e-3) / 1e9,
         "kv_bytes_once": once, "kv_bytes_read_per_query_rows": per_query, "tokens_per_s": wl.total_q / (ms * 1e-3),

@@ -86,6 +86,9 @@ struct DecodeParams {
   const int32_t* cu_k;
   int64_t lse_head_stride;
   int64_t lse_row_stride;
+  // Multi-query items (varlen routing): 0, or the bound on queries per item;
+  // then items[z] is a sequence and its (query, head) rows fill the N side.
+  int32_t multi_q;
   // Append (decode with an in-place cache update): seqlens hold the lengths
   // before this step's token, which takes position seqlens[b]; its K/V rows
   // (k_new/v_new row b, quantised for an FP8 cache) are stored there by the
@@ -160,8 +163,13 @@ struct TileLayout {
 };
 
 // kFp8: one-byte codes (E4M3, or INT8 when kInt8) widened to f16 for f16 MMAs.
-template <int D, bool kFp8, int kStages, bool kInt8 = false>
-__global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResidentBf16)
+// kNB: blocks of 8 rows on the MMAs' N side.  A row is a query head of the
+// GQA group (plain decode: kNB = 1) or, for multi-query items (p.multi_q > 0),
+// a (query, head) pair of the sequence: row r is query r / group, head
+// r % group, and sees the positions up to its own bottom-right causal limit.
+// Two row blocks need more registers: those kernels run 2 CTAs per SM.
+template <int D, bool kFp8, int kStages, bool kInt8 = false, int kNB = 1>
+__global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded : kResidentBf16)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                               const DecodeParams p) {
   constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one position, one kv head
@@ -170,6 +178,7 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   constexpr int kStageBytes = 2 * kTileBytes;     // K then V
   constexpr int kWarpBytes = kStages * kStageBytes;
   constexpr int kDT = D / 16;
+  constexpr int kRows = 8 * kNB;                  // rows served by this CTA (at most)
   constexpr int kBoxElems = TL::kBoxRow / (kFp8 ? 1 : 2);
   // two one-byte codes (bytes 0..1, resp. 2..3, of a word) -> f16x2, exactly
   auto code_lo = [](uint32_t w) { return kInt8 ? int8x2_lo_to_f16x2(w) : e4m3x2_lo_to_f16x2(w); };
@@ -188,9 +197,13 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   int qi;
   const int b = item_sequence(p, z, qi);
   if (b < 0) return;
-  const int64_t qrow_idx = item_row(p, b, qi);
+  // multi-query item: the sequence's lq queries, each with its own limit
+  const int lq = p.multi_q ? __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b) : 1;
+  if (lq <= 0) return;
+  const int64_t qrow_idx = item_row(p, b, qi);  // the item's first query row
 
-  const int len = attended_length(p, b, qi, split == 0 && kvh == 0 && threadIdx.x == 0);
+  // the CTA's positions: those of its last query (the whole prefix)
+  const int len = attended_length(p, b, p.multi_q ? lq - 1 : qi, split == 0 && kvh == 0 && threadIdx.x == 0);
   const int n_splits = (len + p.split_tokens - 1) / p.split_tokens;
   if (split >= (n_splits > 0 ? n_splits : 1)) return;
   const int t_begin = split * p.split_tokens;
@@ -201,6 +214,7 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   const int n_groups = t_end > t_begin ? (t_end - t_begin + kGroupTok - 1) / kGroupTok : 0;
   const int my_groups = n_groups > warp ? (n_groups - warp + kDecWarps - 1) / kDecWarps : 0;
   const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
+  const int n_rows = p.multi_q ? lq * p.group : p.group;  // rows of this item (<= kRows)
 
   uint8_t* wsm = smem + warp * kWarpBytes;
   const uint32_t wsm_u32 = smem_u32(wsm);
@@ -212,26 +226,40 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   }
   __syncwarp();
 
-  // ---- Q as the B operand (n = head lane/4 of this group, k = head dim) ----
-  uint32_t qf[kDT][2];
-  {
-    const int h = lane >> 2;
+  // ---- Q as the B operand (n = row lane/4 of each block, k = head dim) ----
+  uint32_t qf[kNB][kDT][2];
+  // positions this thread's rows see: rows 2j and 2j+1 of each block (masks of the S^T fragments)
+  int lim_a[kNB], lim_b[kNB];
+#pragma unroll
+  for (int bk = 0; bk < kNB; ++bk) {
+    const int r = bk * 8 + (lane >> 2);
     const int j = lane & 3;
-    const bool hv = h < p.group;
-    const uint16_t* qrow = p.q + (qrow_idx * p.num_heads + (int64_t)kvh * p.group + (hv ? h : 0)) * D;
+    const int qr = p.multi_q ? r / p.group : 0;
+    const int hh = p.multi_q ? r % p.group : r;
+    const bool hv = r < n_rows;
+    const uint16_t* qrow =
+        p.q + ((qrow_idx + (hv ? qr : 0)) * p.num_heads + (int64_t)kvh * p.group + (hv ? hh : 0)) * D;
 #pragma unroll
     for (int kk = 0; kk < kDT; ++kk) {
       if constexpr (!kFp8) {
-        qf[kk][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * j) : 0u;
-        qf[kk][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * j) : 0u;
+        qf[bk][kk][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * j) : 0u;
+        qf[bk][kk][1] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * j) : 0u;
       } else {
         // FP8 K fragments carry head dims 4j..4j+3 of each 16-wide slice in
         // k-slots {2j,2j+1,2j+8,2j+9}; Q uses the same permutation.
         const uint2 w = hv ? *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * j) : make_uint2(0u, 0u);
-        qf[kk][0] = w.x;
-        qf[kk][1] = w.y;
+        qf[bk][kk][0] = w.x;
+        qf[bk][kk][1] = w.y;
       }
     }
+    // row (query qr) sees positions < len - (lq - 1 - qr); rows past the item see none
+    auto row_lim = [&](int rr) {
+      if (rr >= n_rows) return 0;
+      const int q_of = p.multi_q ? rr / p.group : 0;
+      return len - (lq - 1 - q_of);
+    };
+    lim_a[bk] = min(t_end, row_lim(bk * 8 + 2 * j));
+    lim_b[bk] = min(t_end, row_lim(bk * 8 + 2 * j + 1));
   }
   // FP8 cache: the MMAs run in f16 (E4M3 widens to f16 exactly).  Q goes from
   // bf16 to f16 scaled by a power of two 2^-e chosen so that its largest
@@ -240,12 +268,14 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   if constexpr (kFp8) {
     float qmax = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < kDT; ++kk)
+    for (int bk = 0; bk < kNB; ++bk)
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        qmax = fmaxf(qmax, fabsf(__uint_as_float(qf[kk][h2] << 16)));
-        qmax = fmaxf(qmax, fabsf(__uint_as_float(qf[kk][h2] & 0xFFFF0000u)));
-      }
+      for (int kk = 0; kk < kDT; ++kk)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          qmax = fmaxf(qmax, fabsf(__uint_as_float(qf[bk][kk][h2] << 16)));
+          qmax = fmaxf(qmax, fabsf(__uint_as_float(qf[bk][kk][h2] & 0xFFFF0000u)));
+        }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
     int e = 0;
@@ -253,11 +283,13 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
     const float qs = exp2f((float)-e);
     scale_log2 *= exp2f((float)e);
 #pragma unroll
-    for (int kk = 0; kk < kDT; ++kk)
+    for (int bk = 0; bk < kNB; ++bk)
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2)
-        qf[kk][h2] = pack_f16x2(__uint_as_float(qf[kk][h2] << 16) * qs,
-                                __uint_as_float(qf[kk][h2] & 0xFFFF0000u) * qs);
+      for (int kk = 0; kk < kDT; ++kk)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+          qf[bk][kk][h2] = pack_f16x2(__uint_as_float(qf[bk][kk][h2] << 16) * qs,
+                                      __uint_as_float(qf[bk][kk][h2] & 0xFFFF0000u) * qs);
   }
 
   auto block_of = [&](int pos0, bool report) -> int {
@@ -299,10 +331,15 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
     }
   };
 
-  float o[kDT][4];
+  float o[kNB][kDT][4];
+  float m0[kNB], m1[kNB], l0[kNB], l1[kNB];
 #pragma unroll
-  for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  for (int bk = 0; bk < kNB; ++bk) {
+#pragma unroll
+    for (int t = 0; t < kDT; ++t) o[bk][t][0] = o[bk][t][1] = o[bk][t][2] = o[bk][t][3] = 0.f;
+    m0[bk] = m1[bk] = -INFINITY;
+    l0[bk] = l1[bk] = 0.f;
+  }
 
   // Append: the warp whose copies read the new position stores its K/V rows
   // for this kv head first (a generic write, then a proxy fence so the TMA
@@ -360,10 +397,13 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
     }
 
     if (blk_ok) {
-      // ---- S^T = K Q^T (16 positions x 8 heads) ----
+      // ---- S^T = K Q^T (16 positions x 8 rows per block) ----
       // two independent accumulator chains (even / odd 16-wide slices of the head dim)
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      float s2[4] = {0.f, 0.f, 0.f, 0.f};
+      float s[kNB][4], s2[kNB][4];
+#pragma unroll
+      for (int bk = 0; bk < kNB; ++bk)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[bk][e] = s2[bk][e] = 0.f;
       {
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int csel = lane >> 4;
@@ -372,68 +412,77 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
           for (int kk = 0; kk < kDT; ++kk) {
             uint32_t a0, a1, a2, a3;
             ldmatrix_x4(ks + TL::offset(row, 2 * kk + csel), a0, a1, a2, a3);
-            mma_bf16_16816((kk & 1) ? s2 : s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+#pragma unroll
+            for (int bk = 0; bk < kNB; ++bk)
+              mma_bf16_16816((kk & 1) ? s2[bk] : s[bk], a0, a1, a2, a3, qf[bk][kk][0], qf[bk][kk][1]);
           }
         } else {
 #pragma unroll
           for (int pp = 0; pp < kDT / 2; ++pp) {
             uint32_t r0, r1, r2, r3;
             ldmatrix_x4(ks + TL::offset(row, 2 * pp + csel), r0, r1, r2, r3);
-            mma_f16_16816(s, code_lo(r0), code_lo(r1), code_hi(r0),
-                          code_hi(r1), qf[2 * pp][0], qf[2 * pp][1]);
-            mma_f16_16816(s2, code_lo(r2), code_lo(r3), code_hi(r2),
-                          code_hi(r3), qf[2 * pp + 1][0], qf[2 * pp + 1][1]);
+            const uint32_t e0 = code_lo(r0), e1 = code_lo(r1), e2 = code_hi(r0), e3 = code_hi(r1);
+            const uint32_t f0 = code_lo(r2), f1 = code_lo(r3), f2 = code_hi(r2), f3 = code_hi(r3);
+#pragma unroll
+            for (int bk = 0; bk < kNB; ++bk) {
+              mma_f16_16816(s[bk], e0, e1, e2, e3, qf[bk][2 * pp][0], qf[bk][2 * pp][1]);
+              mma_f16_16816(s2[bk], f0, f1, f2, f3, qf[bk][2 * pp + 1][0], qf[bk][2 * pp + 1][1]);
+            }
           }
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s[e] += s2[e];
+        for (int bk = 0; bk < kNB; ++bk)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[bk][e] += s2[bk][e];
       }
 
-      // ---- online softmax (log2 domain); this thread: positions lane/4 (+8), heads 2j, 2j+1 ----
+      // ---- online softmax (log2 domain); this thread: positions lane/4 (+8), rows 2j, 2j+1 ----
       // The reference max m moves only when the tile max exceeds it by more
       // than 2^8, so O is rescaled rarely; P stays below 2^8.
       const int tok0 = pos0 + (lane >> 2);
-      const bool v0 = tok0 < t_end;
-      const bool v1 = tok0 + 8 < t_end;
-      const float x0 = v0 ? s[0] * scale_log2 : -INFINITY;
-      const float x1 = v0 ? s[1] * scale_log2 : -INFINITY;
-      const float x2 = v1 ? s[2] * scale_log2 : -INFINITY;
-      const float x3 = v1 ? s[3] * scale_log2 : -INFINITY;
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      uint32_t pb0[kNB], pb1[kNB];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mu0 = (mx0 > m0 + 8.f || (m0 == -INFINITY && mx0 != -INFINITY)) ? mx0 : m0;
-      const float mu1 = (mx1 > m1 + 8.f || (m1 == -INFINITY && mx1 != -INFINITY)) ? mx1 : m1;
-      const bool live0 = mu0 != -INFINITY, live1 = mu1 != -INFINITY;
-      const float p0 = live0 ? fast_exp2(x0 - mu0) : 0.f;
-      const float p1 = live1 ? fast_exp2(x1 - mu1) : 0.f;
-      const float p2 = live0 ? fast_exp2(x2 - mu0) : 0.f;
-      const float p3 = live1 ? fast_exp2(x3 - mu1) : 0.f;
-      if (__any_sync(0xffffffffu, (mu0 != m0 && m0 != -INFINITY) || (mu1 != m1 && m1 != -INFINITY))) {
-        const float al0 = (mu0 != m0 && m0 != -INFINITY) ? fast_exp2(m0 - mu0) : 1.f;
-        const float al1 = (mu1 != m1 && m1 != -INFINITY) ? fast_exp2(m1 - mu1) : 1.f;
-        l0 *= al0;
-        l1 *= al1;
+      for (int bk = 0; bk < kNB; ++bk) {
+        const float x0 = tok0 < lim_a[bk] ? s[bk][0] * scale_log2 : -INFINITY;
+        const float x1 = tok0 < lim_b[bk] ? s[bk][1] * scale_log2 : -INFINITY;
+        const float x2 = tok0 + 8 < lim_a[bk] ? s[bk][2] * scale_log2 : -INFINITY;
+        const float x3 = tok0 + 8 < lim_b[bk] ? s[bk][3] * scale_log2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-        for (int t = 0; t < kDT; ++t) {
-          o[t][0] *= al0;
-          o[t][1] *= al1;
-          o[t][2] *= al0;
-          o[t][3] *= al1;
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
+        const float mu0 = (mx0 > m0[bk] + 8.f || (m0[bk] == -INFINITY && mx0 != -INFINITY)) ? mx0 : m0[bk];
+        const float mu1 = (mx1 > m1[bk] + 8.f || (m1[bk] == -INFINITY && mx1 != -INFINITY)) ? mx1 : m1[bk];
+        const bool live0 = mu0 != -INFINITY, live1 = mu1 != -INFINITY;
+        const float p0 = live0 ? fast_exp2(x0 - mu0) : 0.f;
+        const float p1 = live1 ? fast_exp2(x1 - mu1) : 0.f;
+        const float p2 = live0 ? fast_exp2(x2 - mu0) : 0.f;
+        const float p3 = live1 ? fast_exp2(x3 - mu1) : 0.f;
+        if (__any_sync(0xffffffffu, (mu0 != m0[bk] && m0[bk] != -INFINITY) || (mu1 != m1[bk] && m1[bk] != -INFINITY))) {
+          const float al0 = (mu0 != m0[bk] && m0[bk] != -INFINITY) ? fast_exp2(m0[bk] - mu0) : 1.f;
+          const float al1 = (mu1 != m1[bk] && m1[bk] != -INFINITY) ? fast_exp2(m1[bk] - mu1) : 1.f;
+          l0[bk] *= al0;
+          l1[bk] *= al1;
+#pragma unroll
+          for (int t = 0; t < kDT; ++t) {
+            o[bk][t][0] *= al0;
+            o[bk][t][1] *= al1;
+            o[bk][t][2] *= al0;
+            o[bk][t][3] *= al1;
+          }
+        }
+        m0[bk] = mu0;
+        m1[bk] = mu1;
+        l0[bk] += p0 + p2;
+        l1[bk] += p1 + p3;
+        // P as the B operand (k = position, n = row): positions 0..7, then 8..15
+        pb0[bk] = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+        pb1[bk] = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
       }
-      m0 = mu0;
-      m1 = mu1;
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-      // P as the B operand (k = position, n = head): positions 0..7, then 8..15
-      const uint32_t pb0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
 
-      // ---- O^T += V^T P^T ----
+      // ---- O^T += V^T P^T (V fragments shared by the row blocks) ----
       {
         const int row = (lane & 7) + (lane >> 4) * 8;
         const int csel = (lane >> 3) & 1;
@@ -442,7 +491,8 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
           for (int t = 0; t < kDT; ++t) {
             uint32_t a0, a1, a2, a3;
             ldmatrix_x4_trans(vs + TL::offset(row, 2 * t + csel), a0, a1, a2, a3);
-            mma_bf16_16816(o[t], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+            for (int bk = 0; bk < kNB; ++bk) mma_bf16_16816(o[bk][t], a0, a1, a2, a3, pb0[bk], pb1[bk]);
           }
         } else {
 #pragma unroll
@@ -452,16 +502,22 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
             // r: bytes (pos 2j, dim 2u), (2j, 2u+1), (2j+1, 2u), (2j+1, 2u+1); widen
             // bytes {0, 2} (even dim, both positions), then {1, 3} (odd dim).  INT8
             // picks them in its widening permute; E4M3 reorders the word first.
+            uint32_t ev[4], od[4];
             if constexpr (kInt8) {
-              mma_f16_16816(o[2 * pp], int8x2_even_to_f16x2(r0), int8x2_even_to_f16x2(r1),
-                            int8x2_even_to_f16x2(r2), int8x2_even_to_f16x2(r3), pb0, pb1);
-              mma_f16_16816(o[2 * pp + 1], int8x2_odd_to_f16x2(r0), int8x2_odd_to_f16x2(r1),
-                            int8x2_odd_to_f16x2(r2), int8x2_odd_to_f16x2(r3), pb0, pb1);
+              ev[0] = int8x2_even_to_f16x2(r0); ev[1] = int8x2_even_to_f16x2(r1);
+              ev[2] = int8x2_even_to_f16x2(r2); ev[3] = int8x2_even_to_f16x2(r3);
+              od[0] = int8x2_odd_to_f16x2(r0); od[1] = int8x2_odd_to_f16x2(r1);
+              od[2] = int8x2_odd_to_f16x2(r2); od[3] = int8x2_odd_to_f16x2(r3);
             } else {
               const uint32_t t0 = prmt(r0, 0u, 0x3120u), t1 = prmt(r1, 0u, 0x3120u);
               const uint32_t t2 = prmt(r2, 0u, 0x3120u), t3 = prmt(r3, 0u, 0x3120u);
-              mma_f16_16816(o[2 * pp], code_lo(t0), code_lo(t1), code_lo(t2), code_lo(t3), pb0, pb1);
-              mma_f16_16816(o[2 * pp + 1], code_hi(t0), code_hi(t1), code_hi(t2), code_hi(t3), pb0, pb1);
+              ev[0] = code_lo(t0); ev[1] = code_lo(t1); ev[2] = code_lo(t2); ev[3] = code_lo(t3);
+              od[0] = code_hi(t0); od[1] = code_hi(t1); od[2] = code_hi(t2); od[3] = code_hi(t3);
+            }
+#pragma unroll
+            for (int bk = 0; bk < kNB; ++bk) {
+              mma_f16_16816(o[bk][2 * pp], ev[0], ev[1], ev[2], ev[3], pb0[bk], pb1[bk]);
+              mma_f16_16816(o[bk][2 * pp + 1], od[0], od[1], od[2], od[3], pb0[bk], pb1[bk]);
             }
           }
         }
@@ -480,67 +536,75 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
 
   // ---- merge the four warps of the CTA ----
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  __syncthreads();
-  float* m_s = reinterpret_cast<float*>(smem);           // [warps][8]
-  float* l_s = m_s + kDecWarps * kMaxGroup;               // [warps][8]
-  float* o_s = l_s + kDecWarps * kMaxGroup;               // [warps][8][D]
+  for (int bk = 0; bk < kNB; ++bk)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0[bk] += __shfl_xor_sync(0xffffffffu, l0[bk], off);
+      l1[bk] += __shfl_xor_sync(0xffffffffu, l1[bk], off);
+    }
+  float* m_s = reinterpret_cast<float*>(smem);           // [warps][rows]
+  float* l_s = m_s + kDecWarps * kRows;                   // [warps][rows]
+  float* o_s = l_s + kDecWarps * kRows;                   // [warps][rows][D]
   {
     const int j = lane & 3;
-    if (lane < 4) {
-      m_s[warp * kMaxGroup + 2 * j] = m0;
-      m_s[warp * kMaxGroup + 2 * j + 1] = m1;
-      l_s[warp * kMaxGroup + 2 * j] = l0;
-      l_s[warp * kMaxGroup + 2 * j + 1] = l1;
-    }
-    float* ow = o_s + warp * kMaxGroup * D;
     const int r = lane >> 2;
 #pragma unroll
-    for (int t = 0; t < kDT; ++t) {
-      int d0, d1;
-      if constexpr (!kFp8) {
-        d0 = 16 * t + r;
-        d1 = d0 + 8;
-      } else {
-        d0 = 32 * (t >> 1) + 2 * r + (t & 1);
-        d1 = d0 + 16;
+    for (int bk = 0; bk < kNB; ++bk) {
+      if (lane < 4) {
+        m_s[warp * kRows + bk * 8 + 2 * j] = m0[bk];
+        m_s[warp * kRows + bk * 8 + 2 * j + 1] = m1[bk];
+        l_s[warp * kRows + bk * 8 + 2 * j] = l0[bk];
+        l_s[warp * kRows + bk * 8 + 2 * j + 1] = l1[bk];
       }
-      ow[(2 * j) * D + d0] = o[t][0];
-      ow[(2 * j + 1) * D + d0] = o[t][1];
-      ow[(2 * j) * D + d1] = o[t][2];
-      ow[(2 * j + 1) * D + d1] = o[t][3];
+      float* ow = o_s + (warp * kRows + bk * 8) * D;
+#pragma unroll
+      for (int t = 0; t < kDT; ++t) {
+        int d0, d1;
+        if constexpr (!kFp8) {
+          d0 = 16 * t + r;
+          d1 = d0 + 8;
+        } else {
+          d0 = 32 * (t >> 1) + 2 * r + (t & 1);
+          d1 = d0 + 16;
+        }
+        ow[(2 * j) * D + d0] = o[bk][t][0];
+        ow[(2 * j + 1) * D + d0] = o[bk][t][1];
+        ow[(2 * j) * D + d1] = o[bk][t][2];
+        ow[(2 * j + 1) * D + d1] = o[bk][t][3];
+      }
     }
   }
   __syncthreads();
   const bool single = n_splits <= 1;
-  for (int idx = threadIdx.x; idx < p.group * D; idx += kDecThreads) {
-    const int h = idx / D;
+  const int qpi = p.multi_q ? p.multi_q : 1;  // query rows per item in the partials
+  for (int idx = threadIdx.x; idx < n_rows * D; idx += kDecThreads) {
+    const int r = idx / D;
     const int d = idx % D;
     float ms = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) ms = fmaxf(ms, m_s[w * kMaxGroup + h]);
+    for (int w = 0; w < kDecWarps; ++w) ms = fmaxf(ms, m_s[w * kRows + r]);
     float L = 0.f, acc = 0.f;
     if (ms != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) {
-        const float mw = m_s[w * kMaxGroup + h];
+        const float mw = m_s[w * kRows + r];
         const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - ms);
-        L += l_s[w * kMaxGroup + h] * f;
-        acc += o_s[(w * kMaxGroup + h) * D + d] * f;
+        L += l_s[w * kRows + r] * f;
+        acc += o_s[(w * kRows + r) * D + d] * f;
       }
     }
     const bool any = L > 0.f;
     const float val = any ? acc * p.v_mul / L : 0.f;
     const float lse2 = any ? ms + log2f(L) : -INFINITY;
-    const int hq = kvh * p.group + h;
-    const int64_t bh = (int64_t)z * p.num_heads + hq;  // partials are indexed by grid item
+    const int qr = p.multi_q ? r / p.group : 0;
+    const int hq = kvh * p.group + (p.multi_q ? r % p.group : r);
+    const int64_t orow = qrow_idx + qr;
+    // partials are indexed by grid item, query of the item and head
+    const int64_t bh = ((int64_t)z * qpi + qr) * p.num_heads + hq;
     if (single) {
-      p.out[(qrow_idx * p.num_heads + hq) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+      p.out[(orow * p.num_heads + hq) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
       if (p.lse != nullptr && d == 0)
-        p.lse[hq * p.lse_head_stride + qrow_idx * p.lse_row_stride] = any ? lse2 * kLn2 : -INFINITY;
+        p.lse[hq * p.lse_head_stride + orow * p.lse_row_stride] = any ? lse2 * kLn2 : -INFINITY;
     } else {
       p.ws_o[(bh * p.max_splits + split) * D + d] = val;
       if (d == 0) p.ws_lse[bh * p.max_splits + split] = lse2;
@@ -548,7 +612,7 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 ? kResidentCoded : kResident
   }
 }
 
-// One warp per (sequence, query head): merge the splits by log-sum-exp.
+// One warp per (item, query of the item, query head): merge the splits by log-sum-exp.
 template <int D>
 __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p, int batch) {
   // launched as a programmatic dependent of the split kernel: wait until that
@@ -556,15 +620,20 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int qpi = p.multi_q ? p.multi_q : 1;
   const int64_t bh = (int64_t)blockIdx.x * 4 + warp;
-  if (bh >= (int64_t)batch * p.num_heads) return;
-  const int z = (int)(bh / p.num_heads);
+  if (bh >= (int64_t)batch * qpi * p.num_heads) return;
+  const int z = (int)(bh / ((int64_t)qpi * p.num_heads));
+  const int qr = (int)((bh / p.num_heads) % qpi);
   const int hq = (int)(bh % p.num_heads);
   int qi;
   const int b = item_sequence(p, z, qi);
   if (b < 0) return;
-  const int64_t row = item_row(p, b, qi);
-  const int len = attended_length(p, b, qi, false);
+  const int lq = p.multi_q ? __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b) : 1;
+  if (qr >= lq) return;
+  const int64_t row = item_row(p, b, qi) + qr;
+  // the split kernel's CTAs cover the positions of the item's last query
+  const int len = attended_length(p, b, p.multi_q ? lq - 1 : qi, false);
   const int n = (len + p.split_tokens - 1) / p.split_tokens;
   if (n <= 1) return;
   const float* ls = p.ws_lse + bh * p.max_splits;
@@ -673,20 +742,21 @@ SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, i
   return pl;
 }
 
-template <int D, bool kFp8, bool kInt8 = false>
+template <int D, bool kFp8, bool kInt8 = false, int kNB = 1>
 int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t num_slots, cudaStream_t st) {
   constexpr int kStages = 3;  // shared memory for kResidentCoded (one-byte codes) or kResidentBf16 CTAs per SM
   constexpr int kRowBytes = D * (kFp8 ? 1 : 2);
   using TL = TileLayout<kRowBytes>;
   constexpr int kSmemPipe = kDecWarps * kStages * 2 * TL::kTileBytes + kDecWarps * kStages * 8;
-  constexpr int kSmemMerge = (2 * kDecWarps * kMaxGroup + kDecWarps * kMaxGroup * D) * (int)sizeof(float);
+  constexpr int kRows = 8 * kNB;
+  constexpr int kSmemMerge = (2 * kDecWarps * kRows + kDecWarps * kRows * D) * (int)sizeof(float);
   constexpr int kSmem = (kSmemPipe > kSmemMerge ? kSmemPipe : kSmemMerge) + 1024;
   CUtensorMap mk, mv;
   const int box_elems = TL::kBoxRow / (kFp8 ? 1 : 2);
   if (!make_tmap_3d(&mk, p.k_cache, kFp8 ? 1 : 2, num_slots, p.num_kv_heads, D, box_elems, kGroupTok, TL::kSwizzle) ||
       !make_tmap_3d(&mv, p.v_cache, kFp8 ? 1 : 2, num_slots, p.num_kv_heads, D, box_elems, kGroupTok, TL::kSwizzle))
     return PKV_ERR_CUDA;
-  auto kern = paged_decode_split_kernel<D, kFp8, kStages, kInt8>;
+  auto kern = paged_decode_split_kernel<D, kFp8, kStages, kInt8, kNB>;
   static bool attr_set[64] = {false};  // per instantiation and device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -701,7 +771,7 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t
   if (pl.max_splits > 1) {
     // programmatic dependent launch: the combine grid's launch overlaps the
     // split kernel's last wave instead of following its completion
-    const int64_t rows = (int64_t)batch * p.num_heads;
+    const int64_t rows = (int64_t)batch * (p.multi_q ? p.multi_q : 1) * p.num_heads;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
     cfg.blockDim = dim3(128);
@@ -715,6 +785,19 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t
     if (cudaLaunchKernelEx(&cfg, paged_decode_combine_kernel<D>, p, batch) != cudaSuccess) return PKV_ERR_CUDA;
   }
   return launch_status();
+}
+
+template <int kNB>
+int dispatch_decode_rows(int cache_dtype, int head_dim, const DecodeParams& p, int batch, const SplitPlan& pl,
+                         int64_t ns, cudaStream_t st) {
+  if (head_dim == 128) {
+    if (cache_dtype == PKV_FP8_E4M3) return launch_decode<128, true, false, kNB>(p, batch, pl, ns, st);
+    if (cache_dtype == PKV_INT8) return launch_decode<128, true, true, kNB>(p, batch, pl, ns, st);
+    return launch_decode<128, false, false, kNB>(p, batch, pl, ns, st);
+  }
+  if (cache_dtype == PKV_FP8_E4M3) return launch_decode<64, true, false, kNB>(p, batch, pl, ns, st);
+  if (cache_dtype == PKV_INT8) return launch_decode<64, true, true, kNB>(p, batch, pl, ns, st);
+  return launch_decode<64, false, false, kNB>(p, batch, pl, ns, st);
 }
 
 int dispatch_decode(int cache_dtype, int head_dim, const DecodeParams& p, int batch, const SplitPlan& pl,
@@ -876,11 +959,11 @@ namespace pkv {
 
 // Partials of `items` routed rows, split as a decode batch of `batch` sequences would be.
 size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
-                               int cache_dtype) {
+                               int cache_dtype, int multi_q) {
   if (batch <= 0 || items <= 0 || max_len_k <= 0) return 0;
   const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k, cache_dtype);
   if (pl.max_splits <= 1) return 0;
-  const size_t rows = (size_t)items * num_heads * pl.max_splits;
+  const size_t rows = (size_t)items * (multi_q > 0 ? multi_q : 1) * num_heads * pl.max_splits;
   return rows * head_dim * sizeof(float) + ((rows * sizeof(float) + 255) / 256) * 256;
 }
 
@@ -894,13 +977,13 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
                          int32_t max_len_k, int64_t total_q, float scale, int cache_dtype, float k_scale,
                          float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                         int32_t* err_flag, cudaStream_t st) {
+                         int32_t* err_flag, int32_t multi_q, cudaStream_t st) {
   const bool fp8 = cache_dtype != PKV_BF16;  // one-byte codes
   if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
   const SplitPlan pl =
       plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype);
   if (varlen_decode_workspace(batch, item_bound, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1,
-                              cache_dtype) > workspace_bytes)
+                              cache_dtype, multi_q) > workspace_bytes)
     return PKV_ERR_WORKSPACE;
   DecodeParams p{};
   p.q = static_cast<const uint16_t*>(q);
@@ -920,7 +1003,7 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   if (pl.max_splits > 1) {
-    const size_t rows = (size_t)item_bound * num_heads * pl.max_splits;
+    const size_t rows = (size_t)item_bound * (multi_q > 0 ? multi_q : 1) * num_heads * pl.max_splits;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + rows * head_dim * sizeof(float));
   }
@@ -931,7 +1014,15 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.cu_k = cu_k;
   p.lse_head_stride = total_q;
   p.lse_row_stride = 1;
+  p.multi_q = multi_q;
   const int64_t ns = (int64_t)num_blocks * block_size;
+  if (multi_q > 0) {
+    // (query, head) rows of a sequence in blocks of 8 on the MMAs' N side
+    const int rows = multi_q * p.group;
+    if (rows > kMultiRows) return PKV_ERR_UNSUPPORTED;
+    if (rows > 8) return dispatch_decode_rows<2>(cache_dtype, head_dim, p, item_bound, pl, ns, st);
+    return dispatch_decode_rows<1>(cache_dtype, head_dim, p, item_bound, pl, ns, st);
+  }
   return dispatch_decode(cache_dtype, head_dim, p, item_bound, pl, ns, st);
 }
 

@@ -34,11 +34,22 @@ constexpr int kRouteMaxQ = 8;
 constexpr int kRouteCode = 16;
 static_assert(kRouteMaxQ < kRouteCode, "query index must fit the item code");
 
+// When no sequence has more than kRouteMaxQ queries and max_len_q * group
+// query rows fit kMultiRows, one decode CTA per (split, kv head, sequence)
+// serves every (query, head) row of the sequence, so its K/V is read once;
+// otherwise each routed query row is a decode item of its own.
+constexpr int kMultiRows = 16;
+inline bool multi_query_items(int max_len_q, int group) {
+  return max_len_q >= 1 && max_len_q <= kRouteMaxQ && max_len_q * group <= kMultiRows;
+}
+
 // Decode kernels serving the routed query rows of a paged varlen batch
-// (at most item_bound of them; splits planned for `batch` sequences).
+// (at most item_bound items; splits planned for `batch` sequences).  multi_q:
+// 0 (an item is one query row) or the bound on queries per item (an item is a
+// sequence, see multi_query_items).
 
 size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
-                               int cache_dtype);
+                               int cache_dtype, int multi_q);
 int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* items,
                          const int32_t* item_count, const int32_t* cu_q, const int32_t* cu_k,
                          const int32_t* block_table, int32_t max_blocks_per_seq, int32_t batch, int32_t item_bound,
@@ -46,6 +57,6 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
                          int32_t max_len_k, int64_t total_q, float scale, int cache_dtype, float k_scale,
                          float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                         int32_t* err_flag, cudaStream_t st);
+                         int32_t* err_flag, int32_t multi_q, cudaStream_t st);
 
 }  // namespace pkv

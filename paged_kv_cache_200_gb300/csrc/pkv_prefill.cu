@@ -902,7 +902,7 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ cu_k, int batch,
                                                            int32_t* __restrict__ items, int32_t* __restrict__ count,
                                                            int32_t* __restrict__ item_counter, int route_cap,
-                                                           int route_max_q,
+                                                           int route_max_q, int per_sequence,
                                                            int32_t* __restrict__ cu_g, int64_t gather_cap,
                                                            int32_t* err) {
   __shared__ int n;
@@ -914,13 +914,15 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
   }
   __syncthreads();
   if (items != nullptr) {
-    // every query row of a sequence with 1..kRouteMaxQ queries (item codes
-    // b * kRouteCode + qi; the bound route_cap holds them all)
+    // every query row of a sequence with 1..route_max_q queries (item codes
+    // b * kRouteCode + qi; the bound route_cap holds them all), or, with
+    // per_sequence, one item per such sequence (code b * kRouteCode)
     for (int b = threadIdx.x; b < batch; b += blockDim.x) {
       const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
       if (lq >= 1 && lq <= route_max_q) {
-        const int base = atomicAdd(&n, lq);
-        for (int i = 0; i < lq; ++i)
+        const int nq = per_sequence ? 1 : lq;
+        const int base = atomicAdd(&n, nq);
+        for (int i = 0; i < nq; ++i)
           if (base + i < route_cap) items[base + i] = b * kRouteCode + i;
       }
     }
@@ -1094,12 +1096,16 @@ bool uses_gather(bool paged, int kv_dtype, int block_size, int64_t total_k) {
 // when no sequence of the batch has more (then every query row is routed and
 // there are total_q items), else 1 (then at most one item per sequence).
 int route_max_q(int max_len_q) { return max_len_q <= kRouteMaxQ ? kRouteMaxQ : 1; }
-int route_items_bound(int batch, int total_q, int max_len_q) {
+// Queries per routed item: max_len_q when each item is a whole sequence
+// (multi_query_items), else 0 (each item is one query row).
+int route_multi_q(int max_len_q, int group) { return multi_query_items(max_len_q, group) ? max_len_q : 0; }
+int route_items_bound(int batch, int total_q, int max_len_q, int group) {
+  if (route_multi_q(max_len_q, group) > 0) return batch < total_q ? batch : total_q;
   return route_max_q(max_len_q) > 1 ? total_q : (batch < total_q ? batch : total_q);
 }
 
 VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
-                          bool route, bool gather, int64_t total_k, int kv_dtype) {
+                          bool route, bool gather, int64_t total_k, int kv_dtype, int multi_q) {
   VarlenWs w{0, 0, 0, 0, 0, 0, 256};
   if (batch <= 0) return w;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -1108,7 +1114,8 @@ VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_
     w.items_off = 256;
     w.decode_off = w.items_off + up((size_t)route_items * 4);
     w.total = w.decode_off +
-              varlen_decode_workspace(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, kv_dtype);
+              varlen_decode_workspace(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, kv_dtype,
+                                      multi_q);
   }
   if (gather) {
     w.cu_g_off = up(w.total);
@@ -1157,10 +1164,10 @@ extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q
       total_q < 0)
     return 0;
   const bool gather = pkv::uses_gather(paged != 0, kv_dtype, block_size, total_k);
-  return pkv::varlen_ws_layout(batch, pkv::route_items_bound(batch, total_q, max_len_q), num_heads, num_kv_heads,
-                               head_dim,
-                               max_len_k,
-                               routes_decode(paged != 0, num_heads, num_kv_heads), gather, total_k, kv_dtype)
+  const int group = num_heads / num_kv_heads;
+  return pkv::varlen_ws_layout(batch, pkv::route_items_bound(batch, total_q, max_len_q, group), num_heads,
+                               num_kv_heads, head_dim, max_len_k, routes_decode(paged != 0, num_heads, num_kv_heads),
+                               gather, total_k, kv_dtype, pkv::route_multi_q(max_len_q, group))
       .total;
 }
 
@@ -1202,11 +1209,12 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
 
   const bool gather = uses_gather(paged, kv_dtype, block_size, total_k);
-  const int route_items = route ? route_items_bound(batch, total_q, max_len_q) : 0;
+  const int group = num_heads / num_kv_heads;
+  const int route_items = route ? route_items_bound(batch, total_q, max_len_q, group) : 0;
   const int rmq = route ? route_max_q(max_len_q) : 0;  // queries up to which a sequence is routed
-  const VarlenWs wl =
-      varlen_ws_layout(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, route, gather, total_k,
-                       kv_dtype);
+  const int multi_q = route ? route_multi_q(max_len_q, group) : 0;  // an item is a whole sequence
+  const VarlenWs wl = varlen_ws_layout(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, route,
+                                       gather, total_k, kv_dtype, multi_q);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
                        (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
@@ -1263,8 +1271,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   }
   int32_t* cu_g = gather ? reinterpret_cast<int32_t*>(wsb + wl.cu_g_off) : nullptr;
   varlen_prep_kernel<<<1, (items != nullptr || gather) ? 1024 : 32, 0, st>>>(
-      cu_seqlens_q, cu_seqlens_k, batch, items, count, p.item_counter, route_items, rmq, cu_g, (int64_t)total_k,
-      err_flag);
+      cu_seqlens_q, cu_seqlens_k, batch, items, count, p.item_counter, route_items, rmq, multi_q > 0 ? 1 : 0, cu_g,
+      (int64_t)total_k, err_flag);
   if (gather) {
     const int gx = (max_len_k + kGatherPos - 1) / kGatherPos;
     const dim3 ggrid((unsigned)(gx > 0 ? gx : 1), (unsigned)batch, 1);
@@ -1294,7 +1302,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
                               max_len_k,
                               total_q,
                               scale, kv_dtype, k_scale, v_scale, out, lse, wsb + wl.decode_off,
-                              (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, st);
+                              (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, multi_q, st);
 }
 
 #ifdef PKV_TEST_HOOKS

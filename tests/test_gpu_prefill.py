@@ -344,3 +344,40 @@ def test_varlen_paged_int8(pkv, case):
                                        kv_dtype="int8", k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
     assert_close(f64(out), ref, FP8_ATOL, FP8_RTOL, f"int8 {case}")
     assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"int8 lse {case}")
+
+
+# (max queries, Hq, Hkv, D, block size, cache type): every sequence's (query, head) rows
+# fit one decode pass (queries x group <= 16), so each sequence's K/V is read once
+ONE_PASS = [
+    (4, 32, 8, 128, 16, "bf16"),      # 16 rows: two 8-row blocks
+    (2, 64, 8, 128, 32, "bf16"),      # group 8: 16 rows
+    (4, 8, 4, 64, 16, "bf16"),        # group 2: 8 rows, one block, d64
+    (4, 32, 8, 128, 16, "fp8_e4m3"),
+    (4, 32, 8, 128, 16, "int8"),
+    (3, 16, 4, 128, 32, "bf16"),      # 12 rows: the second block half used
+]
+
+
+@pytest.mark.parametrize("case", ONE_PASS, ids=[f"q{c[0]}_{c[1]}q{c[2]}kv_d{c[3]}_bs{c[4]}_{c[5]}" for c in ONE_PASS])
+def test_multi_query_one_pass(pkv, case):
+    """Speculative verification with few queries: one decode CTA per (split, kv head, sequence)
+    computes every query row of the sequence, each over its own bottom-right causal prefix."""
+    max_q, Hq, Hkv, D, bs, dt = case
+    rng = np.random.default_rng(71 + max_q + Hq)
+    q_lens = rng.integers(1, max_q + 1, size=10)
+    q_lens[0] = max_q
+    prefix = rng.integers(0, 3000, size=10)
+    prefix[2] = 0                                   # only its new tokens
+    prefix[4] = 5000                                # several splits
+    wl = W.make_varlen_paged(q_lens, prefix, Hq, Hkv, D, bs, seed=72 + max_q, device="cuda")
+    if dt != "bf16":
+        wl = W.to_fp8_cache(wl, dt)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=False)
+    kw = {} if dt == "bf16" else dict(kv_dtype=dt, k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=bs, **kw)
+    atol, rtol = (BF16_ATOL, BF16_RTOL) if dt == "bf16" else (FP8_ATOL, FP8_RTOL)
+    assert_close(f64(out), ref, atol, rtol, f"one-pass multi-query {case}")
+    assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"one-pass multi-query lse {case}")
