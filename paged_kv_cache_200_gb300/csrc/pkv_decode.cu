@@ -504,10 +504,15 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
             // picks them in its widening permute; E4M3 reorders the word first.
             uint32_t ev[4], od[4];
             if constexpr (kInt8) {
-              ev[0] = int8x2_even_to_f16x2(r0); ev[1] = int8x2_even_to_f16x2(r1);
-              ev[2] = int8x2_even_to_f16x2(r2); ev[3] = int8x2_even_to_f16x2(r3);
-              od[0] = int8x2_odd_to_f16x2(r0); od[1] = int8x2_odd_to_f16x2(r1);
-              od[2] = int8x2_odd_to_f16x2(r2); od[3] = int8x2_odd_to_f16x2(r3);
+              // V codes widen to 1152 + c (no subtract): O then exceeds the sum
+              // over the codes by 1152 l, since O and l are always scaled
+              // together; the merge below takes 1152 L off once
+              const uint32_t x0 = r0 ^ 0x80808080u, x1 = r1 ^ 0x80808080u;
+              const uint32_t x2 = r2 ^ 0x80808080u, x3 = r3 ^ 0x80808080u;
+              ev[0] = prmt(x0, 0x64646464u, 0x4240u); ev[1] = prmt(x1, 0x64646464u, 0x4240u);
+              ev[2] = prmt(x2, 0x64646464u, 0x4240u); ev[3] = prmt(x3, 0x64646464u, 0x4240u);
+              od[0] = prmt(x0, 0x64646464u, 0x4341u); od[1] = prmt(x1, 0x64646464u, 0x4341u);
+              od[2] = prmt(x2, 0x64646464u, 0x4341u); od[3] = prmt(x3, 0x64646464u, 0x4341u);
             } else {
               const uint32_t t0 = prmt(r0, 0u, 0x3120u), t1 = prmt(r1, 0u, 0x3120u);
               const uint32_t t2 = prmt(r2, 0u, 0x3120u), t3 = prmt(r3, 0u, 0x3120u);
@@ -594,6 +599,7 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
       }
     }
     const bool any = L > 0.f;
+    if constexpr (kInt8) acc -= kInt8Bias * L;  // the V codes were widened to 1152 + c
     const float val = any ? acc * p.v_mul / L : 0.f;
     const float lse2 = any ? ms + log2f(L) : -INFINITY;
     const int qr = p.multi_q ? r / p.group : 0;

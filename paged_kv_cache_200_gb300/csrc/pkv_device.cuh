@@ -168,6 +168,11 @@ __device__ __forceinline__ uint32_t int8x2_odd_to_f16x2(uint32_t w) {
   return d;
 }
 
+// INT8 codes widened without the final subtract hold 1152 + c (the
+// permutes above alone); a product sum over such values exceeds the one over
+// the codes by 1152 times the sum of the other factor, subtracted once.
+constexpr float kInt8Bias = 1152.f;
+
 // Packed fp32 pairs (sm_100+): two lanes of arithmetic per instruction.
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
   uint64_t r;
