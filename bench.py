@@ -860,7 +860,7 @@ def ncu_case(args):
         log("ncu case done: prefill")
         return
     rng = np.random.default_rng(77)
-    dt = "fp8_e4m3" if args.ncu_case == "decode_fp8" else "bf16"
+    dt = {"decode_fp8": "fp8_e4m3", "decode_int8": "int8"}.get(args.ncu_case, "bf16")
     # 64 sequences of 1K..4K cached tokens: ~0.65 GB of bf16 K/V, larger than L2
     wl = W.make_decode(rng.integers(1024, 4096, 64, endpoint=True), 32, 8, 128, 16, seed=77, device="cuda",
                        cache_dtype=dt)
@@ -884,7 +884,7 @@ def main():
                     help="seconds of the all-cores oracle timing (0: skip)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "prefill"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "decode_int8", "prefill"], default=None,
                     help="run a small case for an ncu capture and exit")
     args = ap.parse_args()
     if args.ncu_case:

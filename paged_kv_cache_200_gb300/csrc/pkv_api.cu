@@ -37,8 +37,61 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+namespace {
+
+// Recently encoded tensor maps.  A serving loop calls the attention entry
+// points with the same caches and shapes again and again; the encoding is pure
+// host work, so its result is kept (the map holds addresses only, never data,
+// and is valid on any device).  Small, most recent first, under a mutex.
+struct TmapKey {
+  const void* base;
+  int64_t rows;
+  int elt_bytes, heads, dim, box_inner, box_rows, swizzle_bytes;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && rows == o.rows && elt_bytes == o.elt_bytes && heads == o.heads && dim == o.dim &&
+           box_inner == o.box_inner && box_rows == o.box_rows && swizzle_bytes == o.swizzle_bytes;
+  }
+};
+constexpr int kTmapCacheSize = 16;
+std::mutex g_tmap_mu;
+TmapKey g_tmap_keys[kTmapCacheSize];
+CUtensorMap g_tmap_maps[kTmapCacheSize];
+int g_tmap_count = 0;
+
+bool encode_tmap_3d(CUtensorMap* map, const void* base, int elt_bytes, int64_t rows, int heads, int dim,
+                    int box_inner, int box_rows, int swizzle_bytes);
+
+}  // namespace
+
 bool make_tmap_3d(CUtensorMap* map, const void* base, int elt_bytes, int64_t rows, int heads, int dim,
                   int box_inner, int box_rows, int swizzle_bytes) {
+  const TmapKey key{base, rows, elt_bytes, heads, dim, box_inner, box_rows, swizzle_bytes};
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    for (int i = 0; i < g_tmap_count; ++i)
+      if (g_tmap_keys[i] == key) {
+        *map = g_tmap_maps[i];
+        return true;
+      }
+  }
+  if (!encode_tmap_3d(map, base, elt_bytes, rows, heads, dim, box_inner, box_rows, swizzle_bytes)) return false;
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  // insert at the front, dropping the oldest entry when full
+  const int n = g_tmap_count < kTmapCacheSize ? g_tmap_count + 1 : kTmapCacheSize;
+  for (int i = n - 1; i > 0; --i) {
+    g_tmap_keys[i] = g_tmap_keys[i - 1];
+    g_tmap_maps[i] = g_tmap_maps[i - 1];
+  }
+  g_tmap_keys[0] = key;
+  g_tmap_maps[0] = *map;
+  g_tmap_count = n;
+  return true;
+}
+
+namespace {
+
+bool encode_tmap_3d(CUtensorMap* map, const void* base, int elt_bytes, int64_t rows, int heads, int dim,
+                    int box_inner, int box_rows, int swizzle_bytes) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
@@ -53,6 +106,7 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int elt_bytes, int64_t row
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
 }  // namespace pkv
 
 extern "C" const char* pkv_status_string(int status) {

@@ -180,9 +180,15 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
   constexpr int kDT = D / 16;
   constexpr int kRows = 8 * kNB;                  // rows served by this CTA (at most)
   constexpr int kBoxElems = TL::kBoxRow / (kFp8 ? 1 : 2);
-  // two one-byte codes (bytes 0..1, resp. 2..3, of a word) -> f16x2, exactly
-  auto code_lo = [](uint32_t w) { return kInt8 ? int8x2_lo_to_f16x2(w) : e4m3x2_lo_to_f16x2(w); };
-  auto code_hi = [](uint32_t w) { return kInt8 ? int8x2_hi_to_f16x2(w) : e4m3x2_hi_to_f16x2(w); };
+  // two one-byte codes (bytes 0..1, resp. 2..3, of a word) -> f16x2: E4M3
+  // exactly; INT8 as 1152 + c (the permute alone), the excess taken off the
+  // logits below (K) and the output in the merge (V)
+  auto code_lo = [](uint32_t w) {
+    return kInt8 ? prmt(w ^ 0x80808080u, 0x64646464u, 0x4140u) : e4m3x2_lo_to_f16x2(w);
+  };
+  auto code_hi = [](uint32_t w) {
+    return kInt8 ? prmt(w ^ 0x80808080u, 0x64646464u, 0x4342u) : e4m3x2_hi_to_f16x2(w);
+  };
 
   // The combine kernel may be scheduled as soon as every CTA of this grid has
   // started; it waits for this grid's completion before it reads anything.
@@ -290,6 +296,30 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
         for (int h2 = 0; h2 < 2; ++h2)
           qf[bk][kk][h2] = pack_f16x2(__uint_as_float(qf[bk][kk][h2] << 16) * qs,
                                       __uint_as_float(qf[bk][kk][h2] & 0xFFFF0000u) * qs);
+  }
+  // INT8: K codes widen to 1152 + c, so a score exceeds the one over the codes
+  // by 1152 times the row's sum of (f16) Q; that excess, in logit units, per
+  // row of this thread's S^T fragment (rows 2j, 2j+1 of each block)
+  float kx_a[kNB], kx_b[kNB];
+#pragma unroll
+  for (int bk = 0; bk < kNB; ++bk) kx_a[bk] = kx_b[bk] = 0.f;
+  if constexpr (kInt8) {
+#pragma unroll
+    for (int bk = 0; bk < kNB; ++bk) {
+      float qsum = 0.f;  // this lane's head dims of row lane/4
+#pragma unroll
+      for (int kk = 0; kk < kDT; ++kk)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qf[bk][kk][h2]));
+          qsum += f.x + f.y;
+        }
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // whole row, in every lane of its quad
+      const int j = lane & 3;
+      kx_a[bk] = kInt8Bias * __shfl_sync(0xffffffffu, qsum, 8 * j) * scale_log2;
+      kx_b[bk] = kInt8Bias * __shfl_sync(0xffffffffu, qsum, 8 * j + 4) * scale_log2;
+    }
   }
 
   auto block_of = [&](int pos0, bool report) -> int {
@@ -443,10 +473,10 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
       uint32_t pb0[kNB], pb1[kNB];
 #pragma unroll
       for (int bk = 0; bk < kNB; ++bk) {
-        const float x0 = tok0 < lim_a[bk] ? s[bk][0] * scale_log2 : -INFINITY;
-        const float x1 = tok0 < lim_b[bk] ? s[bk][1] * scale_log2 : -INFINITY;
-        const float x2 = tok0 + 8 < lim_a[bk] ? s[bk][2] * scale_log2 : -INFINITY;
-        const float x3 = tok0 + 8 < lim_b[bk] ? s[bk][3] * scale_log2 : -INFINITY;
+        const float x0 = tok0 < lim_a[bk] ? fmaf(s[bk][0], scale_log2, -kx_a[bk]) : -INFINITY;
+        const float x1 = tok0 < lim_b[bk] ? fmaf(s[bk][1], scale_log2, -kx_b[bk]) : -INFINITY;
+        const float x2 = tok0 + 8 < lim_a[bk] ? fmaf(s[bk][2], scale_log2, -kx_a[bk]) : -INFINITY;
+        const float x3 = tok0 + 8 < lim_b[bk] ? fmaf(s[bk][3], scale_log2, -kx_b[bk]) : -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {

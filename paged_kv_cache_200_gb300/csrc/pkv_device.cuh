@@ -137,40 +137,12 @@ __device__ __forceinline__ uint2 quantize8_int8(uint4 v, float inv) {
   return make_uint2(packed[0], packed[1]);
 }
 
-// Two INT8 codes (bytes 0..1, resp. 2..3, of w) -> f16x2, exactly.  With the
-// sign bit flipped a code c becomes the unsigned byte c + 128; as the low
-// mantissa bits of an f16 whose exponent field gives 2^10 (high byte 0x64) it
-// reads 1024 + c + 128, and subtracting 1152 leaves c.
-__device__ __forceinline__ uint32_t int8x2_lo_to_f16x2(uint32_t w) {
-  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4140u);
-  uint32_t d;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
-  return d;
-}
-__device__ __forceinline__ uint32_t int8x2_hi_to_f16x2(uint32_t w) {
-  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4342u);
-  uint32_t d;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
-  return d;
-}
-
-// Bytes {0, 2}, resp. {1, 3}, of a word of INT8 codes -> f16x2 (same method).
-__device__ __forceinline__ uint32_t int8x2_even_to_f16x2(uint32_t w) {
-  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4240u);
-  uint32_t d;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
-  return d;
-}
-__device__ __forceinline__ uint32_t int8x2_odd_to_f16x2(uint32_t w) {
-  const uint32_t t = prmt(w ^ 0x80808080u, 0x64646464u, 0x4341u);
-  uint32_t d;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x64806480u));
-  return d;
-}
-
-// INT8 codes widened without the final subtract hold 1152 + c (the
-// permutes above alone); a product sum over such values exceeds the one over
-// the codes by 1152 times the sum of the other factor, subtracted once.
+// INT8 codes to f16, exactly, by a byte permute: with its sign bit flipped a
+// code c is the unsigned byte c + 128; placed as the low mantissa byte of an
+// f16 whose exponent field gives 2^10 (high byte 0x64) it reads
+// 1024 + c + 128 = 1152 + c.  The decode kernel feeds these biased values to
+// its MMAs and takes the excess (1152 times the sum of the other factor) off
+// once: from the logits for K, from the output for V.
 constexpr float kInt8Bias = 1152.f;
 
 // Packed fp32 pairs (sm_100+): two lanes of arithmetic per instruction.

@@ -249,8 +249,10 @@ def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale: fl
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     L = lib()
-    need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
-    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device, stream) if need else None)
+    ws = workspace_buf
+    if ws is None:  # (a caller-provided buffer skips the size query; the call checks it)
+        need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
+        ws = workspace(need, q.device, stream) if need else None
     st = L.pkv_paged_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _cache_dtype(k_cache),
                                  _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB,
                                  int(max_seqlen_k), float(scale), float(k_scale), float(v_scale), _ptr(out),
@@ -296,8 +298,10 @@ def paged_attn_decode_with_kvcache(q, k_new, v_new, k_cache, v_cache, cache_seql
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     L = lib()
-    need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
-    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device, stream) if need else None)
+    ws = workspace_buf
+    if ws is None:  # (a caller-provided buffer skips the size query; the call checks it)
+        need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
+        ws = workspace(need, q.device, stream) if need else None
     st = L.pkv_paged_attn_decode_with_kvcache(
         _ptr(q), _ptr(k_new), k_new.stride(0), _ptr(v_new), v_new.stride(0), _ptr(k_cache), _ptr(v_cache),
         _cache_dtype(k_cache), _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB, int(max_seqlen_k),
@@ -382,9 +386,11 @@ def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_l
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
     L = lib()
     paged = 1 if block_table is not None else 0
-    need = L.pkv_paged_attn_varlen_workspace(B, T, total_k, Hq, Hkv, D, int(max_len_q), int(max_len_k), paged,
-                                             _cache_dtype(k), bs)
-    ws = workspace_buf if workspace_buf is not None else (workspace(need, q.device, stream) if need else None)
+    ws = workspace_buf
+    if ws is None:  # (a caller-provided buffer skips the size query; the call checks it)
+        need = L.pkv_paged_attn_varlen_workspace(B, T, total_k, Hq, Hkv, D, int(max_len_q), int(max_len_k), paged,
+                                                 _cache_dtype(k), bs)
+        ws = workspace(need, q.device, stream) if need else None
     st = L.pkv_paged_attn_varlen(_ptr(q), _ptr(k), _ptr(v), _cache_dtype(k), _ptr(cu_seqlens_q),
                                  _ptr(cu_seqlens_k), B, T, total_k, int(max_len_q), int(max_len_k),
                                  _ptr(block_table), MB, bs, NB, Hq, Hkv, D, float(scale), 1 if causal else 0,
