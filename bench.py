@@ -549,11 +549,13 @@ def example_latency(pkv, W, device, iters=200):
     need = pkv.lib().pkv_paged_attn_decode_workspace(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim,
                                                      wl.max_seqlen)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    # what a serving loop holds across steps: the cache views, the host bound, the buffers
+    kc4, vc4, max_len = kc.view(shape4), vc.view(shape4), int(wl.max_seqlen)
 
     def step():
         pkv.kv_cache_write(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
-        pkv.paged_attn_decode(wl.q, kc.view(shape4), vc.view(shape4), wl.cache_seqlens, wl.block_table, wl.scale,
-                              max_seqlen_k=wl.max_seqlen, out=out, workspace_buf=ws)
+        pkv.paged_attn_decode(wl.q, kc4, vc4, wl.cache_seqlens, wl.block_table, wl.scale, max_seqlen_k=max_len,
+                              out=out, workspace_buf=ws)
 
     eager_ms = time_calls(step, iters)
     side = torch.cuda.Stream()

@@ -106,23 +106,45 @@ def _check(status: int):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # (the argument types are c_void_p: a plain int or None converts directly)
+    return None if t is None else t.data_ptr()
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    """The cudaStream_t (as an int) of ``stream``, default: the current device's current stream (the
+    library launches on the current device)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:  # the same handle as current_stream().cuda_stream, without building a Stream
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _cache_dtype(cache: torch.Tensor) -> int:
-    if cache.dtype == torch.bfloat16:
+    if cache.dtype == _BF16:
         return PKV_BF16
     if cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
         return PKV_FP8_E4M3
     if cache.dtype == torch.int8:
         return PKV_INT8
     raise TypeError(f"unsupported cache dtype {cache.dtype}")
+
+
+_BF16 = torch.bfloat16
+_I32 = torch.int32
+_fns = {}
+
+
+def _fn(name):
+    """The library function (bound once, with its argument types)."""
+    f = _fns.get(name)
+    if f is None:
+        f = getattr(lib(), name)
+        _fns[name] = f
+    return f
 
 
 def _require_cuda(*ts):
@@ -169,23 +191,31 @@ def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, k_inv_scale: float = 1.
     or int8 codes.  FP8 stores ``e4m3(x * inv_scale)``; INT8 stores
     ``clamp(rint(x * inv_scale), -127, 127)`` with NaN stored as 0.
     """
-    _require_cuda(k, v, k_cache, v_cache, slot_mapping)
+    # One combined check on the common path (this runs once per layer and
+    # step); the detailed checks below only name what is wrong.
     T, Hkv, D = k.shape
-    if v.shape != k.shape or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
-        raise ValueError("k and v must be bf16 tensors of the same shape [T, Hkv, D]")
-    if k.stride(-1) != 1 or v.stride(-1) != 1 or k.stride(1) != D or v.stride(1) != D:
-        raise ValueError("k/v inner dims [Hkv, D] must be contiguous")
-    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
-        raise ValueError("caches must be contiguous")
-    if k_cache.shape[-2:] != (Hkv, D) or v_cache.shape != k_cache.shape:
-        raise ValueError("caches must end in [Hkv, D] and match each other")
-    if slot_mapping.dtype != torch.int32 or slot_mapping.numel() != T:
+    ks, vs = k.stride(), v.stride()
+    if not (k.is_cuda and v.is_cuda and k_cache.is_cuda and v_cache.is_cuda and slot_mapping.is_cuda
+            and (err_flag is None or err_flag.is_cuda) and k.dtype == _BF16 and v.dtype == _BF16
+            and v.shape == k.shape and ks[2] == 1 and vs[2] == 1 and ks[1] == D and vs[1] == D
+            and k_cache.is_contiguous() and v_cache.is_contiguous() and v_cache.shape == k_cache.shape
+            and k_cache.shape[-2:] == (Hkv, D) and slot_mapping.dtype == _I32 and slot_mapping.numel() == T):
+        _require_cuda(k, v, k_cache, v_cache, slot_mapping, err_flag)
+        if v.shape != k.shape or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+            raise ValueError("k and v must be bf16 tensors of the same shape [T, Hkv, D]")
+        if ks[2] != 1 or vs[2] != 1 or ks[1] != D or vs[1] != D:
+            raise ValueError("k/v inner dims [Hkv, D] must be contiguous")
+        if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+            raise ValueError("caches must be contiguous")
+        if k_cache.shape[-2:] != (Hkv, D) or v_cache.shape != k_cache.shape:
+            raise ValueError("caches must end in [Hkv, D] and match each other")
         raise ValueError("slot_mapping must be int32 with one entry per token")
     num_slots = k_cache.numel() // (Hkv * D)
-    st = lib().pkv_kv_cache_write(_ptr(k), k.stride(0), _ptr(v), v.stride(0), T, Hkv, D, _ptr(k_cache),
-                                  _ptr(v_cache), _cache_dtype(k_cache), num_slots, _ptr(slot_mapping),
-                                  float(k_inv_scale), float(v_inv_scale), _ptr(err_flag), _stream(stream))
-    _check(st)
+    st = _fn("pkv_kv_cache_write")(k.data_ptr(), ks[0], v.data_ptr(), vs[0], T, Hkv, D, k_cache.data_ptr(),
+                                   v_cache.data_ptr(), _cache_dtype(k_cache), num_slots, slot_mapping.data_ptr(),
+                                   k_inv_scale, v_inv_scale, _ptr(err_flag), _stream(stream))
+    if st:
+        _check(st)
 
 
 # ---------------------------------------------------------------------------
@@ -230,16 +260,23 @@ def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale: fl
     ``[B, max_blocks_per_seq]``.  ``max_seqlen_k`` is a host upper bound of the
     lengths (default: the block table's capacity; no device sync is made).
     """
-    _require_cuda(q, k_cache, v_cache, cache_seqlens, block_table)
     B, Hq, D = q.shape
     NB, bs, Hkv, D2 = k_cache.shape
-    if D2 != D or v_cache.shape != k_cache.shape:
-        raise ValueError("cache shape mismatch")
-    if q.dtype != torch.bfloat16 or not q.is_contiguous():
-        raise ValueError("q must be contiguous bf16 [B, Hq, D]")
-    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.is_contiguous()):
-        raise ValueError("caches and block_table must be contiguous")
-    if cache_seqlens.dtype != torch.int32 or block_table.dtype != torch.int32:
+    # one combined check on the common path (once per layer and step); the
+    # detailed checks below only name what is wrong
+    if not (q.is_cuda and k_cache.is_cuda and v_cache.is_cuda and cache_seqlens.is_cuda and block_table.is_cuda
+            and (out is None or out.is_cuda) and (lse is None or lse.is_cuda)
+            and (err_flag is None or err_flag.is_cuda) and (workspace_buf is None or workspace_buf.is_cuda)
+            and D2 == D and v_cache.shape == k_cache.shape and q.dtype == _BF16 and q.is_contiguous()
+            and k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.is_contiguous()
+            and cache_seqlens.dtype == _I32 and block_table.dtype == _I32):
+        _require_cuda(q, k_cache, v_cache, cache_seqlens, block_table, out, lse, err_flag, workspace_buf)
+        if D2 != D or v_cache.shape != k_cache.shape:
+            raise ValueError("cache shape mismatch")
+        if q.dtype != torch.bfloat16 or not q.is_contiguous():
+            raise ValueError("q must be contiguous bf16 [B, Hq, D]")
+        if not (k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.is_contiguous()):
+            raise ValueError("caches and block_table must be contiguous")
         raise ValueError("cache_seqlens and block_table must be int32")
     MB = block_table.shape[1]
     if max_seqlen_k is None:
@@ -248,17 +285,17 @@ def paged_attn_decode(q, k_cache, v_cache, cache_seqlens, block_table, scale: fl
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    L = lib()
     ws = workspace_buf
     if ws is None:  # (a caller-provided buffer skips the size query; the call checks it)
-        need = L.pkv_paged_attn_decode_workspace(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
+        need = _fn("pkv_paged_attn_decode_workspace")(B, Hq, Hkv, D, max(int(max_seqlen_k), 1))
         ws = workspace(need, q.device, stream) if need else None
-    st = L.pkv_paged_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _cache_dtype(k_cache),
-                                 _ptr(cache_seqlens), _ptr(block_table), MB, B, Hq, Hkv, D, bs, NB,
-                                 int(max_seqlen_k), float(scale), float(k_scale), float(v_scale), _ptr(out),
-                                 _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(err_flag),
-                                 _stream(stream))
-    _check(st)
+    st = _fn("pkv_paged_attn_decode")(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), _cache_dtype(k_cache),
+                                      cache_seqlens.data_ptr(), block_table.data_ptr(), MB, B, Hq, Hkv, D, bs, NB,
+                                      int(max_seqlen_k), scale, k_scale, v_scale, out.data_ptr(), _ptr(lse),
+                                      _ptr(ws), 0 if ws is None else ws.numel(), _ptr(err_flag),
+                                      _stream(stream))
+    if st:
+        _check(st)
     return (out, lse) if (return_lse or lse is not None) else out
 
 
