@@ -716,6 +716,10 @@ struct SplitPlan {
   int split_tokens;
   int max_splits;
   size_t workspace;
+  // launch the split kernel as a programmatic dependent of the kernel before
+  // it on the stream (which reads nothing it writes): its CTAs then start on
+  // SMs that kernel's CTAs have left
+  bool after_primary = false;
 };
 
 // Positions per CTA (split_tokens), a multiple of 64 (4 warps x 16), at least
@@ -803,7 +807,21 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t
     attr_set[dev] = true;
   }
   dim3 grid(pl.max_splits, p.num_kv_heads, batch);
-  kern<<<grid, kDecThreads, kSmem, st>>>(mk, mv, p);
+  if (pl.after_primary) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mk, mv, p) != cudaSuccess) return PKV_ERR_CUDA;
+  } else {
+    kern<<<grid, kDecThreads, kSmem, st>>>(mk, mv, p);
+  }
   if (pl.max_splits > 1) {
     // programmatic dependent launch: the combine grid's launch overlaps the
     // split kernel's last wave instead of following its completion
@@ -1013,11 +1031,11 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
                          int32_t max_len_k, int64_t total_q, float scale, int cache_dtype, float k_scale,
                          float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                         int32_t* err_flag, int32_t multi_q, cudaStream_t st) {
+                         int32_t* err_flag, int32_t multi_q, bool after_primary, cudaStream_t st) {
   const bool fp8 = cache_dtype != PKV_BF16;  // one-byte codes
   if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
-  const SplitPlan pl =
-      plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype);
+  SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype);
+  pl.after_primary = after_primary;
   if (varlen_decode_workspace(batch, item_bound, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1,
                               cache_dtype, multi_q) > workspace_bytes)
     return PKV_ERR_WORKSPACE;

@@ -46,7 +46,9 @@ inline bool multi_query_items(int max_len_q, int group) {
 // Decode kernels serving the routed query rows of a paged varlen batch
 // (at most item_bound items; splits planned for `batch` sequences).  multi_q:
 // 0 (an item is one query row) or the bound on queries per item (an item is a
-// sequence, see multi_query_items).
+// sequence, see multi_query_items).  after_primary: launch the split kernel as
+// a programmatic dependent of the kernel just before it on the stream, which
+// must not write anything the decode kernels read.
 
 size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
                                int cache_dtype, int multi_q);
@@ -57,6 +59,6 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
                          int32_t max_len_k, int64_t total_q, float scale, int cache_dtype, float k_scale,
                          float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                         int32_t* err_flag, int32_t multi_q, cudaStream_t st);
+                         int32_t* err_flag, int32_t multi_q, bool after_primary, cudaStream_t st);
 
 }  // namespace pkv

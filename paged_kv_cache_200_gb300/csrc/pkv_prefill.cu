@@ -312,6 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     varlen_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = Smem<D>;
+  // The decode kernels of the same call (the routed query rows) may start as
+  // soon as SMs free up: they read nothing this kernel writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -1302,7 +1305,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
                               max_len_k,
                               total_q,
                               scale, kv_dtype, k_scale, v_scale, out, lse, wsb + wl.decode_off,
-                              (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, multi_q, st);
+                              (gather ? wl.cu_g_off : wl.total) - wl.decode_off, err_flag, multi_q, !all_routed,
+                              st);
 }
 
 #ifdef PKV_TEST_HOOKS
