@@ -70,6 +70,9 @@ typedef enum {
   PKV_ERR_CUDA = 4         /* a kernel launch or a driver call failed */
 } pkv_status;
 
+/* Element types.  Queries, outputs and bf16 caches are bfloat16, the type the
+ * method is stated in; float16 is not built (code 1 is left unassigned, and any
+ * dtype code other than those below returns PKV_ERR_UNSUPPORTED). */
 typedef enum {
   PKV_BF16 = 0,      /* bfloat16 */
   PKV_FP8_E4M3 = 2,  /* OCP FP8 E4M3 (cache only), per-tensor scale */

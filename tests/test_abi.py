@@ -55,6 +55,24 @@ def test_host_side_argument_validation():
     assert lib.pkv_paged_attn_decode(*args(8, 3, 128, 16)) == 1
 
 
+def test_dtype_codes_outside_bf16_fp8_int8_are_unsupported():
+    """float16 is not built: code 1 (and any other unknown code) is refused by every entry point that
+    takes a dtype, with PKV_ERR_UNSUPPORTED, before any launch."""
+    pkv = built_library()
+    lib = pkv.lib()
+    nul = ctypes.c_void_p(0)
+    row = ctypes.c_void_p(4096)  # non-null, aligned new-row pointers (never dereferenced: refused first)
+    for dt in (1, 4, -1):
+        assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 4, 1, 128, nul, nul, dt, 16, nul, 1.0, 1.0, nul, nul) == 2
+        assert lib.pkv_paged_attn_decode(nul, nul, nul, dt, nul, nul, 4, 1, 8, 2, 128, 16, 8, 64, 0.1, 1.0, 1.0,
+                                         nul, nul, nul, 0, nul, nul) == 2
+        assert lib.pkv_paged_attn_decode_with_kvcache(nul, row, 1024, row, 1024, nul, nul, dt, nul, nul, 4, 1, 8,
+                                                      2, 128, 16, 8, 64, 0.1, 1.0, 1.0, 1.0, 1.0, nul, nul, nul,
+                                                      0, nul, nul) == 2
+        assert lib.pkv_paged_attn_varlen(nul, nul, nul, dt, nul, nul, 4, 16, 0, 4, 64, nul, 8, 16, 64, 8, 2, 128,
+                                         0.1, 1, 1.0, 1.0, nul, nul, nul, 0, nul, nul) == 2
+
+
 def test_one_byte_caches_need_valid_inverse_scales():
     """An FP8 or INT8 cache write (and the append of decode-with-append) refuses a zero, negative,
     infinite or NaN inverse scale before any launch; a bf16 cache ignores the scales."""
