@@ -83,7 +83,9 @@ typedef enum {
 #define PKV_DEVERR_SLOT 1        /* a slot_mapping entry >= num_slots (row skipped) */
 #define PKV_DEVERR_BLOCK 2       /* a block_table entry outside [0, num_blocks) was needed */
 #define PKV_DEVERR_LENGTH 4      /* a length is negative or needs more than max_blocks_per_seq blocks */
-#define PKV_DEVERR_TIMEOUT 8     /* a bounded wait inside a kernel gave up (the tile was abandoned) */
+#define PKV_DEVERR_TIMEOUT 8     /* a bounded wait inside a kernel gave up (the tile was abandoned);
+                                    the call's out and lse are then undefined, while the context,
+                                    the caches and later calls stay valid */
 
 /* Human-readable name of a pkv_status. */
 PKV_API const char* pkv_status_string(int status);
