@@ -13,9 +13,9 @@
 //
 // Persistent kernel, one 352-thread CTA per SM.  A work item is a pair of
 // adjacent 128-row query tiles (A, then B) of one (sequence, query head),
-// paired from the sequence's end; both tiles read the same K/V tiles (B's
-// keys: A's last step is masked), so each K/V tile is loaded once for 256
-// query rows.  Items are claimed through a global counter, longest first, and
+// paired from the sequence's end; both tiles read the same K/V tiles (tile
+// A stops at its own last visible tile, one before B's), so each K/V tile is
+// loaded once for 256 query rows.  Items are claimed through a global counter, longest first, and
 // published to the CTA's warps through a shared ring.
 //   warp 0      producer: Q of both tiles (TMA), then K/V tiles of 128 keys
 //               (2 stages each), K one tile ahead of V.  Packed K/V: one TMA
@@ -28,7 +28,8 @@
 //               every ~120-140 cycles, whatever N is, so the two tiles' MMAs
 //               come from two threads and interleave in the tensor core.
 //   warps 3..6  softmax of tile A, warps 7..10 of tile B: one thread per query
-//               row, all 128 keys of each tile.  The running max moves only
+//               row, all 128 keys of each tile.  The two groups take turns
+//               tile by tile while both have tiles left.  The running max moves only
 //               when it grows by more than 2^8, so O is rescaled rarely (by
 //               the same thread, in TMEM).  P (bf16 pairs) overwrites half
 //               of its S columns.  After the tile's last PV the group reads O,
@@ -250,8 +251,9 @@ __device__ __forceinline__ SeqBase seq_check(const PrefillParams& p, const int (
 // Pair pe of a sequence, counted from its end, holds query tiles T-2-2pe (A)
 // and T-1-2pe (B), T = ceil(Lq/128): the last tiles, which see the most keys,
 // pair up, and a sequence with an odd tile count leaves tile 0 alone (it sees
-// one K/V tile).  Both tiles run the same K/V steps (tile A's step past its
-// diagonal is fully masked), so the two softmax groups alternate to the end.
+// one K/V tile).  Tile B sees the most keys; tile A stops at its own last
+// visible K/V tile (one before B's when the query and key lengths match) and
+// releases the stages it does not read.
 __device__ __forceinline__ void pair_tiles(int Lq, int pe, int& tA, int& tB) {
   const int T = (Lq + kBM - 1) / kBM;
   tB = T - 1 - 2 * pe;
@@ -280,9 +282,8 @@ __device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase&
       s.n[x] = kmax < 0 ? 0 : min(kmax / kBN + 1, kv_tiles);
     }
   }
-  // tile B's rows see more keys than tile A's; both run B's K/V steps
+  // tile B's rows see at least as many keys as tile A's: the pair reads B's K/V tiles
   s.n_kv = max(s.n[0], s.n[1]);
-  if (s.rows[0] > 0) s.n[0] = s.n_kv;
   s.skip = s.rows[1] <= 0 || s.Lq <= p.route_decode;
   return s;
 }
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Seq sq = seq_derive(p, si, pair);
         const int nkv = sq.n_kv;
         if (nkv == 0) continue;
-        const int nx = xq ? sq.n[1] : sq.n[0];  // 0 or nkv (the tiles run in lockstep)
+        const int nx = xq ? sq.n[1] : sq.n[0];  // this tile's K/V tiles: 0..nkv
         if (nx == 0) {
           // this tile has no rows: release each K/V stage of the item once it is loaded
           for (int j = 0; j < nkv && ok; ++j) {
@@ -689,9 +690,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jt == nx - 1) ++oc;
           return true;
         };
+        // K/V tiles past this tile's last visible one (tile A only): released once loaded
+        auto pass = [&](int bar0, int full0, int jt) -> bool {
+          const int gg = g + jt, s = gg & 1;
+          if (!mbar_wait(bar(full0 + s), (gg >> 1) & 1, abort_flag)) return false;
+          mbar_arrive(bar(bar0 + s));
+          return true;
+        };
         for (int j = 0; j <= nkv && ok; ++j) {
-          if (j >= 1 && !issue_pv(j - 1)) ok = false;
-          if (ok && j < nkv && !issue_s(j)) ok = false;
+          if (j >= 1 && !(j - 1 < nx ? issue_pv(j - 1) : pass(kVEmpty0, kVFull0, j - 1))) ok = false;
+          if (ok && j < nkv && !(j < nx ? issue_s(j) : pass(kKEmpty0, kKFull0, j))) ok = false;
         }
         if (!ok) break;
         ++qc;
@@ -725,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // registers): the output offsets, the row limits and the loop counts.
       int rows, nkv, vis0, jm;
       int64_t obase, lse_idx;  // this tile's first output element; this row's lse index
-      bool turns;
+      int nturn;  // tiles taken in turn with the other group: the first n[0]
       {
         const Seq sq = seq_derive(p, si, x.pair);
         // (selects, not an indexed load: xq differs between warps but the arrays stay in registers)
@@ -740,10 +748,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         vis0 = min(row0 + r + sq.diag, sq.Lk - 1);
         const int first = row0 + sq.diag;  // limit of the tile's first row
         jm = min(first < kBN - 1 ? 0 : (first + 1) / kBN, sq.Lk / kBN);
-        // When both tiles have rows, the two groups take turns, tile by tile
-        // (A0, B0, A1, B1, ...): each softmax then has the SM's sub-partitions
-        // to itself, and while one group works the other tile's MMAs run.
-        turns = sq.rows[0] > 0;
+        // While both tiles have K/V tiles left, the two groups take turns, tile
+        // by tile (A0, B0, A1, B1, ...): each softmax then has the SM's
+        // sub-partitions to itself, and while one group works the other tile's
+        // MMAs run.  Tile B's tiles past A's last one run without turns.
+        nturn = sq.n[0];
       }
       if (rows <= 0) continue;
       // the offsets wait in shared memory while the tile loop runs (registers)
@@ -765,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nkv; ++j) {
         if (!mbar_wait(bar(kSFull0 + xq), sc & 1, abort_flag)) { ok = false; break; }
         ++sc;
-        if (turns) {  // tile A waits for B's previous tile, tile B for A's current one
+        if (j < nturn) {  // tile A waits for B's previous tile, tile B for A's current one
           const int need = xq == 0 ? tc - 1 : tc;
           if (need >= 0 && !mbar_wait(bar(kTurn0 + xq), need & 1, abort_flag)) { ok = false; break; }
         }
@@ -835,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kPFull0 + xq));
-        if (turns) {
+        if (j < nturn) {
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kTurn0 + (xq ^ 1)));
           ++tc;
