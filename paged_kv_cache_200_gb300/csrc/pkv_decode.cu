@@ -732,13 +732,17 @@ struct SplitPlan {
 //    contexts: bf16 6.47 -> 6.64 TB/s, FP8 5.82 -> 5.88 TB/s against 8 waves of
 //    2 CTAs per SM).
 //  * Otherwise the lengths are mixed and unknown on the host: about 32 CTAs
-//    per SM at the longest length, which leaves the short sequences one CTA.
+//    per SM at the longest length, which leaves the short sequences one CTA;
+//    16 when each item carries two row blocks (multi-query items of more than
+//    8 (query, head) rows), whose CTAs do twice the work per position (64
+//    sequences x 4 queries: 0.418 -> 0.399 ms).
 constexpr int64_t kCtaOverheadPos = 96;  // prologue + merge of one CTA, in positions of streaming time
 constexpr int64_t kCtasPerSmMixed = 32;
 
 int resident_ctas(int cache_dtype) { return cache_dtype == PKV_BF16 ? kResidentBf16 : kResidentCoded; }
 
-SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seqlen_k, int cache_dtype) {
+SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seqlen_k, int cache_dtype,
+                     int row_blocks) {
   SplitPlan pl{64, 1, 0};
   if (batch <= 0 || max_seqlen_k <= 0) return pl;
   const int64_t units = (int64_t)batch * num_kv_heads;
@@ -770,7 +774,7 @@ SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, i
       if (cn == 512) break;  // every larger n gives the same split
     }
   } else {
-    const int64_t target = sms * kCtasPerSmMixed;
+    const int64_t target = sms * kCtasPerSmMixed / (row_blocks > 1 ? 2 : 1);
     c = clamp_split((L * units + target - 1) / target);
   }
   pl.split_tokens = (int)c;
@@ -873,8 +877,8 @@ extern "C" size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_hea
                                                   int32_t head_dim, int32_t max_seqlen_k) {
   if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seqlen_k <= 0) return 0;
   // enough for every cache element type (their plans differ in CTAs per SM)
-  const size_t a = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_BF16).workspace;
-  const size_t b = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_INT8).workspace;
+  const size_t a = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_BF16, 1).workspace;
+  const size_t b = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_INT8, 1).workspace;
   return a > b ? a : b;
 }
 
@@ -918,7 +922,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
       (reinterpret_cast<uintptr_t>(out) & 7u))
     return PKV_ERR_INVALID_ARG;
   const int mlen = max_seqlen_k > 0 ? max_seqlen_k : 1;
-  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, mlen, cache_dtype);
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, mlen, cache_dtype, 1);
   if (pl.workspace > 0 && (workspace == nullptr || workspace_bytes < pl.workspace ||
                            (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
@@ -1015,7 +1019,8 @@ namespace pkv {
 size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
                                int cache_dtype, int multi_q) {
   if (batch <= 0 || items <= 0 || max_len_k <= 0) return 0;
-  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k, cache_dtype);
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k, cache_dtype,
+                                  multi_query_row_blocks(multi_q, num_heads / num_kv_heads));
   if (pl.max_splits <= 1) return 0;
   const size_t rows = (size_t)items * (multi_q > 0 ? multi_q : 1) * num_heads * pl.max_splits;
   return rows * head_dim * sizeof(float) + ((rows * sizeof(float) + 255) / 256) * 256;
@@ -1034,7 +1039,8 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          int32_t* err_flag, int32_t multi_q, bool after_primary, cudaStream_t st) {
   const bool fp8 = cache_dtype != PKV_BF16;  // one-byte codes
   if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
-  SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype);
+  SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype,
+                            multi_query_row_blocks(multi_q, num_heads / num_kv_heads));
   pl.after_primary = after_primary;
   if (varlen_decode_workspace(batch, item_bound, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1,
                               cache_dtype, multi_q) > workspace_bytes)
@@ -1074,7 +1080,8 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
     // (query, head) rows of a sequence in blocks of 8 on the MMAs' N side
     const int rows = multi_q * p.group;
     if (rows > kMultiRows) return PKV_ERR_UNSUPPORTED;
-    if (rows > 8) return dispatch_decode_rows<2>(cache_dtype, head_dim, p, item_bound, pl, ns, st);
+    if (multi_query_row_blocks(multi_q, p.group) > 1)
+      return dispatch_decode_rows<2>(cache_dtype, head_dim, p, item_bound, pl, ns, st);
     return dispatch_decode_rows<1>(cache_dtype, head_dim, p, item_bound, pl, ns, st);
   }
   return dispatch_decode(cache_dtype, head_dim, p, item_bound, pl, ns, st);

@@ -42,6 +42,9 @@ constexpr int kMultiRows = 16;
 inline bool multi_query_items(int max_len_q, int group) {
   return max_len_q >= 1 && max_len_q <= kRouteMaxQ && max_len_q * group <= kMultiRows;
 }
+// Blocks of 8 (query, head) rows on the decode MMAs' N side for items of
+// multi_q queries (multi_q = 0: one query row per item).
+inline int multi_query_row_blocks(int multi_q, int group) { return multi_q > 0 && multi_q * group > 8 ? 2 : 1; }
 
 // Decode kernels serving the routed query rows of a paged varlen batch
 // (at most item_bound items; splits planned for `batch` sequences).  multi_q:
