@@ -236,21 +236,48 @@ def time_decode_steps(step, steps, warmup):
 
 
 def time_e2e(step, steps, warmup):
-    """Per step: H2D of the step's inputs from pinned memory, write + decode, D2H of the output."""
+    """Per step: one H2D copy of the step's inputs (packed in one pinned host buffer, each tensor at a
+    256-byte boundary), write + decode on device views of that buffer, and a D2H read of the step's
+    output.  The read runs on a copy stream (two output buffers), so it overlaps the next step's
+    kernels, which do not depend on it; every read has completed when the timed region ends."""
     wl = step.wl
-    host = {name: getattr(wl, name).cpu().pin_memory() for name in
-            ("q", "k_new", "v_new", "slot_mapping", "cache_seqlens", "block_table")}
-    dev = {name: torch.empty_like(getattr(wl, name)) for name in host}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    names = ("q", "k_new", "v_new", "slot_mapping", "cache_seqlens", "block_table")
+    srcs = [getattr(wl, name).contiguous() for name in names]
+    offs, total = [], 0
+    for t in srcs:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=wl.q.device)
+    dev = {}
+    for name, t, off in zip(names, srcs, offs):
+        nb = t.numel() * t.element_size()
+        host_buf[off:off + nb].copy_(t.cpu().view(-1).view(torch.uint8))
+        dev[name] = dev_buf[off:off + nb].view(t.dtype).view(t.shape)
+    out_dev = [step.out, torch.empty_like(step.out)]
+    out_host = [torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True) for _ in range(2)]
+    h2d = total
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    cur = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=wl.q.device)
+    decoded = [torch.cuda.Event() for _ in range(2)]
+    read = [torch.cuda.Event() for _ in range(2)]
+    count = [0]
 
     def one():
-        for name, t in host.items():
-            dev[name].copy_(t, non_blocking=True)
+        i = count[0]
+        b = i & 1
+        dev_buf.copy_(host_buf, non_blocking=True)
         step.write(dev["k_new"], dev["v_new"], dev["slot_mapping"])
-        step.decode(dev["q"], dev["cache_seqlens"], dev["block_table"])
-        out_host.copy_(step.out, non_blocking=True)
+        if i >= 2:
+            cur.wait_event(read[b])  # the read of two steps back has left this output buffer
+        step.decode(dev["q"], dev["cache_seqlens"], dev["block_table"], out=out_dev[b])
+        decoded[b].record(cur)
+        side.wait_event(decoded[b])
+        with torch.cuda.stream(side):
+            out_host[b].copy_(out_dev[b], non_blocking=True)
+        read[b].record(side)
+        count[0] += 1
 
     for _ in range(warmup):
         one()
@@ -259,6 +286,7 @@ def time_e2e(step, steps, warmup):
     start.record()
     for _ in range(steps):
         one()
+    cur.wait_stream(side)  # every output read is inside the timed region
     end.record()
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps, h2d, d2h
@@ -861,6 +889,20 @@ def ncu_case(args):
         torch.cuda.synchronize()
         log("ncu case done: prefill")
         return
+    if args.ncu_case == "multi_query":
+        # the speculative-verification workload itself (64 seqs x 4 new tokens, 1K..16K cached): 2.2 GB of K/V
+        rng = np.random.default_rng(1008)
+        prefix = rng.integers(1024, 16384, size=64, endpoint=True)
+        wl = W.make_varlen_paged(np.full(64, 4), prefix, 32, 8, 128, 16, seed=1009, device="cuda")
+        sh = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+        pkv.kv_cache_write(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+        for _ in range(5):
+            pkv.paged_attn_varlen(wl.q, wl.k_cache.view(sh), wl.v_cache.view(sh), wl.cu_seqlens_q,
+                                  wl.cu_seqlens_k, wl.max_len_q, wl.max_len_k, block_table=wl.block_table,
+                                  scale=wl.scale)
+        torch.cuda.synchronize()
+        log("ncu case done: multi_query")
+        return
     rng = np.random.default_rng(77)
     dt = {"decode_fp8": "fp8_e4m3", "decode_int8": "int8"}.get(args.ncu_case, "bf16")
     # 64 sequences of 1K..4K cached tokens: ~0.65 GB of bf16 K/V, larger than L2
@@ -886,7 +928,8 @@ def main():
                     help="seconds of the all-cores oracle timing (0: skip)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "decode_int8", "prefill"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "decode_int8", "prefill", "multi_query"],
+                    default=None,
                     help="run a small case for an ncu capture and exit")
     args = ap.parse_args()
     if args.ncu_case:
