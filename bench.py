@@ -550,7 +550,7 @@ def extra_workloads(pkv, W, device, pk, args):
     pre = prefill_workload(pkv, W, device, pk, args)
     also.update(pre)
     for key in ("varlen_prefill_packed", "varlen_prefill_paged", "varlen_prefill_paged_direct",
-                "varlen_prefill_paged_fp8", "varlen_prefill_paged_int8"):
+                "varlen_prefill_paged_fp8", "varlen_prefill_paged_fp8_direct"):
         if key in pre:
             e = pre[key]
             legs[key] = {"ms": _r(e["ms"]), "TFLOP_s": _r(e["TFLOP_per_s"]), "frac": _r(e["frac_of_bf16_peak"])}
@@ -795,6 +795,12 @@ def prefill_workload(pkv, W, device, pk, args):
     tf = flops / (ms * 1e-3) / 1e12
     res["varlen_prefill_paged_fp8"] = {
         "workload": "same, FP8 E4M3 cache (per-tensor scales; write quantises, prefill widens the gathered codes)",
+        "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "iters": iters}
+    ms = paged_leg(False, "fp8_e4m3", wf)
+    tf = flops / (ms * 1e-3) / 1e12
+    res["varlen_prefill_paged_fp8_direct"] = {
+        "workload": "same FP8 E4M3 cache, no gather bound: the tile loop reads the one-byte pages and widens them "
+                    "to f16 in shared memory (f16 MMAs)",
         "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"], "iters": iters}
     del wp, wf, kc4, vc4, out
     torch.cuda.empty_cache()

@@ -50,6 +50,8 @@ constexpr int kBM = 128;          // query rows per query tile
 constexpr int kPairRows = 2 * kBM;  // query rows per work item (tiles A and B)
 constexpr int kBN = 128;          // keys per K/V tile
 constexpr int kThreads = 352;     // producer warp, 2 MMA warps, 2 softmax warp groups
+constexpr int kThreadsCoded = 384;  // one-byte caches: + a widening warp
+constexpr int kWidenWarp = 11;
 constexpr int kSoftmaxWarp0 = 3;  // first softmax warp (tile A: warps 3..6, tile B: 7..10)
 constexpr int kGroupThreads = 128;  // a softmax warp group: one thread per row of its tile
 constexpr uint32_t kTmemCols = 512;
@@ -105,10 +107,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 x bf16 -> f32, A K-major.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
+// Instruction descriptor, kind::f16: bf16 x bf16 (or f16 x f16) -> f32, A K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn_major, bool f16 = false) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -170,7 +172,7 @@ struct Smem {
   static constexpr int kK = kQ + 2 * kTileBytes;        // 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;        // 2 stages
   static constexpr int kBar = kV + 2 * kTileBytes;
-  static constexpr int kNumBars = 32;
+  static constexpr int kNumBars = 40;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
   static constexpr int kRingData = kMisc + 16;          // 4 ring slots x 8 ints (item, q0, Lq, k0, Lk)
   static constexpr int kEpi = kRingData + 4 * 32;       // per softmax thread: output and lse offsets, rows (32 B)
@@ -197,16 +199,20 @@ enum Bar {
   kODone0 = 16,      // +X: the item's last PV_X done (MMA -> softmax X epilogue)
   kOFree0 = 18,      // +X: softmax X has read O_X (128 arrivals -> MMA, before the next item's first PV_X)
   kRingFull0 = 20,   // +slot (4): a work item index published by the producer
-  kRingEmpty0 = 24,  // +slot (4): both MMA threads and the 8 softmax warps have read the slot
+  kRingEmpty0 = 24,  // +slot (4): both MMA threads, the 8 softmax warps (and the widening warp) have read it
   kDrain0 = 28,      // +X: every MMA of issuer X done (end of the kernel)
   kTurn0 = 30,       // +X: the other softmax group finished its tile; group X may start its next one
-  kBarCount = 32
+  kQReady0 = 32,     // +X: one-byte caches: Q converted to f16 in place (producer -> MMA)
+  kKReady0 = 34,     // +stage: one-byte caches: K widened to f16 in place (producer -> MMA)
+  kVReady0 = 36,     // +stage: one-byte caches: V widened to f16 in place (producer -> MMA)
+  kBarCount = 38
 };
 static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kKEmpty0 == kKFull0 + 2 &&
                   kVFull0 == kKEmpty0 + 2 && kVEmpty0 == kVFull0 + 2 && kSFull0 == kVEmpty0 + 2 &&
                   kPFull0 == kSFull0 + 2 && kODone0 == kPFull0 + 2 && kOFree0 == kODone0 + 2 &&
                   kRingFull0 == kOFree0 + 2 && kRingEmpty0 == kRingFull0 + kRing && kDrain0 == kRingEmpty0 + kRing &&
-                  kTurn0 == kDrain0 + 2 && kBarCount == kTurn0 + 2,
+                  kTurn0 == kDrain0 + 2 && kQReady0 == kTurn0 + 2 && kKReady0 == kQReady0 + 2 &&
+                  kVReady0 == kKReady0 + 2 && kBarCount == kVReady0 + 2,
               "mbarrier index ranges must not overlap");
 static_assert(Smem<128>::kNumBars >= kBarCount && Smem<64>::kNumBars >= kBarCount, "too few mbarrier slots");
 
@@ -305,14 +311,98 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int it) {
   return x;
 }
 
+// ---------------------------------------------------------------------------
+// one-byte caches read by the tile loop: widening to f16 in shared memory
+// ---------------------------------------------------------------------------
+// With an FP8 or INT8 cache the tile loop runs f16 x f16 MMAs: every E4M3 code
+// and every INT8 code (-127..127) is exactly an f16 value, so the producer warp
+// widens each landed K/V tile in place, and converts each Q tile from bf16 to
+// f16 once per item (exact for |q| in f16's normal range; |q| > 65504 would
+// become infinite).  The per-tensor scales act as in the gathered path: k_scale
+// joins the logit scale and v_scale the output factor.
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// A [128 rows x 128] bf16 tile (two 128-byte atoms), converted to f16 in
+// place, 16 bytes per lane and access (elementwise: the swizzle does not matter).
+__device__ __forceinline__ void widen_q_f16(uint8_t* tile, int lane) {
+  uint4* v = reinterpret_cast<uint4*>(tile);
+#pragma unroll 4
+  for (int i = lane; i < 2 * kBM * 8; i += 32) {
+    uint4 w = v[i];
+    w.x = bf16x2_to_f16x2(w.x);
+    w.y = bf16x2_to_f16x2(w.y);
+    w.z = bf16x2_to_f16x2(w.z);
+    w.w = bf16x2_to_f16x2(w.w);
+    v[i] = w;
+  }
+}
+
+// Codes 4k..4k+1 (lo) or 4k+2..4k+3 (hi) of a 32-bit word of one-byte codes -> f16x2.
+template <int kCode>
+__device__ __forceinline__ uint32_t code2_to_f16x2(uint32_t w, bool hi) {
+  if constexpr (kCode == 1) {
+    return hi ? e4m3x2_hi_to_f16x2(w) : e4m3x2_lo_to_f16x2(w);
+  } else {
+    // INT8: with its sign bit flipped, code c is the low mantissa byte of the
+    // f16 1152 + c (exponent byte 0x64); 1152 is then taken off exactly
+    const uint32_t b = prmt(w ^ 0x80808080u, 0x64646464u, hi ? 0x4342u : 0x4140u);
+    __half2 h = *reinterpret_cast<const __half2*>(&b);
+    h = __hsub2(h, __half2half2(__ushort_as_half((unsigned short)0x6480u)));  // 1152
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// The one-byte [128 rows x 128 B] tile that TMA landed (128-byte swizzle) in
+// the second half of a K/V stage, widened in place to the f16 tile the MMAs
+// read (two 128-byte atoms of 128 rows, 128-byte swizzle).  Lane l takes rows
+// l, l+32, l+64, l+96 and reads a whole row before writing: the one-byte row r
+// occupies exactly the bytes of f16 row r of the second atom, and no other lane
+// reads or writes them.
+template <int kCode>
+__device__ __forceinline__ void widen_kv_f16(uint8_t* stage, int lane) {
+  const uint8_t* src = stage + kBM * 128;
+#pragma unroll 1
+  for (int i = 0; i < kBN / 32; ++i) {
+    const int r = lane + 32 * i;
+    const int sw = r & 7;
+    uint4 in[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) in[c] = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ sw) << 4));
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {  // codes 16c..16c+15 -> f16 chunks 2c, 2c+1 of atom c / 4
+      const uint32_t w[4] = {in[c].x, in[c].y, in[c].z, in[c].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        h[2 * k] = code2_to_f16x2<kCode>(w[k], false);
+        h[2 * k + 1] = code2_to_f16x2<kCode>(w[k], true);
+      }
+      uint8_t* row = stage + (c >> 2) * (kBM * 128) + r * 128;
+      *reinterpret_cast<uint4*>(row + ((((2 * c) & 7) ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(row + ((((2 * c + 1) & 7) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
 // Persistent kernel: one CTA per SM takes work items from the global counter.
 // All roles walk the same published list and keep running counters (items,
 // tiles) so the barriers' phases continue across items.
-template <int D, bool kPaged>
-__global__ void __launch_bounds__(kThreads, 1)
+// kCode: 0 bf16 K/V (packed or paged); 1 E4M3, 2 INT8 codes (paged, d128),
+// widened to f16 in shared memory by the producer warp.
+template <int D, bool kPaged, int kCode>
+__global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
     varlen_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = Smem<D>;
+  constexpr bool kCoded = kCode != 0;
+  static_assert(!kCoded || (kPaged && D == 128), "one-byte K/V tiles: paged, head dim 128");
+  // the MMA threads wait for a landed tile (bf16) or for its widening (one-byte codes)
+  constexpr int kQWait0 = kCoded ? kQReady0 : kQFull0;
+  constexpr int kKWait0 = kCoded ? kKReady0 : kKFull0;
+  constexpr int kVWait0 = kCoded ? kVReady0 : kVFull0;
   // The decode kernels of the same call (the routed query rows) may start as
   // soon as SMs free up: they read nothing this kernel writes.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -344,9 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kDrain0 + 1), 1);
     mbar_init(bar(kTurn0), kGroupThreads / 32);
     mbar_init(bar(kTurn0 + 1), kGroupThreads / 32);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(kQReady0 + x), 1);
+      mbar_init(bar(kKReady0 + x), 1);
+      mbar_init(bar(kVReady0 + x), 1);
+    }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(bar(kRingFull0 + r), 1);
-      mbar_init(bar(kRingEmpty0 + r), 2 + 2 * kGroupThreads / 32);
+      mbar_init(bar(kRingEmpty0 + r), 2 + 2 * kGroupThreads / 32 + (kCoded ? 1 : 0));
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -482,9 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int br = kPaged ? p.box_rows : kBN;
       const int npages = kBN / br;
       // Paged tiles: lane (page pg, head-dim atom at) issues one box; at most
-      // 8 pages x 2 atoms, as block sizes are multiples of 16.
+      // 8 pages x 2 atoms, as block sizes are multiples of 16.  A one-byte
+      // row (128 codes) is one 128-byte box row: one box per page, landing in
+      // the second half of the stage.
+      constexpr int kLoadAtoms = kCoded ? 1 : L::kAtoms;
       const int pg = lane % npages, at = lane / npages;
-      const bool box_lane = lane < npages * L::kAtoms;
+      const bool box_lane = lane < npages * kLoadAtoms;
       // Block id of this lane's page of local tile j (0 past the keys).  The
       // table is read two tiles before the id is used, so the load's latency
       // overlaps the waits in between; tile_slot checks and converts it.
@@ -531,10 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < npages; ++q)
             if (key0 + q * br < sq.Lk) ++loaded;
           // one lane per (page, atom) issues that box, after the byte count is registered
-          if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * L::kAtoms));
+          if (lane == 0) mbar_expect_tx(full, (uint32_t)(loaded * br * 128 * kLoadAtoms));
           __syncwarp();
           if (box_lane && pg < loaded)
-            tma_load_3d(dst + at * L::kAtomBytes + pg * br * 128, map, at * 64, kvh, my_slot, full);
+            tma_load_3d(dst + (kCoded ? L::kAtomBytes : at * L::kAtomBytes) + pg * br * 128, map,
+                        kCoded ? 0 : at * 64, kvh, my_slot, full);
           __syncwarp();
         }
         (t ? last_v : last_k)[s] = u;
@@ -599,8 +698,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stages are released by one arrival of each thread.  Lanes 1..31 idle.
     const int xq = warp - 1;
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false);
-      constexpr uint32_t kIdescPV = make_idesc(kBM, D, true);
+      constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, false, kCoded);
+      constexpr uint32_t kIdescPV = make_idesc(kBM, D, true, kCoded);
       bool ok = true, issued = false;
       int g = 0;   // K/V tiles consumed
       int qc = 0;  // items whose tile attends keys (Q buffer uses)
@@ -620,15 +719,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nkv == 0) continue;
         const int nx = xq ? sq.n[1] : sq.n[0];  // this tile's K/V tiles: 0..nkv
         if (nx == 0) {
-          // this tile has no rows: release each K/V stage of the item once it is loaded
+          // this tile has no rows: release each K/V stage of the item once it is
+          // loaded (K and V each on its own: with one-byte caches V(j) is widened
+          // only after the producer has seen K(j-1) released)
           for (int j = 0; j < nkv && ok; ++j) {
             const int gg = g + j, s = gg & 1;
-            if (!mbar_wait(bar(kKFull0 + s), (gg >> 1) & 1, abort_flag) ||
-                !mbar_wait(bar(kVFull0 + s), (gg >> 1) & 1, abort_flag)) {
+            if (!mbar_wait(bar(kKWait0 + s), (gg >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
             mbar_arrive(bar(kKEmpty0 + s));
+            if (!mbar_wait(bar(kVWait0 + s), (gg >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
             mbar_arrive(bar(kVEmpty0 + s));
           }
           g += nkv;
@@ -640,8 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // threads' reads of S(j-1) were ordered before that PV by its P wait.
         auto issue_s = [&](int j) -> bool {
           const int gg = g + j, s = gg & 1;
-          if (!mbar_wait(bar(kKFull0 + s), (gg >> 1) & 1, abort_flag)) return false;
-          if (j == 0 && !mbar_wait(bar(kQFull0 + xq), qc & 1, abort_flag)) return false;
+          if (!mbar_wait(bar(kKWait0 + s), (gg >> 1) & 1, abort_flag)) return false;
+          if (j == 0 && !mbar_wait(bar(kQWait0 + xq), qc & 1, abort_flag)) return false;
+          tc_fence_after();  // (one-byte caches: the producer's widening writes are ordered before the MMAs)
           const uint64_t qdesc = sw128_desc(sbase + L::kQ + xq * L::kTileBytes, 16, 1024);
           const uint64_t kdesc = sw128_desc(sbase + L::kK + s * L::kTileBytes, 16, 1024);
 #pragma unroll
@@ -658,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O += P(jt) V(jt)
         auto issue_pv = [&](int jt) -> bool {
           const int gg = g + jt, s = gg & 1;
-          if (!mbar_wait(bar(kVFull0 + s), (gg >> 1) & 1, abort_flag)) return false;
+          if (!mbar_wait(bar(kVWait0 + s), (gg >> 1) & 1, abort_flag)) return false;
           // keys at or beyond Lk (only in a sequence's last K/V tile): zero their
           // V rows, so that stale or foreign data never meets P = 0.  Both MMA
           // threads do this, each before its own PV; they only ever write zeros.
@@ -698,8 +803,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         for (int j = 0; j <= nkv && ok; ++j) {
-          if (j >= 1 && !(j - 1 < nx ? issue_pv(j - 1) : pass(kVEmpty0, kVFull0, j - 1))) ok = false;
-          if (ok && j < nkv && !(j < nx ? issue_s(j) : pass(kKEmpty0, kKFull0, j))) ok = false;
+          if (j >= 1 && !(j - 1 < nx ? issue_pv(j - 1) : pass(kVEmpty0, kVWait0, j - 1))) ok = false;
+          if (ok && j < nkv && !(j < nx ? issue_s(j) : pass(kKEmpty0, kKWait0, j))) ok = false;
         }
         if (!ok) break;
         ++qc;
@@ -714,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();  // the warp reconverges before the CTA barrier below
-  } else {
+  } else if (!kCoded || warp < kWidenWarp) {
     // ------------------------------------------------------------------ softmax warps
     const int xq = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warp group
     const int quarter = warp & 3;       // TMEM lanes this warp may access
@@ -818,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(pk[k]), __uint_as_float(pk[k + 1])), c2, nm2), x0, x1);
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             sum2[(k >> 1) & 1] = fadd2(sum2[(k >> 1) & 1], f32x2_pack(p0, p1));
-            pk[k >> 1] = pack_bf16x2(p0, p1);
+            pk[k >> 1] = kCoded ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
           PKV_TMEM_ST32(tS(xq) + lane_off + 64 * h, pk);
         }
@@ -897,6 +1002,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) fail();
     tc_fence_before();
+  } else {
+    // ------------------------------------------------------------------ widening warp
+    // One-byte caches: each landed Q, K and V tile of the published items, in
+    // the order the MMA threads use them, is widened in place to f16 and
+    // released to them (the whole warp converts; lane 0 signals).
+    if constexpr (kCoded) {
+      bool ok = true;
+      int g = 0;                // K/V tiles
+      int qc[2] = {0, 0};       // Q loads per tile slot
+      auto widen = [&](int full, uint32_t parity, int ready, uint8_t* buf, bool q) -> bool {
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(bar(full), parity, abort_flag);
+        if (!__shfl_sync(0xffffffffu, wok, 0)) return false;
+        mbar_wait(bar(full), parity, abort_flag);  // every lane acquires the landed bytes (complete)
+        if (q)
+          widen_q_f16(buf, lane);
+        else
+          widen_kv_f16<kCode>(buf, lane);
+        fence_proxy_async_smem();  // the generic writes, before the tensor core reads them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ready));
+        return true;
+      };
+      for (int u = 0; ok; ++u) {
+        SeqBase si;
+        Item x;
+        if (__any_sync(0xffffffffu, ring_get(u, si, x) < 0)) break;  // (every lane reads the entry)
+        const Seq sq = seq_derive(p, si, x.pair);
+        if (sq.n_kv == 0) continue;
+        for (int xq = 0; xq < 2 && ok; ++xq) {
+          if (sq.n[xq] == 0) continue;
+          if (!widen(kQFull0 + xq, (uint32_t)qc[xq] & 1u, kQReady0 + xq, smem + L::kQ + xq * L::kTileBytes, true))
+            ok = false;
+          ++qc[xq];
+        }
+        for (int j = 0; j < sq.n_kv && ok; ++j) {
+          const int gg = g + j, s = gg & 1;
+          const uint32_t par = (uint32_t)(gg >> 1) & 1u;
+          if (!widen(kKFull0 + s, par, kKReady0 + s, smem + L::kK + s * L::kTileBytes, false) ||
+              !widen(kVFull0 + s, par, kVReady0 + s, smem + L::kV + s * L::kTileBytes, false))
+            ok = false;
+        }
+        g += sq.n_kv;
+      }
+      if (!ok && lane == 0) fail();
+      __syncwarp();
+    }
   }
 
   __syncthreads();
@@ -1139,10 +1291,10 @@ VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_
   return w;
 }
 
-template <int D, bool kPaged>
+template <int D, bool kPaged, int kCode = 0>
 int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillParams& p,
                    int batch, cudaStream_t st) {
-  auto kern = varlen_prefill_kernel<D, kPaged>;
+  auto kern = varlen_prefill_kernel<D, kPaged, kCode>;
   const int smem = Smem<D>::kAlloc;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -1155,7 +1307,7 @@ int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
   }
   const int64_t items = (int64_t)p.n_pairs * batch * p.num_heads;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
-  kern<<<grid, kThreads, smem, st>>>(mq, mk, mv, p);
+  kern<<<grid, kCode ? kThreadsCoded : kThreads, smem, st>>>(mq, mk, mv, p);
   return launch_status();
 }
 
@@ -1204,8 +1356,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   // no sequence has more queries than the routing bound: every query row goes
   // to the decode kernels and no prefill tile runs
   const bool all_routed = route && max_len_q <= kRouteMaxQ;
-  // the prefill tiles read a one-byte cache only through the gather (paged mode, total_k > 0)
-  if (fp8 && !all_routed && (!paged || total_k <= 0)) return PKV_ERR_UNSUPPORTED;
+  // the prefill tiles read a one-byte cache in paged mode only: through the
+  // gather (total_k > 0) or, without a gather bound, widened in the tile loop
+  // (head dim 128)
+  if (fp8 && !all_routed && (!paged || (total_k <= 0 && head_dim != 128))) return PKV_ERR_UNSUPPORTED;
   if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
     return PKV_ERR_INVALID_ARG;
   if (!causal) return PKV_ERR_UNSUPPORTED;
@@ -1236,6 +1390,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   // packed offsets cu_g in place of cu_seqlens_k (same lengths for the
   // gathered sequences, zero for the ones the decode kernels take).
   const bool packed_tiles = !paged || gather;
+  const bool coded_tiles = fp8 && !packed_tiles;  // one-byte pages widened by the tile loop
   const void* kt = gather ? static_cast<const void*>(wsb + wl.gk_off) : k;
   const void* vt = gather ? static_cast<const void*>(wsb + wl.gv_off) : v;
   CUtensorMap mq, mk, mv;
@@ -1243,9 +1398,11 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   const int kv_box = packed_tiles ? 128 : (block_size < 128 ? block_size : 128);
   // [rows, heads, dim] bf16, boxes of 64 elements x 1 head x box rows, 128-byte swizzle
   // (not needed when every query row goes to the decode kernels)
+  // (one-byte pages: boxes of 128 codes, one 128-byte row per position)
+  const int kv_elt = coded_tiles ? 1 : 2, kv_inner = coded_tiles ? 128 : 64;
   if (!all_routed && (!make_tmap_3d(&mq, q, 2, total_q, num_heads, head_dim, 64, 128, 128) ||
-                      !make_tmap_3d(&mk, kt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128) ||
-                      !make_tmap_3d(&mv, vt, 2, kv_rows, num_kv_heads, head_dim, 64, kv_box, 128)))
+                      !make_tmap_3d(&mk, kt, kv_elt, kv_rows, num_kv_heads, head_dim, kv_inner, kv_box, 128) ||
+                      !make_tmap_3d(&mv, vt, kv_elt, kv_rows, num_kv_heads, head_dim, kv_inner, kv_box, 128)))
     return PKV_ERR_CUDA;
 
   PrefillParams p{};
@@ -1303,8 +1460,10 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   if (all_routed)
     rc = launch_status();
   else if (head_dim == 128)
-    rc = packed_tiles ? launch_prefill<128, false>(mq, mk, mv, p, batch, st)
-                      : launch_prefill<128, true>(mq, mk, mv, p, batch, st);
+    rc = packed_tiles                     ? launch_prefill<128, false>(mq, mk, mv, p, batch, st)
+         : !coded_tiles                   ? launch_prefill<128, true>(mq, mk, mv, p, batch, st)
+         : kv_dtype == PKV_FP8_E4M3       ? launch_prefill<128, true, 1>(mq, mk, mv, p, batch, st)
+                                          : launch_prefill<128, true, 2>(mq, mk, mv, p, batch, st);
   else
     rc = packed_tiles ? launch_prefill<64, false>(mq, mk, mv, p, batch, st)
                       : launch_prefill<64, true>(mq, mk, mv, p, batch, st);

@@ -107,26 +107,28 @@ def test_one_byte_caches_need_valid_inverse_scales():
     assert append(0, 0.0, float("nan")) == 0  # bf16 cache: the scales are not used
 
 
-def test_one_byte_varlen_needs_the_gather_only_when_prefill_tiles_run():
-    """A one-byte (FP8 / INT8) cache in a varlen call: packed K/V is refused; in paged mode
-    without a gather bound it is refused when some sequence has more than 8 queries (the
-    prefill tiles would read it), and accepted when every query row goes to the decode
-    kernels (here the call then fails on its null pointers instead, status 1, before any
-    launch)."""
+def test_one_byte_varlen_modes():
+    """A one-byte (FP8 / INT8) cache in a varlen call: packed K/V is refused; in paged mode it is
+    accepted with a gather bound, without one when the tile loop can widen the pages itself (head
+    dim 128) or when every query row goes to the decode kernels, and refused otherwise (head dim
+    64 with prefill tiles and no gather bound).  Accepted calls then fail on their null pointers,
+    status 1, before any launch."""
     pkv = built_library()
     lib = pkv.lib()
     nul = ctypes.c_void_p(0)
     tbl = ctypes.c_void_p(4096)  # a non-null block table pointer (never dereferenced: refused first)
 
-    def varlen(dt, table, max_len_q, total_k=0):
+    def varlen(dt, table, max_len_q, total_k=0, D=128):
         return lib.pkv_paged_attn_varlen(nul, nul, nul, dt, nul, nul, 4, 16, total_k, max_len_q, 64, table, 8, 16,
-                                         64, 8, 2, 128, 0.1, 1, 0.5, 0.5, nul, nul, nul, 0, nul, nul)
+                                         64, 8, 2, D, 0.1, 1, 0.5, 0.5, nul, nul, nul, 0, nul, nul)
 
     for dt in (2, 3):
-        assert varlen(dt, nul, 4) == 2          # packed K/V in one-byte codes
-        assert varlen(dt, tbl, 40) == 2         # prefill tiles without a gather bound
-        assert varlen(dt, tbl, 4) == 1          # all rows routed: accepted (then: null pointers)
-        assert varlen(dt, tbl, 40, 4096) == 1   # with a gather bound: accepted (then: null pointers)
+        assert varlen(dt, nul, 4) == 2            # packed K/V in one-byte codes
+        assert varlen(dt, tbl, 40) == 1           # prefill tiles widen the pages (d128): accepted
+        assert varlen(dt, tbl, 40, D=64) == 2     # d64 prefill tiles need the gather bound
+        assert varlen(dt, tbl, 40, 4096, D=64) == 1
+        assert varlen(dt, tbl, 4, D=64) == 1      # all rows routed: accepted (then: null pointers)
+        assert varlen(dt, tbl, 40, 4096) == 1     # with a gather bound: accepted (then: null pointers)
 
 
 def test_copy_blocks_host_validation():

@@ -263,6 +263,49 @@ def test_varlen_paged_fp8(pkv, case):
     assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"fp8 lse {case}")
 
 
+# One-byte pages read by the tile loop itself (no gather bound): head dim 128 only.
+CODED_DIRECT = [c for c in FP8_PAGED if c[4] == 128] + [
+    ([1, 2, 127, 128, 129, 300], [0, 5, 0, 700, 1, 2], 8, 1, 128, 32),   # ragged tails, odd group
+    ([260], [0], 64, 8, 128, 128),                                       # one page per tile
+]
+
+
+@pytest.mark.parametrize("dt", ["fp8_e4m3", "int8"])
+@pytest.mark.parametrize("case", CODED_DIRECT, ids=[f"bs{c[5]}_{c[2]}q{c[3]}kv_{i}" for i, c in
+                                                    enumerate(CODED_DIRECT)])
+def test_varlen_paged_one_byte_direct(pkv, case, dt):
+    """FP8 / INT8 pages widened to f16 in shared memory by the tile loop, against the oracle
+    over the same codes; and equal, within the same tolerance, to the gathered path."""
+    q_lens, prefix, Hq, Hkv, D, bs = case
+    wl = W.to_fp8_cache(W.make_varlen_paged(q_lens, prefix, Hq, Hkv, D, bs, seed=sum(q_lens) + 11, device="cuda",
+                                            extra_blocks=2), dt)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=False)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=bs,
+                                       kv_dtype=dt, k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+    assert_close(f64(out), ref, FP8_ATOL, FP8_RTOL, f"{dt} direct {case}")
+    assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"{dt} direct lse {case}")
+    out_g, _ = _paged(pkv, wl, kc, vc, gather=True)
+    assert_close(f64(out), f64(out_g), FP8_ATOL, FP8_RTOL, f"{dt} direct vs gathered {case}")
+
+
+@pytest.mark.parametrize("dt", ["fp8_e4m3", "int8"])
+def test_varlen_prefill_full_size_paged_one_byte_direct(pkv, dt):
+    wl = W.to_fp8_cache(W.varlen_prefill(device="cuda", paged=True), dt)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=False)
+    seqs = [int(np.argmax(wl.q_lens)), 3]
+    ks, vs, tsub = _sub_pool(wl, kc, vc, seqs)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), ks, vs, wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True, block_table=tsub,
+                                       block_size=wl.block_size, seqs=seqs, kv_dtype=dt,
+                                       k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+    rows = _rows_of(wl, seqs)
+    assert_close(f64(out)[rows], ref[rows], FP8_ATOL, FP8_RTOL, f"prefill paged {dt} direct")
+
+
 def test_varlen_prefill_full_size_paged_fp8(pkv):
     wl = W.to_fp8_cache(W.varlen_prefill(device="cuda", paged=True))
     kc, vc = _write_new_tokens(pkv, wl)
@@ -313,13 +356,7 @@ def test_multi_query_decode_rows(pkv, dt, gather, chunk):
     if dt != "bf16":
         wl = W.to_fp8_cache(wl)
     kc, vc = _write_new_tokens(pkv, wl)
-    if dt != "bf16" and not gather and chunk:
-        # the longer chunk runs on the prefill tiles, which read a one-byte cache only
-        # through the gather: without a gather bound the call is refused before any launch
-        with pytest.raises(pkv.PkvError) as e:
-            _paged(pkv, wl, kc, vc, gather=False)
-        assert e.value.status == 2  # PKV_ERR_UNSUPPORTED
-        return
+    # (a one-byte cache without a gather bound: the longer chunk's tiles widen the pages themselves)
     out, lse = _paged(pkv, wl, kc, vc, gather=gather)
     kw = {} if dt == "bf16" else dict(kv_dtype="fp8_e4m3", k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
     ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
