@@ -263,9 +263,13 @@ PKV_API size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q, i
  *          (PKV_DEVERR_LENGTH).
  * kv_dtype: PKV_BF16; or, in paged mode, PKV_FP8_E4M3 or PKV_INT8, where a
  *          cached code c stands for c's value times k_scale (resp. v_scale).
- *          A one-byte cache needs total_k > 0 when some sequence has more
- *          queries than the routing bound below (its tiles read the gathered
- *          copy); otherwise the call returns PKV_ERR_UNSUPPORTED.
+ *          With total_k > 0 the tiles read a bf16 copy gathered into the
+ *          workspace; with total_k == 0 and head_dim 128 they read the pages
+ *          themselves, widen the codes to f16 in shared memory and run f16
+ *          MMAs, the query then also taken as f16 (|q| must stay below 65504);
+ *          with total_k == 0 and head_dim 64 (and some sequence with more
+ *          queries than the routing bound below) the call returns
+ *          PKV_ERR_UNSUPPORTED.
  * Supported: head_dim 64 or 128, causal != 0; paged block_size a multiple of 16
  * that divides 128 or is a multiple of 128.  All of q, k, v, out 16-byte aligned.
  * Routing (paged mode, num_heads/num_kv_heads <= 8): when no sequence has more

@@ -393,9 +393,11 @@ def paged_attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_len_q: int, max_l
     sequences the prefill tiles serve) lets the library gather their K/V into
     a packed bf16 buffer first, which blocks under 64 tokens and one-byte
     caches (uint8 E4M3 or int8 codes, value = code * k_scale / v_scale) use.
-    A one-byte cache needs it unless no sequence has more than 8 queries (then
-    every query row runs on the decode kernels).  Without ``workspace_buf`` the
-    scratch comes from a buffer cached per (device, stream).
+    Without it a one-byte cache with head dim 128 is read page by page and
+    widened to f16 in shared memory (the query taken as f16 too); head dim 64
+    needs it unless no sequence has more than 8 queries (then every query row
+    runs on the decode kernels).  Without ``workspace_buf`` the scratch comes
+    from a buffer cached per (device, stream).
     """
     _require_cuda(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table)
     T, Hq, D = q.shape
