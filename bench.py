@@ -895,6 +895,19 @@ def ncu_case(args):
         torch.cuda.synchronize()
         log("ncu case done: prefill")
         return
+    if args.ncu_case == "prefill_fp8_direct":
+        # the paged prefill workload with an FP8 cache and no gather bound: the tile loop widens the pages
+        wl = W.to_fp8_cache(W.varlen_prefill(device="cuda", paged=True))
+        sh = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+        pkv.kv_cache_write(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping,
+                           k_inv_scale=wl.extra["k_inv_scale"], v_inv_scale=wl.extra["v_inv_scale"])
+        for _ in range(4):
+            pkv.paged_attn_varlen(wl.q, wl.k_cache.view(sh), wl.v_cache.view(sh), wl.cu_seqlens_q,
+                                  wl.cu_seqlens_k, wl.max_len_q, wl.max_len_k, block_table=wl.block_table,
+                                  scale=wl.scale, k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"])
+        torch.cuda.synchronize()
+        log("ncu case done: prefill_fp8_direct")
+        return
     if args.ncu_case == "multi_query":
         # the speculative-verification workload itself (64 seqs x 4 new tokens, 1K..16K cached): 2.2 GB of K/V
         rng = np.random.default_rng(1008)
@@ -934,7 +947,8 @@ def main():
                     help="seconds of the all-cores oracle timing (0: skip)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "decode_int8", "prefill", "multi_query"],
+    ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "decode_int8", "prefill", "multi_query",
+                                           "prefill_fp8_direct"],
                     default=None,
                     help="run a small case for an ncu capture and exit")
     args = ap.parse_args()
