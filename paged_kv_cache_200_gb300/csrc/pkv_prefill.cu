@@ -11,12 +11,13 @@
 // Causal alignment: query i of a sequence with Lq queries and Lk keys sees key
 // j iff j <= i + Lk - Lq (the queries are the last Lq positions; prefix reuse).
 //
-// Persistent kernel, one 352-thread CTA per SM.  A work item is a pair of
-// adjacent 128-row query tiles (A, then B) of one (sequence, query head),
-// paired from the sequence's end; both tiles read the same K/V tiles (tile
-// A stops at its own last visible tile, one before B's), so each K/V tile is
-// loaded once for 256 query rows.  Items are claimed through a global counter, longest first, and
-// published to the CTA's warps through a shared ring.
+// Persistent kernel, one 352-thread CTA per SM (384 with one-byte pages).  A
+// work item is a pair of adjacent 128-row query tiles (A, then B) of one
+// (sequence, query head), paired from the sequence's end; both tiles read the
+// same K/V tiles (tile A stops at its own last visible tile, one before B's),
+// so each K/V tile is loaded once for 256 query rows.  Items are claimed
+// through a global counter, longest first, and published to the CTA's warps
+// through a shared ring.
 //   warp 0      producer: Q of both tiles (TMA), then K/V tiles of 128 keys
 //               (2 stages each), K one tile ahead of V.  Packed K/V: one TMA
 //               box per head-dim half.  Paged K/V: one box per page and
@@ -29,11 +30,14 @@
 //               come from two threads and interleave in the tensor core.
 //   warps 3..6  softmax of tile A, warps 7..10 of tile B: one thread per query
 //               row, all 128 keys of each tile.  The two groups take turns
-//               tile by tile while both have tiles left.  The running max moves only
-//               when it grows by more than 2^8, so O is rescaled rarely (by
-//               the same thread, in TMEM).  P (bf16 pairs) overwrites half
-//               of its S columns.  After the tile's last PV the group reads O,
-//               releases it, and stores the normalised rows.
+//               tile by tile while both have tiles left.  The running max
+//               moves only when it grows by more than 2^8, so O is rescaled
+//               rarely (by the same thread, in TMEM).  P (bf16 pairs)
+//               overwrites half of its S columns.  After the tile's last PV
+//               the group reads O, releases it, and stores the normalised rows.
+//   warp 11     (FP8 / INT8 pages only) widening: each landed one-byte K/V
+//               tile becomes the f16 tile in place, each Q tile f16, and the
+//               MMAs run f16 x f16.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A at 256, O_B at 384.
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA flags
 // PKV_DEVERR_TIMEOUT, waits (bounded) for its own copies and MMAs, frees TMEM
