@@ -198,12 +198,25 @@ class DecodeStep:
                                                          wl.max_seqlen)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=wl.q.device)
         self.launches = 2 + (1 if need > 0 else 0)
+        self.fused_launches = 1 + (1 if need > 0 else 0)
+        self.before = (wl.cache_seqlens - 1).contiguous()  # tokens cached before the step
 
     def write(self, k_new=None, v_new=None, slots=None):
         wl = self.wl
         self.pkv.kv_cache_write(wl.k_new if k_new is None else k_new, wl.v_new if v_new is None else v_new,
                                 wl.k_cache, wl.v_cache, wl.slot_mapping if slots is None else slots,
                                 k_inv_scale=wl.k_inv_scale, v_inv_scale=wl.v_inv_scale)
+
+    def fused(self, q=None, k_new=None, v_new=None, before=None, table=None, out=None):
+        """The whole step in one launch: each new K/V row appended by the split-KV decode kernel itself."""
+        wl = self.wl
+        self.pkv.paged_attn_decode_with_kvcache(wl.q if q is None else q, wl.k_new if k_new is None else k_new,
+                                                wl.v_new if v_new is None else v_new, self.kc4, self.vc4,
+                                                self.before if before is None else before,
+                                                wl.block_table if table is None else table, wl.scale,
+                                                max_seqlen_k=wl.max_seqlen, k_scale=wl.k_scale, v_scale=wl.v_scale,
+                                                k_inv_scale=wl.k_inv_scale, v_inv_scale=wl.v_inv_scale,
+                                                out=self.out if out is None else out, workspace_buf=self.ws)
 
     def decode(self, q=None, seqlens=None, table=None, out=None):
         wl = self.wl
@@ -235,14 +248,33 @@ def time_decode_steps(step, steps, warmup):
     return total / steps, dec
 
 
+def time_fused_steps(step, steps, warmup):
+    """Device-timed loop of the one-launch step (append + decode); returns (ms per step, mean call ms)."""
+    for _ in range(warmup):
+        step.fused()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        ev[i][0].record()
+        step.fused()
+        ev[i][1].record()
+    end.record()
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    call = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return total / steps, call
+
+
 def time_e2e(step, steps, warmup):
     """Per step: one H2D copy of the step's inputs (packed in one pinned host buffer, each tensor at a
-    256-byte boundary), write + decode on device views of that buffer, and a D2H read of the step's
-    output.  The read runs on a copy stream (two output buffers), so it overlaps the next step's
+    256-byte boundary), the one-launch step (append + decode) on device views of that buffer, and a D2H
+    read of the step's output.  The read runs on a copy stream (two output buffers), so it overlaps the next step's
     kernels, which do not depend on it; every read has completed when the timed region ends."""
     wl = step.wl
-    names = ("q", "k_new", "v_new", "slot_mapping", "cache_seqlens", "block_table")
-    srcs = [getattr(wl, name).contiguous() for name in names]
+    names = ("q", "k_new", "v_new", "before", "block_table")
+    srcs = [(step.before if name == "before" else getattr(wl, name)).contiguous() for name in names]
     offs, total = [], 0
     for t in srcs:
         offs.append(total)
@@ -268,10 +300,9 @@ def time_e2e(step, steps, warmup):
         i = count[0]
         b = i & 1
         dev_buf.copy_(host_buf, non_blocking=True)
-        step.write(dev["k_new"], dev["v_new"], dev["slot_mapping"])
         if i >= 2:
             cur.wait_event(read[b])  # the read of two steps back has left this output buffer
-        step.decode(dev["q"], dev["cache_seqlens"], dev["block_table"], out=out_dev[b])
+        step.fused(dev["q"], dev["k_new"], dev["v_new"], dev["before"], dev["block_table"], out=out_dev[b])
         decoded[b].record(cur)
         side.wait_event(decoded[b])
         with torch.cuda.stream(side):
@@ -448,7 +479,7 @@ def run_pkv(args, rank, world, device):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    ms, dec_ms = time_decode_steps(step, args.steps, args.warmup)
+    ms, dec_ms = time_fused_steps(step, args.steps, args.warmup)
     clk = clocks.stop()
     ms_max = max_over_ranks(ms, device)
     if world > 1:
@@ -462,8 +493,8 @@ def run_pkv(args, rank, world, device):
         also, legs = extra_workloads(pkv, W, device, pk, args)
 
     dec_bytes = decode_bytes(wl)
-    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = profile_traffic("paged_decode_split_bf16_d128")
+    achieved = nbytes / (dec_ms * 1e-3) / 1e9
+    traffic = profile_traffic("paged_decode_split_append_bf16_d128")
     result = {
         "metric": METRIC,
         "value": job_throughput_gbs(nbytes, ms_max, world),
@@ -480,7 +511,8 @@ def run_pkv(args, rank, world, device):
         "config": {
             "workload": "decode_batch64: 64 seqs, cached lengths U[1024,16384] + 1 new token each, 32 q / 8 kv "
                         "heads, head_dim 128, bf16 cache, block_size 16, permuted pool; step = KV write of the 64 "
-                        "new tokens + paged decode attention",
+                        "new tokens + paged decode attention, as one launch (each new row appended by the split-KV "
+                        "decode kernel; the two-launch step is in also.decode_with_kvcache)",
             "batch": wl.batch,
             "attended_tokens": int((wl.lens_before + 1).sum()),
             # share of the block pool holding tokens (the pool has exactly the blocks the lengths need)
@@ -491,21 +523,22 @@ def run_pkv(args, rank, world, device):
         },
         "tokens_per_s": world * wl.batch / (ms_max * 1e-3),
         "roofline": {
-            "kernel": "paged_attn_decode (split-KV kernel + combine, one call)",
+            "kernel": "paged_attn_decode_with_kvcache (split-KV kernel with the step's K/V append + combine, "
+                      "one call)",
             "bound": "hbm",
             "achieved": achieved,
             "peak": pk["hbm_gbs"],
             "unit": "GB/s",
             "frac": achieved / pk["hbm_gbs"],
             "traffic": traffic,
-            "algorithmic_bytes": dec_bytes,
+            "algorithmic_bytes": nbytes,
             "launch_ms": dec_ms,
             "peak_source": pk["source"] + " copy bandwidth (hbm_gbs)",
             "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
         },
         "e2e": {"value": job_throughput_gbs(nbytes, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": step.launches * args.steps,
+        "gpu_launches": step.fused_launches * args.steps,
         "clocks": clk,
     }
     if cpu is not None:
