@@ -971,18 +971,30 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
       obase = epi[0];
       lse_idx = epi[1];
       const bool row_valid = r < (int)epi[2];
-      // O in 32-column chunks: read, normalise, pack to bf16 and store this
-      // thread's row piece (64 bytes) straight away, so no whole row is held in
-      // registers.  O is released after its last chunk is read.
+      // O, normalised, packed to bf16 and stored 32 columns at a time; O is
+      // released once read.  Head dim 64: the whole row in one TMEM round trip
+      // (64 registers).  Head dim 128: chunk by chunk, so that no 128-register
+      // row is live (that spilled and cost 2-6 %).
       uint4* orow = reinterpret_cast<uint4*>(p.out + obase + (int64_t)r * p.num_heads * D);
+      constexpr int kOneTrip = D <= 64;
+      uint32_t o_all[kOneTrip ? D : 32];
+      if constexpr (kOneTrip) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, (o_all + ch * 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kOFree0 + xq));
+      }
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o);
-        tmem_wait_ld();
-        if (ch == D / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(bar(kOFree0 + xq));
+        const uint32_t* o = o_all + (kOneTrip ? ch * 32 : 0);
+        if constexpr (!kOneTrip) {
+          PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o_all);
+          tmem_wait_ld();
+          if (ch == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(kOFree0 + xq));
+          }
         }
         if (row_valid) {
           uint32_t w[16];
