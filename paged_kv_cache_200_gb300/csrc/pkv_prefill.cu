@@ -73,7 +73,9 @@ struct PrefillParams {
   int32_t num_blocks;
   int32_t num_heads;
   int32_t group;
-  int32_t n_pairs;       // query-tile pairs of the longest sequence
+  int32_t n_pairs;       // tile pairs (or, with head_pairs, query tiles) of the longest sequence
+  int32_t head_pairs;    // 1: a pair is one query tile of two heads of a GQA group (even groups); 0: two tiles of one head
+  int32_t item_heads;    // items per (pair, sequence): num_heads / 2 with head_pairs, else num_heads
   int32_t batch;
   int32_t route_decode;  // sequences with at most this many queries are left to the decode kernels (0: none)
   int32_t* item_counter; // work-item counter, zero at launch
@@ -258,16 +260,22 @@ __device__ __forceinline__ SeqBase seq_check(const PrefillParams& p, const int (
   if (bad && report) flag_error(p.err, PKV_DEVERR_LENGTH);
   return s;
 }
-// Pair pe of a sequence, counted from its end, holds query tiles T-2-2pe (A)
-// and T-1-2pe (B), T = ceil(Lq/128): the last tiles, which see the most keys,
-// pair up, and a sequence with an odd tile count leaves tile 0 alone (it sees
-// one K/V tile).  Tile B sees the most keys; tile A stops at its own last
-// visible K/V tile (one before B's when the query and key lengths match) and
-// releases the stages it does not read.
-__device__ __forceinline__ void pair_tiles(int Lq, int pe, int& tA, int& tB) {
+// Pair pe of a sequence, counted from its end.  With head pairs (even GQA
+// groups) it is query tile T-1-pe, T = ceil(Lq/128), of two heads of the same
+// group: A and B see the same keys and read the same K/V tiles.  Otherwise it
+// holds query tiles T-2-2pe (A) and T-1-2pe (B) of one head: the last tiles,
+// which see the most keys, pair up, and a sequence with an odd tile count
+// leaves tile 0 alone (it sees one K/V tile); tile B sees the most keys, and
+// tile A stops at its own last visible K/V tile (one before B's when the query
+// and key lengths match) and releases the stages it does not read.
+__device__ __forceinline__ void pair_tiles(int Lq, int pe, bool head_pairs, int& tA, int& tB) {
   const int T = (Lq + kBM - 1) / kBM;
-  tB = T - 1 - 2 * pe;
-  tA = tB - 1;
+  tB = head_pairs ? T - 1 - pe : T - 1 - 2 * pe;
+  tA = head_pairs ? tB : tB - 1;
+}
+// Query head of tile X of an item whose head slot is hs.
+__device__ __forceinline__ int tile_head(const PrefillParams& p, int hs, int x) {
+  return p.head_pairs ? 2 * hs + x : hs;
 }
 __device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase& b0, int pair) {
   Seq s;
@@ -278,7 +286,7 @@ __device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase&
   s.diag = s.Lk - s.Lq;
   const int kv_tiles = (s.Lk + kBN - 1) / kBN;
   int t[2];
-  pair_tiles(s.Lq, pair, t[0], t[1]);
+  pair_tiles(s.Lq, pair, p.head_pairs != 0, t[0], t[1]);
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
     if (t[x] < 0) {
@@ -298,20 +306,21 @@ __device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase&
   return s;
 }
 
-// Work item -> (sequence, query-tile pair, head).  Items are ordered by pair
-// (counted from each sequence's end: the pairs with the most keys under
-// causal masking first), then sequence, then head, so CTAs running side by
-// side share K/V through L2.
+// Work item -> (sequence, pair, head slot: the head, or with head pairs the
+// pair of heads 2 hs, 2 hs + 1).  Items are ordered by pair (counted from each
+// sequence's end: the pairs with the most keys under causal masking first),
+// then sequence, then head slot, so CTAs running side by side share K/V
+// through L2.
 struct Item {
   int b, pair, head;
 };
 __device__ __forceinline__ Item item_of(const PrefillParams& p, int it) {
-  const int per = p.batch * p.num_heads;
+  const int per = p.batch * p.item_heads;
   Item x;
   x.pair = it / per;
   const int rem = it % per;
-  x.b = rem / p.num_heads;
-  x.head = rem % p.num_heads;
+  x.b = rem / p.item_heads;
+  x.head = rem % p.item_heads;
   return x;
 }
 
@@ -415,7 +424,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_items = p.n_pairs * p.batch * p.num_heads;
+  const int n_items = p.n_pairs * p.batch * p.item_heads;
 
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -549,7 +558,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
       const SeqBase si = seq_check(p, raw, x.pair == 0 && x.head == 0 && lane == 0);
       const Seq sq = seq_derive(p, si, x.pair);
       if (sq.skip) {
-        const int block_end = (it / p.num_heads + 1) * p.num_heads;  // first item of the next (pair, sequence)
+        const int block_end = (it / p.item_heads + 1) * p.item_heads;  // first item of the next (pair, sequence)
         if (lane == 0 && block_end < n_items) atomicMax(p.item_counter, block_end);
         resolve_next();
         it = next;
@@ -561,7 +570,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
         it = next;
         continue;
       }
-      const int kvh = x.head / p.group;
+      const int kvh = tile_head(p, x.head, 0) / p.group;  // (both heads of a head pair share it)
       const int32_t* bt = kPaged ? p.block_table + (int64_t)x.b * p.max_blocks : nullptr;
       // Q of tile X (only when it attends keys), into its buffer once the
       // previous item's last S of that tile is done
@@ -571,7 +580,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
         if (lane == 0) {
           mbar_expect_tx(bar(kQFull0 + xq), L::kTileBytes);
           for (int a = 0; a < L::kAtoms; ++a)
-            tma_load_3d(sbase + L::kQ + xq * L::kTileBytes + a * L::kAtomBytes, &tm_q, a * 64, x.head,
+            tma_load_3d(sbase + L::kQ + xq * L::kTileBytes + a * L::kAtomBytes, &tm_q, a * 64, tile_head(p, x.head, xq),
                         sq.q0 + sq.row0[xq], bar(kQFull0 + xq));
         }
         last_q[xq] = qc[xq];
@@ -651,10 +660,11 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
         const int lq = raw[1] - raw[0];
         if (lq <= p.route_decode) return;
         int tq[2];
-        pair_tiles(lq, y.pair, tq[0], tq[1]);
+        pair_tiles(lq, y.pair, p.head_pairs != 0, tq[0], tq[1]);
         for (int xq = 0; xq < 2; ++xq)
           if (tq[xq] >= 0)
-            for (int a = 0; a < L::kAtoms; ++a) tma_prefetch_3d(&tm_q, a * 64, y.head, raw[0] + tq[xq] * kBM);
+            for (int a = 0; a < L::kAtoms; ++a)
+              tma_prefetch_3d(&tm_q, a * 64, tile_head(p, y.head, xq), raw[0] + tq[xq] * kBM);
       };
       // K(0), Q_A, Q_B (the K stage frees up before the Q buffers do), then K
       // one tile ahead of V
@@ -849,8 +859,9 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
         rows = xq ? sq.rows[1] : sq.rows[0];
         const int row0 = xq ? sq.row0[1] : sq.row0[0];
         nkv = xq ? sq.n[1] : sq.n[0];
-        obase = ((int64_t)(sq.q0 + row0) * p.num_heads + x.head) * D;
-        lse_idx = (int64_t)x.head * p.total_q + sq.q0 + row0 + r;
+        const int head = tile_head(p, x.head, xq);
+        obase = ((int64_t)(sq.q0 + row0) * p.num_heads + head) * D;
+        lse_idx = (int64_t)head * p.total_q + sq.q0 + row0 + r;
         // key limit of this row (bottom-right causal, inside the keys); tiles
         // before jm need no mask for any row of the tile (its first row has
         // the smallest limit)
@@ -1321,7 +1332,7 @@ int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int64_t items = (int64_t)p.n_pairs * batch * p.num_heads;
+  const int64_t items = (int64_t)p.n_pairs * batch * p.item_heads;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
   kern<<<grid, kCode ? kThreadsCoded : kThreads, smem, st>>>(mq, mk, mv, p);
   return launch_status();
@@ -1431,7 +1442,11 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.num_blocks = num_blocks;
   p.num_heads = num_heads;
   p.group = num_heads / num_kv_heads;
-  p.n_pairs = (max_len_q + kPairRows - 1) / kPairRows;
+  // even GQA groups pair two heads of a group on one query tile (same keys,
+  // shared K/V); other groups pair two adjacent tiles of one head
+  p.head_pairs = (p.group % 2 == 0) ? 1 : 0;
+  p.item_heads = p.head_pairs ? num_heads / 2 : num_heads;
+  p.n_pairs = p.head_pairs ? (max_len_q + kBM - 1) / kBM : (max_len_q + kPairRows - 1) / kPairRows;
   p.batch = batch;
   p.route_decode = rmq;
   // FP8: the gathered codes are exact bf16 values; k_scale joins the logit
