@@ -313,6 +313,7 @@ __device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase&
 // through L2.
 struct Item {
   int b, pair, head;
+  int head_b;  // (ring consumers) the query head of tile B; tile A's is tile_head(p, head, 0)
 };
 __device__ __forceinline__ Item item_of(const PrefillParams& p, int it) {
   const int per = p.batch * p.item_heads;
@@ -497,6 +498,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
     sb.Lk = e[4];
     x.pair = e[5];
     x.head = e[6];
+    x.head_b = e[7];
     x.b = 0;
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kRingEmpty0 + slot));
@@ -521,6 +523,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
         e[4] = sb.Lk;
         e[5] = x.pair;
         e[6] = x.head;
+        e[7] = tile_head(p, x.head, 1);
         mbar_arrive(bar(kRingFull0 + slot));
       }
       __syncwarp();
@@ -859,7 +862,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
         rows = xq ? sq.rows[1] : sq.rows[0];
         const int row0 = xq ? sq.row0[1] : sq.row0[0];
         nkv = xq ? sq.n[1] : sq.n[0];
-        const int head = tile_head(p, x.head, xq);
+        const int head = xq ? x.head_b : x.head * (1 + p.head_pairs);  // tile_head(p, x.head, xq)
         obase = ((int64_t)(sq.q0 + row0) * p.num_heads + head) * D;
         lse_idx = (int64_t)head * p.total_q + sq.q0 + row0 + r;
         // key limit of this row (bottom-right causal, inside the keys); tiles
