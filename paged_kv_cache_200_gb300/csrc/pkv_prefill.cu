@@ -12,12 +12,13 @@
 // j iff j <= i + Lk - Lq (the queries are the last Lq positions; prefix reuse).
 //
 // Persistent kernel, one 352-thread CTA per SM (384 with one-byte pages).  A
-// work item is a pair of adjacent 128-row query tiles (A, then B) of one
-// (sequence, query head), paired from the sequence's end; both tiles read the
-// same K/V tiles (tile A stops at its own last visible tile, one before B's),
-// so each K/V tile is loaded once for 256 query rows.  Items are claimed
-// through a global counter, longest first, and published to the CTA's warps
-// through a shared ring.
+// work item is a pair of 128-row query tiles (A, B) of one sequence that read
+// the same K/V tiles, so each K/V tile is loaded once for 256 query rows: one
+// query tile of two heads of a GQA group when the group is even (both see the
+// same keys), else two adjacent tiles of one head, paired from the sequence's
+// end (tile A stops at its own last visible K/V tile, one before B's).  Items
+// are claimed through a global counter, longest first, and published to the
+// CTA's warps through a shared ring.
 //   warp 0      producer: Q of both tiles (TMA), then K/V tiles of 128 keys
 //               (2 stages each), K one tile ahead of V.  Packed K/V: one TMA
 //               box per head-dim half.  Paged K/V: one box per page and
