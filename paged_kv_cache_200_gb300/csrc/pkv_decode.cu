@@ -70,6 +70,7 @@ struct DecodeParams {
   int32_t num_blocks;
   int32_t split_tokens;
   int32_t max_splits;
+  int32_t split_major;  // grid order: (items, kv heads, splits) instead of (splits, kv heads, items)
   float scale_log2;
   float v_mul;
   uint16_t* out;
@@ -197,9 +198,9 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
+  const int split = p.split_major ? blockIdx.z : blockIdx.x;
   const int kvh = blockIdx.y;
-  const int z = blockIdx.z;
+  const int z = p.split_major ? blockIdx.x : blockIdx.z;
   int qi;
   const int b = item_sequence(p, z, qi);
   if (b < 0) return;
@@ -720,6 +721,10 @@ struct SplitPlan {
   // it on the stream (which reads nothing it writes): its CTAs then start on
   // SMs that kernel's CTAs have left
   bool after_primary = false;
+  // grid order: split index slowest (few, long sequences: each wave then
+  // spreads over every sequence; long-context decode +1 %), else fastest
+  // (many sequences of mixed lengths: a sequence's splits run side by side)
+  bool split_major = false;
 };
 
 // Positions per CTA (split_tokens), a multiple of 64 (4 warps x 16), at least
@@ -758,6 +763,7 @@ SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, i
   if (whole <= 512) {
     c = whole;
   } else if (units < sms) {
+    pl.split_major = true;
     const int64_t slots = sms * resident_ctas(cache_dtype);
     const int64_t n_max = 8 * slots / units + 1;  // beyond 8 waves' worth of splits nothing is gained
     c = whole;
@@ -810,7 +816,8 @@ int launch_decode(const DecodeParams& p, int batch, const SplitPlan& pl, int64_t
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
-  dim3 grid(pl.max_splits, p.num_kv_heads, batch);
+  const dim3 grid = pl.split_major ? dim3(batch, p.num_kv_heads, pl.max_splits)
+                                   : dim3(pl.max_splits, p.num_kv_heads, batch);
   if (pl.after_primary) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -941,6 +948,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
   p.num_blocks = num_blocks;
   p.split_tokens = pl.split_tokens;
   p.max_splits = pl.max_splits;
+  p.split_major = pl.split_major ? 1 : 0;
   const bool coded = cache_dtype != PKV_BF16;  // one-byte codes with per-tensor scales
   p.scale_log2 = scale * kLog2e * (coded ? k_scale : 1.f);
   p.v_mul = coded ? v_scale : 1.f;
@@ -1058,6 +1066,7 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
   p.num_blocks = num_blocks;
   p.split_tokens = pl.split_tokens;
   p.max_splits = pl.max_splits;
+  p.split_major = pl.split_major ? 1 : 0;
   p.scale_log2 = scale * kLog2e * (fp8 ? k_scale : 1.f);
   p.v_mul = fp8 ? v_scale : 1.f;
   p.out = static_cast<uint16_t*>(out);
