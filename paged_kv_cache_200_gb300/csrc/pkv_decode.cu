@@ -332,15 +332,30 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
     return blk;
   };
 
+  // Block ids of this warp's tiles: lane l holds that of tile blk_base + l,
+  // loaded and checked 32 tiles at a time, so that a stage's copies wait on no
+  // global load.  Bit s of stage_ok: the tile in stage s has a valid block.
+  int blk_base = -32, blk_lane = -1;
+  uint32_t stage_ok = 0;
+  auto tile_block = [&](int i) -> int {  // (warp-uniform i, increasing)
+    if (i >= blk_base + 32) {
+      blk_base = i & ~31;
+      const int ti = blk_base + lane;
+      blk_lane = ti < my_groups ? block_of(t_begin + (warp + ti * kDecWarps) * kGroupTok, true) : -1;
+    }
+    return __shfl_sync(0xffffffffu, blk_lane, i & 31);
+  };
+
   // Stage i's copies: one TMA box per 128-byte (or 64-byte) column slice of K
   // and of V; a bad block id issues nothing and just completes the phase.
   auto issue = [&](int i) {
     if (i >= my_groups) return;
     const int g = warp + i * kDecWarps;
     const int pos0 = t_begin + g * kGroupTok;
-    const int blk = block_of(pos0, lane == 0);
+    const int blk = tile_block(i);
+    const int st = i % kStages;
+    stage_ok = blk >= 0 ? (stage_ok | (1u << st)) : (stage_ok & ~(1u << st));
     if (lane == 0) {
-      const int st = i % kStages;
       const uint32_t bar = bar0 + 8 * st;
       const uint32_t dst = wsm_u32 + st * kStageBytes;
       fence_proxy_async_smem();  // order earlier generic writes (V tail zeroing) before the async copies
@@ -412,7 +427,7 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
     consumed = i + 1;
     const int g = warp + i * kDecWarps;
     const int pos0 = t_begin + g * kGroupTok;
-    const bool blk_ok = block_of(pos0, false) >= 0;
+    const bool blk_ok = (stage_ok >> st) & 1u;
     uint8_t* stp = wsm + st * kStageBytes;
     const uint32_t ks = smem_u32(stp);
     const uint32_t vs = ks + kTileBytes;

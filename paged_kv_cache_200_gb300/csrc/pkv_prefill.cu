@@ -80,6 +80,9 @@ struct PrefillParams {
   int32_t batch;
   int32_t route_decode;  // sequences with at most this many queries are left to the decode kernels (0: none)
   int32_t* item_counter; // work-item counter, zero at launch
+  const int32_t* unit_order;  // units (sequence b, pair pe) coded b * n_pairs + pe, most K/V tiles first
+  const int32_t* n_units;     // units in unit_order
+  const int32_t* active_ctas; // CTAs that run (the others leave their SMs to the decode kernels of the call)
   float scale_log2;
   float v_mul;           // output factor (FP8 V scale of a gathered cache, else 1)
   int64_t total_q;
@@ -274,6 +277,15 @@ __device__ __forceinline__ void pair_tiles(int Lq, int pe, bool head_pairs, int&
   tB = head_pairs ? T - 1 - pe : T - 1 - 2 * pe;
   tA = head_pairs ? tB : tB - 1;
 }
+// K/V tiles that pair pe of a sequence with Lq queries and Lk keys reads:
+// those its tile B attends (B sees at least as many keys as A).
+__device__ __forceinline__ int unit_kv_tiles(int Lq, int Lk, int pe, bool head_pairs) {
+  int tA, tB;
+  pair_tiles(Lq, pe, head_pairs, tA, tB);
+  const int rows = min(kBM, Lq - tB * kBM);
+  const int kmax = tB * kBM + rows - 1 + Lk - Lq;  // last key tile B's last row sees
+  return kmax < 0 ? 0 : min(kmax / kBN + 1, (Lk + kBN - 1) / kBN);
+}
 // Query head of tile X of an item whose head slot is hs.
 __device__ __forceinline__ int tile_head(const PrefillParams& p, int hs, int x) {
   return p.head_pairs ? 2 * hs + x : hs;
@@ -308,21 +320,20 @@ __device__ __forceinline__ Seq seq_derive(const PrefillParams& p, const SeqBase&
 }
 
 // Work item -> (sequence, pair, head slot: the head, or with head pairs the
-// pair of heads 2 hs, 2 hs + 1).  Items are ordered by pair (counted from each
-// sequence's end: the pairs with the most keys under causal masking first),
-// then sequence, then head slot, so CTAs running side by side share K/V
-// through L2.
+// pair of heads 2 hs, 2 hs + 1).  Items run through the units (sequence, pair)
+// in the order the prep kernel writes (the pairs that read the most K/V tiles
+// first), the head slots of a unit one after another, so CTAs running side by
+// side share K/V through L2.
 struct Item {
   int b, pair, head;
   int head_b;  // (ring consumers) the query head of tile B; tile A's is tile_head(p, head, 0)
 };
 __device__ __forceinline__ Item item_of(const PrefillParams& p, int it) {
-  const int per = p.batch * p.item_heads;
+  const int code = __ldg(p.unit_order + it / p.item_heads);
   Item x;
-  x.pair = it / per;
-  const int rem = it % per;
-  x.b = rem / p.item_heads;
-  x.head = rem % p.item_heads;
+  x.b = code / p.n_pairs;
+  x.pair = code % p.n_pairs;
+  x.head = it % p.item_heads;
   return x;
 }
 
@@ -418,6 +429,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
   constexpr int kQWait0 = kCoded ? kQReady0 : kQFull0;
   constexpr int kKWait0 = kCoded ? kKReady0 : kKFull0;
   constexpr int kVWait0 = kCoded ? kVReady0 : kVFull0;
+  if ((int)blockIdx.x >= __ldg(p.active_ctas)) return;
   // The decode kernels of the same call (the routed query rows) may start as
   // soon as SMs free up: they read nothing this kernel writes.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -426,7 +438,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_items = p.n_pairs * p.batch * p.item_heads;
+  const int n_items = __ldg(p.n_units) * p.item_heads;
 
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -534,10 +546,9 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
     // The next item is claimed from the global counter a few tiles before
     // the current one's last, and its offsets are loaded while those tiles
     // are issued: neither latency then sits between two items, and a claimed
-    // item waits only a few tiles (dynamic balance is kept).  A skipped item
-    // (a sequence left to the decode kernels, or a pair past its end) moves
-    // the counter past the other heads of its (pair, sequence), which are
-    // skipped too.
+    // item waits only a few tiles (dynamic balance is kept).  The unit list
+    // holds only pairs with rows of sequences this kernel serves; an item that
+    // turns out empty all the same is passed over.
     int claim = 0;  // lane 0: atomic result for the next item
     bool claimed = false, resolved = false;
     int it = 0, next = n_items;
@@ -562,8 +573,6 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
       const SeqBase si = seq_check(p, raw, x.pair == 0 && x.head == 0 && lane == 0);
       const Seq sq = seq_derive(p, si, x.pair);
       if (sq.skip) {
-        const int block_end = (it / p.item_heads + 1) * p.item_heads;  // first item of the next (pair, sequence)
-        if (lane == 0 && block_end < n_items) atomicMax(p.item_counter, block_end);
         resolve_next();
         it = next;
         continue;
@@ -1089,55 +1098,228 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
   }
 }
 
-// Varlen prep: compacts the sequences that have exactly one query (decode rows
-// of a mixed batch) into items[0..*count); the prefill kernel skips them and
-// the split-KV decode kernels serve them, one CTA per (split, kv head, item).
-// It also resets the prefill kernel's work-item counter.
-__global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __restrict__ cu_q,
-                                                           const int32_t* __restrict__ cu_k, int batch,
-                                                           int32_t* __restrict__ items, int32_t* __restrict__ count,
-                                                           int32_t* __restrict__ item_counter, int route_cap,
-                                                           int route_max_q, int per_sequence,
-                                                           int32_t* __restrict__ cu_g, int64_t gather_cap,
-                                                           int32_t* err) {
+// Tile-count buckets of the unit order (counts past the last share it).
+constexpr int kOrderBuckets = 2048;
+
+// SM split of a mixed batch.  The prefill CTAs hold one SM each for the whole
+// call, and the decode kernels that serve the routed rows start on the SMs the
+// prefill leaves free, then take the prefill's SMs as its CTAs finish.  The
+// prep kernel models the call's time for every prefill CTA count K and runs
+// the best K (all SMs when no row is routed):
+// - a prefill work item takes kItemNs plus kStepNs per K/V step at head dim
+//   128 (measured on this kernel: about 1.3 and 2.1 us; head dim 64 steps take
+//   0.8 of that, one-byte pages widened in the tile loop 1.4x);
+// - the prefill on K CTAs ends at max(P / K, t_1, t_K + t_(K+1)), P the summed
+//   item times and t_i the i-th longest item: the longest-first order puts the
+//   first K items on their own CTAs, and the next one after the shortest of them;
+// - the routed rows' K/V bytes stream at kDecodeBytesPerNs per SM (about 45 GB/s
+//   measured per SM of the split-KV kernel), on the S - K free SMs until the
+//   prefill ends and on all S after, at most at kDecodeChipBytesPerNs.
+constexpr float kItemNs = 1300.f;
+constexpr float kStepNs = 2100.f;
+constexpr float kDecodeBytesPerNs = 45.f;
+constexpr float kDecodeChipBytesPerNs = 5800.f;
+constexpr float kSplitSlack = 0.02f;
+
+struct PrepArgs {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int batch;
+  // routed rows (items == nullptr: none)
+  int32_t* items;
+  int32_t* count;
+  int route_cap;
+  int route_max_q;   // sequences with up to this many queries are routed (0: none)
+  int per_sequence;  // one item per routed sequence (else one per query row)
+  // prefill work items and unit list (unit_order == nullptr: no prefill kernel)
+  int32_t* item_counter;
+  int32_t* unit_order;
+  int32_t* n_units;
+  int units_cap;
+  int n_pairs;
+  int head_pairs;
+  int item_heads;
+  // SM split: prefill CTAs that run (of sms)
+  int32_t* active_ctas;
+  int sms;
+  float step_ns;          // kStepNs scaled to the head dim and page format
+  float decode_pos_bytes; // K/V bytes of one routed position (all kv heads)
+  // gathered sequences' packed offsets (cu_g == nullptr: no gather)
+  int32_t* cu_g;
+  int64_t gather_cap;
+  int32_t* err;
+};
+
+// Varlen prep (one CTA of 1024 threads): compacts the sequences the decode
+// kernels serve (one query, or up to route_max_q) into items[0..*count),
+// resets the prefill kernel's work-item counter, writes its unit list and the
+// SM split, and, for a gathered batch, the packed offsets.
+__global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
   __shared__ int n;
   __shared__ int64_t carry;
+  __shared__ unsigned long long routed_pos;  // positions the routed items read (decode load)
+  __shared__ unsigned long long unit_tiles;  // K/V tile steps of all prefill units
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     n = 0;
     carry = 0;
-    *item_counter = 0;
+    routed_pos = 0;
+    unit_tiles = 0;
+    *a.item_counter = 0;
   }
   __syncthreads();
-  if (items != nullptr) {
+  if (a.items != nullptr) {
     // every query row of a sequence with 1..route_max_q queries (item codes
     // b * kRouteCode + qi; the bound route_cap holds them all), or, with
     // per_sequence, one item per such sequence (code b * kRouteCode)
-    for (int b = threadIdx.x; b < batch; b += blockDim.x) {
-      const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
-      if (lq >= 1 && lq <= route_max_q) {
-        const int nq = per_sequence ? 1 : lq;
+    unsigned long long pos = 0;
+    for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+      const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+      if (lq >= 1 && lq <= a.route_max_q) {
+        const int nq = a.per_sequence ? 1 : lq;
         const int base = atomicAdd(&n, nq);
         for (int i = 0; i < nq; ++i)
-          if (base + i < route_cap) items[base + i] = b * kRouteCode + i;
+          if (base + i < a.route_cap) a.items[base + i] = b * kRouteCode + i;
+        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+        if (lk > 0) pos += (unsigned long long)lk * nq;
       }
     }
+    if (pos) atomicAdd(&routed_pos, pos);
     __syncthreads();
-    if (threadIdx.x == 0) *count = n < route_cap ? n : route_cap;
+    if (threadIdx.x == 0) *a.count = n < a.route_cap ? n : a.route_cap;
   }
-  if (cu_g != nullptr) {
+  if (a.unit_order != nullptr) {
+    // The prefill kernel's units (sequence b, pair pe, for the sequences it
+    // serves) in longest-processing-time order: by the K/V tiles the pair
+    // reads, most first, so that the longest items start at once and the
+    // short ones fill in at the end.  A counting sort over the tile counts;
+    // units with equal counts land in any order, which changes no result.
+    // blockDim.x (1024) divides kOrderBuckets.
+    __shared__ int hist[kOrderBuckets];
+    __shared__ int wtot[32];
+    __shared__ float wbest_t[32];
+    __shared__ int wbest_k[32];  // (the per-warp minima, then the picks)
+    __shared__ int s_units;
+    for (int i = threadIdx.x; i < kOrderBuckets; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int pass = 0; pass < 2; ++pass) {
+      for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+        const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+        if (lq < 0 || lk < 0) {
+          if (pass == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
+          continue;
+        }
+        if (lq <= a.route_max_q) continue;  // no rows, or left to the decode kernels
+        const int T = (lq + kBM - 1) / kBM;
+        const int all = a.head_pairs ? T : (T + 1) / 2;
+        if (pass == 0 && all > a.n_pairs) flag_error(a.err, PKV_DEVERR_LENGTH);  // more queries than max_len_q
+        const int nu = min(all, a.n_pairs);
+        unsigned long long tiles = 0;
+        for (int pe = 0; pe < nu; ++pe) {
+          const int t = unit_kv_tiles(lq, lk, pe, a.head_pairs != 0);
+          const int c = min(t, kOrderBuckets - 1);
+          if (pass == 0) {
+            atomicAdd(&hist[c], 1);
+            tiles += t;
+          } else {
+            const int pos = atomicAdd(&hist[c], 1);
+            if (pos < a.units_cap)
+              a.unit_order[pos] = b * a.n_pairs + pe;
+            else
+              flag_error(a.err, PKV_DEVERR_LENGTH);  // more query rows than total_q
+          }
+        }
+        if (tiles) atomicAdd(&unit_tiles, tiles);
+      }
+      __syncthreads();
+      if (pass == 1) break;
+      // bucket c -> first position of its units: the units with more tiles
+      // come before it.  Thread t owns the buckets kOrderBuckets-1-t*per-i.
+      const int per = kOrderBuckets / blockDim.x;
+      int local = 0;
+      for (int i = 0; i < per; ++i) local += hist[kOrderBuckets - 1 - threadIdx.x * per - i];
+      int x = local;  // inclusive warp scan
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wtot[warp] = x;
+      __syncthreads();
+      int run = x - local;
+      for (int w = 0; w < warp; ++w) run += wtot[w];
+      for (int i = 0; i < per; ++i) {
+        const int c = kOrderBuckets - 1 - threadIdx.x * per - i;
+        const int h = hist[c];
+        hist[c] = run;
+        run += h;
+      }
+      if (threadIdx.x == blockDim.x - 1) {
+        s_units = run < a.units_cap ? run : a.units_cap;
+        *a.n_units = s_units;
+      }
+      __syncthreads();
+      // SM split (hist holds each bucket's first position): thread K-1 models K
+      // prefill CTAs; the largest K whose modelled time is within kSplitSlack
+      // of the smallest runs (near the best K the model is flat, while one CTA
+      // too few for the longest items costs a whole item)
+      const int units = s_units;
+      float t_mine = INFINITY;
+      const int K = threadIdx.x + 1;
+      if (routed_pos > 0 && units > 0 && K <= a.sms) {
+        // time of the j-th longest item: its unit's bucket is the lowest one
+        // whose first position is at most the unit's rank
+        auto item_t = [&](int64_t j) -> float {
+          const int64_t r = j / a.item_heads;
+          int lo = 0, hi = kOrderBuckets - 1;  // hist[kOrderBuckets - 1] == 0 <= r
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (hist[mid] <= r) hi = mid; else lo = mid + 1;
+          }
+          return kItemNs + a.step_ns * (float)lo;
+        };
+        const int64_t n_items = (int64_t)units * a.item_heads;
+        const float P = (float)a.item_heads * ((float)units * kItemNs + (float)unit_tiles * a.step_ns);
+        const float D = (float)routed_pos * a.decode_pos_bytes;  // bytes
+        float tp = fmaxf(P / (float)K, item_t(0));
+        if (n_items > K) tp = fmaxf(tp, item_t(K - 1) + item_t(K));
+        const float free_rate = (float)(a.sms - K) * kDecodeBytesPerNs;
+        const float all_rate = fminf((float)a.sms * kDecodeBytesPerNs, kDecodeChipBytesPerNs);
+        t_mine = D <= free_rate * tp ? tp : tp + (D - free_rate * tp) / all_rate;
+      }
+      float t_min = t_mine;
+      for (int o = 16; o > 0; o >>= 1) t_min = fminf(t_min, __shfl_xor_sync(0xffffffffu, t_min, o));
+      if (lane == 0) wbest_t[warp] = t_min;
+      __syncthreads();
+      t_min = INFINITY;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t_min = fminf(t_min, wbest_t[w]);
+      int k_pick = t_min < INFINITY && t_mine <= t_min * (1.f + kSplitSlack) ? K : 0;
+      for (int o = 16; o > 0; o >>= 1) k_pick = max(k_pick, __shfl_xor_sync(0xffffffffu, k_pick, o));
+      if (lane == 0) wbest_k[warp] = k_pick;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int kb = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) kb = max(kb, wbest_k[w]);
+        if (kb <= 0) kb = a.sms;  // no routed rows: every CTA
+        *a.active_ctas = kb;
+      }
+      __syncthreads();
+    }
+  }
+  if (a.cu_g != nullptr) {
     // Packed offsets of the gathered sequences (those the prefill kernel
     // serves: more than one query, or any query when nothing is routed):
     // cu_g[b] = sum of their key counts before b.  Exclusive scan, one
     // 32-sequence chunk per warp step, carried across passes.
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nw = blockDim.x >> 5;
     __shared__ int64_t warp_sum[32];
-    for (int base = 0; base < batch; base += blockDim.x) {
+    for (int base = 0; base < a.batch; base += blockDim.x) {
       const int b = base + threadIdx.x;
       int64_t v = 0;
-      if (b < batch) {
-        const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
-        const int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
-        const bool gathered = lq > route_max_q;
+      if (b < a.batch) {
+        const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+        const bool gathered = lq > a.route_max_q;
         v = gathered && lk > 0 ? lk : 0;
       }
       int64_t x = v;  // inclusive warp scan
@@ -1149,7 +1331,7 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
       __syncthreads();
       int64_t before = carry;
       for (int w = 0; w < warp; ++w) before += warp_sum[w];
-      if (b < batch) cu_g[b] = (int32_t)(before + x - v);
+      if (b < a.batch) a.cu_g[b] = (int32_t)(before + x - v);
       __syncthreads();
       if (threadIdx.x == 0) {
         for (int w = 0; w < nw; ++w) carry += warp_sum[w];
@@ -1157,8 +1339,8 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const int32_t* __rest
       __syncthreads();
     }
     if (threadIdx.x == 0) {
-      cu_g[batch] = (int32_t)carry;
-      if (carry > gather_cap) flag_error(err, PKV_DEVERR_LENGTH);  // rows past the buffer are not gathered
+      a.cu_g[a.batch] = (int32_t)carry;
+      if (carry > a.gather_cap) flag_error(a.err, PKV_DEVERR_LENGTH);  // rows past the buffer are not gathered
     }
   }
 }
@@ -1270,7 +1452,7 @@ int g_test_skip_k = -1;
 #endif
 
 struct VarlenWs {
-  size_t count_off, items_off, decode_off, cu_g_off, gk_off, gv_off, total;
+  size_t count_off, items_off, decode_off, order_off, cu_g_off, gk_off, gv_off, total;
 };
 
 // Paged K/V with blocks smaller than this (or FP8) are gathered into a packed
@@ -1283,10 +1465,13 @@ bool uses_gather(bool paged, int kv_dtype, int block_size, int64_t total_k) {
   return paged && total_k > 0 && (kv_dtype != PKV_BF16 || block_size < kGatherBelowBlock);
 }
 
-// [0, 256): the prefill work-item counter and the routed-row count; then the
-// routed row list and the decode partials (paged mode), then, when K/V are
-// gathered, the packed offsets cu_g[batch+1] and the packed K and V buffers
-// of total_k rows each.
+// [0, 256): the prefill work-item counter, the routed-row count, the prefill
+// unit count and the prefill CTAs that run; then the prefill unit list (batch x n_pairs entries at
+// most, when the prefill kernel runs), the routed row list and the decode
+// partials (paged mode), then, when K/V are gathered, the packed offsets
+// cu_g[batch+1] and the packed K and V buffers of total_k rows each.
+constexpr size_t kUnitCountOff = 8;
+constexpr size_t kActiveCtasOff = 12;
 // Queries up to which a sequence is routed to the decode kernels: kRouteMaxQ
 // when no sequence of the batch has more (then every query row is routed and
 // there are total_q items), else 1 (then at most one item per sequence).
@@ -1294,19 +1479,37 @@ int route_max_q(int max_len_q) { return max_len_q <= kRouteMaxQ ? kRouteMaxQ : 1
 // Queries per routed item: max_len_q when each item is a whole sequence
 // (multi_query_items), else 0 (each item is one query row).
 int route_multi_q(int max_len_q, int group) { return multi_query_items(max_len_q, group) ? max_len_q : 0; }
+// Pairs of the longest sequence: query tiles with head pairs (even GQA
+// groups), else pairs of tiles of one head.
+int prefill_pairs(int max_len_q, int group) {
+  return group % 2 == 0 ? (max_len_q + kBM - 1) / kBM : (max_len_q + kPairRows - 1) / kPairRows;
+}
+// Entries of the prefill unit list: none when every query row is routed,
+// else at most one per pair of each sequence, no more than
+// ceil(Lq_b / 128) <= Lq_b / 128 + 1 each.
+int64_t prefill_units(int batch, int total_q, int max_len_q, int group, bool route) {
+  if (route && max_len_q <= kRouteMaxQ) return 0;
+  const int64_t all = (int64_t)batch * prefill_pairs(max_len_q, group);
+  const int64_t by_rows = (int64_t)total_q / kBM + batch;
+  return all < by_rows ? all : by_rows;
+}
 int route_items_bound(int batch, int total_q, int max_len_q, int group) {
   if (route_multi_q(max_len_q, group) > 0) return batch < total_q ? batch : total_q;
   return route_max_q(max_len_q) > 1 ? total_q : (batch < total_q ? batch : total_q);
 }
 
 VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
-                          bool route, bool gather, int64_t total_k, int kv_dtype, int multi_q) {
-  VarlenWs w{0, 0, 0, 0, 0, 0, 256};
+                          bool route, bool gather, int64_t total_k, int kv_dtype, int multi_q, int64_t units) {
+  VarlenWs w{0, 0, 0, 0, 0, 0, 0, 256};
   if (batch <= 0) return w;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  if (units > 0) {
+    w.order_off = w.total;
+    w.total += up((size_t)units * 4);
+  }
   if (route && route_items > 0) {
     w.count_off = 4;
-    w.items_off = 256;
+    w.items_off = w.total;
     w.decode_off = w.items_off + up((size_t)route_items * 4);
     w.total = w.decode_off +
               varlen_decode_workspace(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, kv_dtype,
@@ -1337,7 +1540,8 @@ int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
     attr_set[dev] = true;
   }
   const int64_t items = (int64_t)p.n_pairs * batch * p.item_heads;
-  const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
+  const int64_t sms = device_sm_count();
+  const int grid = (int)(items < sms ? items : sms);
   kern<<<grid, kCode ? kThreadsCoded : kThreads, smem, st>>>(mq, mk, mv, p);
   return launch_status();
 }
@@ -1360,9 +1564,11 @@ extern "C" size_t pkv_paged_attn_varlen_workspace(int32_t batch, int32_t total_q
     return 0;
   const bool gather = pkv::uses_gather(paged != 0, kv_dtype, block_size, total_k);
   const int group = num_heads / num_kv_heads;
+  const bool route = routes_decode(paged != 0, num_heads, num_kv_heads);
   return pkv::varlen_ws_layout(batch, pkv::route_items_bound(batch, total_q, max_len_q, group), num_heads,
-                               num_kv_heads, head_dim, max_len_k, routes_decode(paged != 0, num_heads, num_kv_heads),
-                               gather, total_k, kv_dtype, pkv::route_multi_q(max_len_q, group))
+                               num_kv_heads, head_dim, max_len_k, route, gather, total_k, kv_dtype,
+                               pkv::route_multi_q(max_len_q, group),
+                               pkv::prefill_units(batch, total_q, max_len_q, group, route))
       .total;
 }
 
@@ -1410,8 +1616,12 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   const int route_items = route ? route_items_bound(batch, total_q, max_len_q, group) : 0;
   const int rmq = route ? route_max_q(max_len_q) : 0;  // queries up to which a sequence is routed
   const int multi_q = route ? route_multi_q(max_len_q, group) : 0;  // an item is a whole sequence
+  const int64_t units = prefill_units(batch, total_q, max_len_q, group, route);
+  // unit codes b * n_pairs + pe and item numbers are int32
+  if ((int64_t)batch * prefill_pairs(max_len_q, group) > INT32_MAX || units * num_heads > INT32_MAX)
+    return PKV_ERR_UNSUPPORTED;
   const VarlenWs wl = varlen_ws_layout(batch, route_items, num_heads, num_kv_heads, head_dim, max_len_k, route,
-                                       gather, total_k, kv_dtype, multi_q);
+                                       gather, total_k, kv_dtype, multi_q, units);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
                        (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
@@ -1450,7 +1660,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   // shared K/V); other groups pair two adjacent tiles of one head
   p.head_pairs = (p.group % 2 == 0) ? 1 : 0;
   p.item_heads = p.head_pairs ? num_heads / 2 : num_heads;
-  p.n_pairs = p.head_pairs ? (max_len_q + kBM - 1) / kBM : (max_len_q + kPairRows - 1) / kPairRows;
+  p.n_pairs = prefill_pairs(max_len_q, p.group);
   p.batch = batch;
   p.route_decode = rmq;
   // FP8: the gathered codes are exact bf16 values; k_scale joins the logit
@@ -1469,14 +1679,39 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   int32_t* count = nullptr;
   int32_t* items = nullptr;
   p.item_counter = static_cast<int32_t*>(workspace);
+  int32_t* unit_order = units > 0 ? reinterpret_cast<int32_t*>(wsb + wl.order_off) : nullptr;
+  p.unit_order = unit_order;
+  p.n_units = reinterpret_cast<const int32_t*>(wsb + kUnitCountOff);
+  p.active_ctas = reinterpret_cast<const int32_t*>(wsb + kActiveCtasOff);
   if (route && route_items > 0) {
     count = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.count_off);
     items = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.items_off);
   }
   int32_t* cu_g = gather ? reinterpret_cast<int32_t*>(wsb + wl.cu_g_off) : nullptr;
-  varlen_prep_kernel<<<1, (items != nullptr || gather) ? 1024 : 32, 0, st>>>(
-      cu_seqlens_q, cu_seqlens_k, batch, items, count, p.item_counter, route_items, rmq, multi_q > 0 ? 1 : 0, cu_g,
-      (int64_t)total_k, err_flag);
+  PrepArgs pa{};
+  pa.cu_q = cu_seqlens_q;
+  pa.cu_k = cu_seqlens_k;
+  pa.batch = batch;
+  pa.items = items;
+  pa.count = count;
+  pa.route_cap = route_items;
+  pa.route_max_q = rmq;
+  pa.per_sequence = multi_q > 0 ? 1 : 0;
+  pa.item_counter = p.item_counter;
+  pa.unit_order = unit_order;
+  pa.n_units = reinterpret_cast<int32_t*>(wsb + kUnitCountOff);
+  pa.units_cap = (int)units;
+  pa.n_pairs = p.n_pairs;
+  pa.head_pairs = p.head_pairs;
+  pa.item_heads = p.item_heads;
+  pa.active_ctas = reinterpret_cast<int32_t*>(wsb + kActiveCtasOff);
+  pa.sms = device_sm_count();
+  pa.step_ns = kStepNs * (head_dim == 64 ? 0.8f : 1.f) * (coded_tiles ? 1.4f : 1.f);
+  pa.decode_pos_bytes = (float)num_kv_heads * head_dim * 2.f * (fp8 ? 1.f : 2.f);
+  pa.cu_g = cu_g;
+  pa.gather_cap = (int64_t)total_k;
+  pa.err = err_flag;
+  varlen_prep_kernel<<<1, 1024, 0, st>>>(pa);
   if (gather) {
     const int gx = (max_len_k + kGatherPos - 1) / kGatherPos;
     const dim3 ggrid((unsigned)(gx > 0 ? gx : 1), (unsigned)batch, 1);

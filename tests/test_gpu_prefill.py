@@ -50,6 +50,9 @@ PACKED = [
     ([50], [50], 2, 1, 128),                                   # one pair of heads, one tile
     ([10, 3, 1], [0, 1, 7], 4, 2, 128),                        # empty rows, paired heads
     ([300, 129], [300, 500], 6, 2, 128),                       # odd group: single-CTA path
+    # 40 sequences of 1..400 queries over 0..300 more keys: many units of every tile count
+    (list(np.random.default_rng(5).integers(1, 401, 40)),
+     list(np.random.default_rng(5).integers(1, 401, 40) + np.random.default_rng(6).integers(0, 301, 40)), 8, 2, 64),
 ]
 
 
@@ -233,6 +236,24 @@ def test_mixed_chunked_full_size(pkv, gather):
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
+def test_mixed_light_chunk_heavy_decode(pkv, gather):
+    """One 200-query chunk beside 100 long decode rows: the call gives the prefill few CTAs (the routed
+    rows' decode kernels take the other SMs from the start); every output row is still exact."""
+    rng = np.random.default_rng(21)
+    dec = rng.integers(4096, 8192, size=100, endpoint=True)
+    wl = W.make_varlen_paged(np.r_[200, np.ones(100, dtype=np.int64)], np.r_[100, dec], 32, 8, 128, 16, seed=22,
+                             device="cuda")
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=gather)
+    seqs = [0, 1, 50, 100]
+    ks, vs, tsub = _sub_pool(wl, kc, vc, seqs)
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), ks, vs, wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True, block_table=tsub,
+                                       block_size=wl.block_size, seqs=seqs)
+    _check_rows(out, lse, ref, ref_lse, rows=_rows_of(wl, seqs), what="light chunk")
+
+
 # ---------------------------------------------------------------------------
 # FP8 E4M3 cache in prefill (K/V gathered and widened, scales folded)
 # ---------------------------------------------------------------------------
@@ -331,6 +352,22 @@ def test_gather_bound_too_small_is_flagged(pkv):
                           gather_k_tokens=W.gather_tokens(wl) - 100)
     torch.cuda.synchronize()
     assert int(err.item()) & 4  # PKV_DEVERR_LENGTH
+
+
+def test_more_queries_than_max_len_q_is_flagged(pkv):
+    """A sequence with more queries than the caller's max_len_q is flagged (PKV_DEVERR_LENGTH); the tiles
+    that the bound covers (those with the most keys, counted from the sequence's end) are still exact."""
+    wl = W.make_varlen_packed([300, 100], [300, 100], 8, 2, 128, seed=98, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.zeros_like(wl.q)
+    pkv.paged_attn_varlen(wl.q, wl.k, wl.v, wl.cu_seqlens_q, wl.cu_seqlens_k, 128, wl.max_len_k, scale=wl.scale,
+                          out=out, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 4  # PKV_DEVERR_LENGTH
+    ref, _ = O.paged_attn_varlen(bits(wl.q), bits(wl.k), bits(wl.v), wl.cu_seqlens_q.cpu().numpy(),
+                                 wl.cu_seqlens_k.cpu().numpy(), wl.scale, True)
+    rows = np.r_[256:300, 300:400]  # the last query tile of each sequence
+    assert_close(f64(out)[rows], ref[rows], BF16_ATOL, BF16_RTOL, "last tiles")
 
 
 # ---------------------------------------------------------------------------
