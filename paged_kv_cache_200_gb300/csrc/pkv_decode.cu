@@ -751,18 +751,17 @@ struct SplitPlan {
 //    end on a whole wave and penalises many short CTAs (measured on 8 x 128K
 //    contexts: bf16 6.47 -> 6.64 TB/s, FP8 5.82 -> 5.88 TB/s against 8 waves of
 //    2 CTAs per SM).
-//  * Otherwise the lengths are mixed and unknown on the host: about 32 CTAs
-//    per SM at the longest length, which leaves the short sequences one CTA;
-//    16 when each item carries two row blocks (multi-query items of more than
-//    8 (query, head) rows), whose CTAs do twice the work per position (64
-//    sequences x 4 queries: 0.418 -> 0.399 ms).
+//  * Otherwise the lengths are mixed and unknown on the host: about 16 CTAs
+//    per SM at the longest length, which leaves the short sequences one CTA
+//    (measured on 64 sequences of 1K..16K: 6.41 TB/s at 32, 6.47-6.50 at 16,
+//    6.38 at 12; for 64 sequences x 4 queries, whose items carry two row
+//    blocks, 0.383 ms at 16 and 0.395 at 8).
 constexpr int64_t kCtaOverheadPos = 96;  // prologue + merge of one CTA, in positions of streaming time
-constexpr int64_t kCtasPerSmMixed = 32;
+constexpr int64_t kCtasPerSmMixed = 16;
 
 int resident_ctas(int cache_dtype) { return cache_dtype == PKV_BF16 ? kResidentBf16 : kResidentCoded; }
 
-SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seqlen_k, int cache_dtype,
-                     int row_blocks) {
+SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, int max_seqlen_k, int cache_dtype) {
   SplitPlan pl{64, 1, 0};
   if (batch <= 0 || max_seqlen_k <= 0) return pl;
   const int64_t units = (int64_t)batch * num_kv_heads;
@@ -795,7 +794,7 @@ SplitPlan plan_split(int batch, int num_heads, int num_kv_heads, int head_dim, i
       if (cn == 512) break;  // every larger n gives the same split
     }
   } else {
-    const int64_t target = sms * kCtasPerSmMixed / (row_blocks > 1 ? 2 : 1);
+    const int64_t target = sms * kCtasPerSmMixed;
     c = clamp_split((L * units + target - 1) / target);
   }
   pl.split_tokens = (int)c;
@@ -899,8 +898,8 @@ extern "C" size_t pkv_paged_attn_decode_workspace(int32_t batch, int32_t num_hea
                                                   int32_t head_dim, int32_t max_seqlen_k) {
   if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seqlen_k <= 0) return 0;
   // enough for every cache element type (their plans differ in CTAs per SM)
-  const size_t a = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_BF16, 1).workspace;
-  const size_t b = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_INT8, 1).workspace;
+  const size_t a = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_BF16).workspace;
+  const size_t b = pkv::plan_split(batch, num_heads, num_kv_heads, head_dim, max_seqlen_k, PKV_INT8).workspace;
   return a > b ? a : b;
 }
 
@@ -944,7 +943,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, int32_t
       (reinterpret_cast<uintptr_t>(out) & 7u))
     return PKV_ERR_INVALID_ARG;
   const int mlen = max_seqlen_k > 0 ? max_seqlen_k : 1;
-  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, mlen, cache_dtype, 1);
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, mlen, cache_dtype);
   if (pl.workspace > 0 && (workspace == nullptr || workspace_bytes < pl.workspace ||
                            (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_WORKSPACE;
@@ -1042,8 +1041,7 @@ namespace pkv {
 size_t varlen_decode_workspace(int batch, int items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
                                int cache_dtype, int multi_q) {
   if (batch <= 0 || items <= 0 || max_len_k <= 0) return 0;
-  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k, cache_dtype,
-                                  multi_query_row_blocks(multi_q, num_heads / num_kv_heads));
+  const SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k, cache_dtype);
   if (pl.max_splits <= 1) return 0;
   const size_t rows = (size_t)items * (multi_q > 0 ? multi_q : 1) * num_heads * pl.max_splits;
   return rows * head_dim * sizeof(float) + ((rows * sizeof(float) + 255) / 256) * 256;
@@ -1062,8 +1060,7 @@ int launch_varlen_decode(const void* q, const void* k_cache, const void* v_cache
                          int32_t* err_flag, int32_t multi_q, bool after_primary, cudaStream_t st) {
   const bool fp8 = cache_dtype != PKV_BF16;  // one-byte codes
   if (num_heads / num_kv_heads > kMaxGroup || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
-  SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype,
-                            multi_query_row_blocks(multi_q, num_heads / num_kv_heads));
+  SplitPlan pl = plan_split(batch, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1, cache_dtype);
   pl.after_primary = after_primary;
   if (varlen_decode_workspace(batch, item_bound, num_heads, num_kv_heads, head_dim, max_len_k > 0 ? max_len_k : 1,
                               cache_dtype, multi_q) > workspace_bytes)

@@ -184,7 +184,7 @@ def test_empty_calls_do_nothing_and_invalid_sizes_are_rejected():
 def _split_plan(batch, num_kv_heads, max_len, sms, resident):
     """The decode split plan as the library states it: positions per CTA (a multiple of 64,
     at least 512, at most the whole sequence).  Few (sequence, kv head) units: the split
-    count with the fewest waves x (split + 96); otherwise about 32 CTAs per SM."""
+    count with the fewest waves x (split + 96); otherwise about 16 CTAs per SM."""
     whole = (max_len + 63) // 64 * 64
 
     def clamp(c):
@@ -205,7 +205,7 @@ def _split_plan(batch, num_kv_heads, max_len, sms, resident):
             if c == 512:
                 break
         return best_c
-    return clamp(-(-max_len * units // (sms * 32)))
+    return clamp(-(-max_len * units // (sms * 16)))
 
 
 @pytest.mark.parametrize("shape", [(8, 64, 8, 128, 131073), (64, 32, 8, 128, 16385), (1, 8, 8, 128, 32768),
