@@ -81,6 +81,7 @@ struct PrefillParams {
   int32_t route_decode;  // sequences with at most this many queries are left to the decode kernels (0: none)
   int32_t* item_counter; // work-item counter, zero at launch
   const int32_t* unit_order;  // units (sequence b, pair pe) coded b * n_pairs + pe, most K/V tiles first
+  const int4* unit_seq;       // per unit: its sequence's cu_q[b], cu_q[b+1], cu_k[b], cu_k[b+1]
   const int32_t* n_units;     // units in unit_order
   const int32_t* active_ctas; // CTAs that run (the others leave their SMs to the decode kernels of the call)
   float scale_log2;
@@ -241,12 +242,15 @@ struct Seq {
   bool skip;
 };
 
-// Cumulative offsets of sequence b: q0, q1, k0, k1 (loads only; checked by seq_check).
-__device__ __forceinline__ void seq_load(const PrefillParams& p, int b, int (&raw)[4]) {
-  raw[0] = __ldg(p.cu_q + b);
-  raw[1] = __ldg(p.cu_q + b + 1);
-  raw[2] = __ldg(p.cu_k + b);
-  raw[3] = __ldg(p.cu_k + b + 1);
+// Unit u of the list: its code and its sequence's cumulative offsets q0, q1,
+// k0, k1 (two independent loads; the offsets are checked by seq_check).
+__device__ __forceinline__ void unit_load(const PrefillParams& p, int u, int (&raw)[4], int& code) {
+  const int4 r = __ldg(p.unit_seq + u);
+  code = __ldg(p.unit_order + u);
+  raw[0] = r.x;
+  raw[1] = r.y;
+  raw[2] = r.z;
+  raw[3] = r.w;
 }
 __device__ __forceinline__ SeqBase seq_check(const PrefillParams& p, const int (&raw)[4], bool report) {
   SeqBase s;
@@ -328,8 +332,7 @@ struct Item {
   int b, pair, head;
   int head_b;  // (ring consumers) the query head of tile B; tile A's is tile_head(p, head, 0)
 };
-__device__ __forceinline__ Item item_of(const PrefillParams& p, int it) {
-  const int code = __ldg(p.unit_order + it / p.item_heads);
+__device__ __forceinline__ Item item_of(const PrefillParams& p, int it, int code) {
   Item x;
   x.b = code / p.n_pairs;
   x.pair = code % p.n_pairs;
@@ -429,9 +432,15 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
   constexpr int kQWait0 = kCoded ? kQReady0 : kQFull0;
   constexpr int kKWait0 = kCoded ? kKReady0 : kKFull0;
   constexpr int kVWait0 = kCoded ? kVReady0 : kVFull0;
+  // Launched as a programmatic dependent of the kernel before it: wait until
+  // that grid has completed and its writes (the unit list, the work counter;
+  // the gathered K/V, when a gather ran before, which lets this grid launch
+  // only at its end) are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if ((int)blockIdx.x >= __ldg(p.active_ctas)) return;
   // The decode kernels of the same call (the routed query rows) may start as
-  // soon as SMs free up: they read nothing this kernel writes.
+  // soon as SMs free up: they read nothing this kernel writes, and the routed
+  // row list they read is complete (the prep grid has completed).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -552,6 +561,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
     int claim = 0;  // lane 0: atomic result for the next item
     bool claimed = false, resolved = false;
     int it = 0, next = n_items;
+    int it_code = 0, next_code = 0;  // unit codes of it and next
     int raw[4] = {0, 0, 0, 0};
     auto claim_next = [&]() {
       if (claimed) return;
@@ -562,25 +572,28 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
       claim_next();
       if (resolved) return;
       next = __shfl_sync(0xffffffffu, claim, 0);
-      if (next < n_items) seq_load(p, item_of(p, next).b, raw);
+      if (next < n_items) unit_load(p, next / p.item_heads, raw, next_code);
       resolved = true;
     };
     resolve_next();
     it = next;
+    it_code = next_code;
     while (ok && it < n_items) {
       claimed = resolved = false;
-      const Item x = item_of(p, it);
+      const Item x = item_of(p, it, it_code);
       const SeqBase si = seq_check(p, raw, x.pair == 0 && x.head == 0 && lane == 0);
       const Seq sq = seq_derive(p, si, x.pair);
       if (sq.skip) {
         resolve_next();
         it = next;
+        it_code = next_code;
         continue;
       }
       if (!publish(it, si, x)) { ok = false; break; }
       if (sq.n_kv == 0) {
         resolve_next();
         it = next;
+        it_code = next_code;
         continue;
       }
       const int kvh = tile_head(p, x.head, 0) / p.group;  // (both heads of a head pair share it)
@@ -669,7 +682,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
       // its Q loads (which wait for this item's last S of each tile) hit L2.
       auto prefetch_next_q = [&]() {
         if (lane != 0 || next >= n_items) return;
-        const Item y = item_of(p, next);
+        const Item y = item_of(p, next, next_code);
         const int lq = raw[1] - raw[0];
         if (lq <= p.route_decode) return;
         int tq[2];
@@ -703,6 +716,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
       if (!ok) break;
       resolve_next();
       it = next;
+      it_code = next_code;
       g += sq.n_kv;
     }
     if (ok && !publish(-1, SeqBase{0, 0, 0, 0}, Item{0, 0, 0})) ok = false;
@@ -1099,7 +1113,7 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
 }
 
 // Tile-count buckets of the unit order (counts past the last share it).
-constexpr int kOrderBuckets = 2048;
+constexpr int kOrderBuckets = 1024;
 
 // SM split of a mixed batch.  The prefill CTAs hold one SM each for the whole
 // call, and the decode kernels that serve the routed rows start on the SMs the
@@ -1134,6 +1148,7 @@ struct PrepArgs {
   // prefill work items and unit list (unit_order == nullptr: no prefill kernel)
   int32_t* item_counter;
   int32_t* unit_order;
+  int4* unit_seq;
   int32_t* n_units;
   int units_cap;
   int n_pairs;
@@ -1152,9 +1167,13 @@ struct PrepArgs {
 
 // Varlen prep (one CTA of 1024 threads): compacts the sequences the decode
 // kernels serve (one query, or up to route_max_q) into items[0..*count),
-// resets the prefill kernel's work-item counter, writes its unit list and the
-// SM split, and, for a gathered batch, the packed offsets.
+// resets the prefill kernel's work-item counter, writes the packed offsets of
+// a gathered batch, then the prefill unit list (with each unit's sequence
+// offsets, so that a claimed item needs one round of loads) and the SM split.
 __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
+  // the prefill kernel after this one (when no gather runs between them) may
+  // launch now: it waits for this grid's completion before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int n;
   __shared__ int64_t carry;
   __shared__ unsigned long long routed_pos;  // positions the routed items read (decode load)
@@ -1188,6 +1207,44 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
     __syncthreads();
     if (threadIdx.x == 0) *a.count = n < a.route_cap ? n : a.route_cap;
   }
+  if (a.cu_g != nullptr) {
+    // Packed offsets of the gathered sequences (those the prefill kernel
+    // serves: more than one query, or any query when nothing is routed):
+    // cu_g[b] = sum of their key counts before b.  Exclusive scan, one
+    // 32-sequence chunk per warp step, carried across passes.
+    const int nw = blockDim.x >> 5;
+    __shared__ int64_t warp_sum[32];
+    for (int base = 0; base < a.batch; base += blockDim.x) {
+      const int b = base + threadIdx.x;
+      int64_t v = 0;
+      if (b < a.batch) {
+        const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+        const bool gathered = lq > a.route_max_q;
+        v = gathered && lk > 0 ? lk : 0;
+      }
+      int64_t x = v;  // inclusive warp scan
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) warp_sum[warp] = x;
+      __syncthreads();
+      int64_t before = carry;
+      for (int w = 0; w < warp; ++w) before += warp_sum[w];
+      if (b < a.batch) a.cu_g[b] = (int32_t)(before + x - v);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int w = 0; w < nw; ++w) carry += warp_sum[w];
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      a.cu_g[a.batch] = (int32_t)carry;
+      if (carry > a.gather_cap) flag_error(a.err, PKV_DEVERR_LENGTH);  // rows past the buffer are not gathered
+    }
+    __syncthreads();  // (the unit list below reads cu_g)
+  }
   if (a.unit_order != nullptr) {
     // The prefill kernel's units (sequence b, pair pe, for the sequences it
     // serves) in longest-processing-time order: by the K/V tiles the pair
@@ -1204,7 +1261,8 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
     __syncthreads();
     for (int pass = 0; pass < 2; ++pass) {
       for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
-        const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+        const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
+        const int lq = q1 - q0;
         const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
         if (lq < 0 || lk < 0) {
           if (pass == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
@@ -1215,6 +1273,10 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
         const int all = a.head_pairs ? T : (T + 1) / 2;
         if (pass == 0 && all > a.n_pairs) flag_error(a.err, PKV_DEVERR_LENGTH);  // more queries than max_len_q
         const int nu = min(all, a.n_pairs);
+        // the offsets the prefill kernel reads K/V at: the packed copy's when gathered
+        // (cu_g is written above by other threads of this CTA: plain loads)
+        const int k0 = pass == 1 ? (a.cu_g != nullptr ? a.cu_g[b] : __ldg(a.cu_k + b)) : 0;
+        const int k1 = pass == 1 ? (a.cu_g != nullptr ? a.cu_g[b + 1] : __ldg(a.cu_k + b + 1)) : 0;
         unsigned long long tiles = 0;
         for (int pe = 0; pe < nu; ++pe) {
           const int t = unit_kv_tiles(lq, lk, pe, a.head_pairs != 0);
@@ -1224,9 +1286,10 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
             tiles += t;
           } else {
             const int pos = atomicAdd(&hist[c], 1);
-            if (pos < a.units_cap)
+            if (pos < a.units_cap) {
               a.unit_order[pos] = b * a.n_pairs + pe;
-            else
+              a.unit_seq[pos] = make_int4(q0, q1, k0, k1);
+            } else
               flag_error(a.err, PKV_DEVERR_LENGTH);  // more query rows than total_q
           }
         }
@@ -1264,9 +1327,13 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
       // of the smallest runs (near the best K the model is flat, while one CTA
       // too few for the longest items costs a whole item)
       const int units = s_units;
+      if (routed_pos == 0 || units == 0) {  // (uniform) nothing routed: every CTA
+        if (threadIdx.x == 0) *a.active_ctas = a.sms;
+        continue;
+      }
       float t_mine = INFINITY;
       const int K = threadIdx.x + 1;
-      if (routed_pos > 0 && units > 0 && K <= a.sms) {
+      if (K <= a.sms) {
         // time of the j-th longest item: its unit's bucket is the lowest one
         // whose first position is at most the unit's rank
         auto item_t = [&](int64_t j) -> float {
@@ -1300,47 +1367,10 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
       if (threadIdx.x == 0) {
         int kb = 0;
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) kb = max(kb, wbest_k[w]);
-        if (kb <= 0) kb = a.sms;  // no routed rows: every CTA
+        if (kb <= 0) kb = a.sms;
         *a.active_ctas = kb;
       }
       __syncthreads();
-    }
-  }
-  if (a.cu_g != nullptr) {
-    // Packed offsets of the gathered sequences (those the prefill kernel
-    // serves: more than one query, or any query when nothing is routed):
-    // cu_g[b] = sum of their key counts before b.  Exclusive scan, one
-    // 32-sequence chunk per warp step, carried across passes.
-    const int nw = blockDim.x >> 5;
-    __shared__ int64_t warp_sum[32];
-    for (int base = 0; base < a.batch; base += blockDim.x) {
-      const int b = base + threadIdx.x;
-      int64_t v = 0;
-      if (b < a.batch) {
-        const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
-        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
-        const bool gathered = lq > a.route_max_q;
-        v = gathered && lk > 0 ? lk : 0;
-      }
-      int64_t x = v;  // inclusive warp scan
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (lane == 31) warp_sum[warp] = x;
-      __syncthreads();
-      int64_t before = carry;
-      for (int w = 0; w < warp; ++w) before += warp_sum[w];
-      if (b < a.batch) a.cu_g[b] = (int32_t)(before + x - v);
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        for (int w = 0; w < nw; ++w) carry += warp_sum[w];
-      }
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-      a.cu_g[a.batch] = (int32_t)carry;
-      if (carry > a.gather_cap) flag_error(a.err, PKV_DEVERR_LENGTH);  // rows past the buffer are not gathered
     }
   }
 }
@@ -1452,7 +1482,7 @@ int g_test_skip_k = -1;
 #endif
 
 struct VarlenWs {
-  size_t count_off, items_off, decode_off, order_off, cu_g_off, gk_off, gv_off, total;
+  size_t count_off, items_off, decode_off, order_off, useq_off, cu_g_off, gk_off, gv_off, total;
 };
 
 // Paged K/V with blocks smaller than this (or FP8) are gathered into a packed
@@ -1466,10 +1496,12 @@ bool uses_gather(bool paged, int kv_dtype, int block_size, int64_t total_k) {
 }
 
 // [0, 256): the prefill work-item counter, the routed-row count, the prefill
-// unit count and the prefill CTAs that run; then the prefill unit list (batch x n_pairs entries at
-// most, when the prefill kernel runs), the routed row list and the decode
-// partials (paged mode), then, when K/V are gathered, the packed offsets
-// cu_g[batch+1] and the packed K and V buffers of total_k rows each.
+// unit count and the prefill CTAs that run; then, when the prefill kernel
+// runs, its unit list (int32 codes) and the units' sequence offsets (int4),
+// each at most min(batch x n_pairs, total_q / 128 + batch) entries; then the
+// routed row list and the decode partials (paged mode), then, when K/V are
+// gathered, the packed offsets cu_g[batch+1] and the packed K and V buffers of
+// total_k rows each.
 constexpr size_t kUnitCountOff = 8;
 constexpr size_t kActiveCtasOff = 12;
 // Queries up to which a sequence is routed to the decode kernels: kRouteMaxQ
@@ -1500,12 +1532,13 @@ int route_items_bound(int batch, int total_q, int max_len_q, int group) {
 
 VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_heads, int head_dim, int max_len_k,
                           bool route, bool gather, int64_t total_k, int kv_dtype, int multi_q, int64_t units) {
-  VarlenWs w{0, 0, 0, 0, 0, 0, 0, 256};
+  VarlenWs w{0, 0, 0, 0, 0, 0, 0, 0, 256};
   if (batch <= 0) return w;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   if (units > 0) {
     w.order_off = w.total;
-    w.total += up((size_t)units * 4);
+    w.useq_off = w.order_off + up((size_t)units * 4);
+    w.total = w.useq_off + up((size_t)units * 16);
   }
   if (route && route_items > 0) {
     w.count_off = 4;
@@ -1542,7 +1575,20 @@ int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
   const int64_t items = (int64_t)p.n_pairs * batch * p.item_heads;
   const int64_t sms = device_sm_count();
   const int grid = (int)(items < sms ? items : sms);
-  kern<<<grid, kCode ? kThreadsCoded : kThreads, smem, st>>>(mq, mk, mv, p);
+  // a programmatic dependent of the kernel before it: after the prep, its CTAs
+  // start as the prep runs and wait for its completion (the gather does not
+  // trigger: its grid needs the SMs to itself)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kCode ? kThreadsCoded : kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) return PKV_ERR_CUDA;
   return launch_status();
 }
 
@@ -1681,6 +1727,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   p.item_counter = static_cast<int32_t*>(workspace);
   int32_t* unit_order = units > 0 ? reinterpret_cast<int32_t*>(wsb + wl.order_off) : nullptr;
   p.unit_order = unit_order;
+  p.unit_seq = units > 0 ? reinterpret_cast<const int4*>(wsb + wl.useq_off) : nullptr;
   p.n_units = reinterpret_cast<const int32_t*>(wsb + kUnitCountOff);
   p.active_ctas = reinterpret_cast<const int32_t*>(wsb + kActiveCtasOff);
   if (route && route_items > 0) {
@@ -1699,6 +1746,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   pa.per_sequence = multi_q > 0 ? 1 : 0;
   pa.item_counter = p.item_counter;
   pa.unit_order = unit_order;
+  pa.unit_seq = units > 0 ? reinterpret_cast<int4*>(wsb + wl.useq_off) : nullptr;
   pa.n_units = reinterpret_cast<int32_t*>(wsb + kUnitCountOff);
   pa.units_cap = (int)units;
   pa.n_pairs = p.n_pairs;
