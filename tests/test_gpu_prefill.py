@@ -254,6 +254,36 @@ def test_mixed_light_chunk_heavy_decode(pkv, gather):
     _check_rows(out, lse, ref, ref_lse, rows=_rows_of(wl, seqs), what="light chunk")
 
 
+MIXED_MATRIX = [(hq, hkv, d, dt, g) for hq, hkv in ((8, 2), (6, 2)) for d in (64, 128)
+                for dt in ("bf16", "fp8_e4m3", "int8") for g in (False, True)
+                if not (dt != "bf16" and d == 64 and not g)]  # one-byte d64 pages need the gather bound
+
+
+@pytest.mark.parametrize("case", MIXED_MATRIX,
+                         ids=[f"{c[0]}q{c[1]}kv_d{c[2]}_{c[3]}_{'gathered' if c[4] else 'direct'}" for c in MIXED_MATRIX])
+def test_mixed_batch_matrix(pkv, case):
+    """Three chunks over prefixes beside 25 routed decode rows, in one call, for even and odd GQA
+    groups (head pairs / tile pairs), head dim 64 and 128, bf16 / FP8 / INT8 caches, pages read
+    directly or gathered: every output row against the oracle.  The call splits the SMs between
+    the prefill tiles and the decode rows by its own model of the two loads."""
+    Hq, Hkv, D, dt, gather = case
+    rng = np.random.default_rng(Hq + D)
+    dec = rng.integers(100, 1200, size=25, endpoint=True)
+    wl = W.make_varlen_paged(np.r_[300, 130, 77, np.ones(25, dtype=np.int64)], np.r_[0, 450, 900, dec], Hq, Hkv, D,
+                             16, seed=Hq * 7 + D, device="cuda", extra_blocks=2)
+    if dt != "bf16":
+        wl = W.to_fp8_cache(wl, dt)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=gather)
+    kw = dict(kv_dtype=dt, k_scale=wl.extra["k_scale"], v_scale=wl.extra["v_scale"]) if dt != "bf16" else {}
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=16, **kw)
+    atol, rtol = (BF16_ATOL, BF16_RTOL) if dt == "bf16" else (FP8_ATOL, FP8_RTOL)
+    assert_close(f64(out), ref, atol, rtol, f"mixed {case}")
+    assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"mixed lse {case}")
+
+
 # ---------------------------------------------------------------------------
 # FP8 E4M3 cache in prefill (K/V gathered and widened, scales folded)
 # ---------------------------------------------------------------------------
