@@ -425,6 +425,13 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
       break;
     }
     consumed = i + 1;
+    // Many sequences (the sequence-major grid): refill now the stage this warp
+    // finished with in the previous iteration (its lanes passed the __syncwarp
+    // at that iteration's end), so that two tiles are in flight while this one
+    // is computed (decode batch step +0.3 %, multi-query +0.2 %, same box).
+    // Few long sequences (split-major) stream at the copy peak already and
+    // lose 1-5 % with the extra copies in flight: they refill after the compute.
+    if (!p.split_major) issue(i + kStages - 1);
     const int g = warp + i * kDecWarps;
     const int pos0 = t_begin + g * kGroupTok;
     const bool blk_ok = (stage_ok >> st) & 1u;
@@ -575,7 +582,7 @@ __global__ void __launch_bounds__(kDecThreads, kFp8 && kNB == 1 ? kResidentCoded
       }
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
-    issue(i + kStages - 1);
+    if (p.split_major) issue(i + kStages - 1);
   }
   // copies issued but never consumed (only after a timeout) land before the
   // shared memory is reused; if one of them does not land in time either, the
