@@ -270,8 +270,10 @@ def time_fused_steps(step, steps, warmup):
 def time_e2e(step, steps, warmup):
     """Per step: one H2D copy of the step's inputs (packed in one pinned host buffer, each tensor at a
     256-byte boundary), the one-launch step (append + decode) on device views of that buffer, and a D2H
-    read of the step's output.  The read runs on a copy stream (two output buffers), so it overlaps the next step's
-    kernels, which do not depend on it; every read has completed when the timed region ends."""
+    read of the step's output.  Both copies run on copy streams with two device buffers each: the
+    next step's inputs are copied while this step's kernels run, and this step's output is read
+    while the next step's run; a step's kernels wait for its own input copy.  Every copy of the
+    timed steps is issued and has completed inside the timed region."""
     wl = step.wl
     names = ("q", "k_new", "v_new", "before", "block_table")
     srcs = [(step.before if name == "before" else getattr(wl, name)).contiguous() for name in names]
@@ -280,44 +282,64 @@ def time_e2e(step, steps, warmup):
         offs.append(total)
         total += (t.numel() * t.element_size() + 255) // 256 * 256
     host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=wl.q.device)
-    dev = {}
+    dev_buf = [torch.empty(total, dtype=torch.uint8, device=wl.q.device) for _ in range(2)]
+    dev = [{}, {}]
     for name, t, off in zip(names, srcs, offs):
         nb = t.numel() * t.element_size()
         host_buf[off:off + nb].copy_(t.cpu().view(-1).view(torch.uint8))
-        dev[name] = dev_buf[off:off + nb].view(t.dtype).view(t.shape)
+        for b in range(2):
+            dev[b][name] = dev_buf[b][off:off + nb].view(t.dtype).view(t.shape)
     out_dev = [step.out, torch.empty_like(step.out)]
     out_host = [torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True) for _ in range(2)]
     h2d = total
     d2h = out_host[0].numel() * out_host[0].element_size()
     cur = torch.cuda.current_stream()
-    side = torch.cuda.Stream(device=wl.q.device)
+    up = torch.cuda.Stream(device=wl.q.device)    # H2D
+    down = torch.cuda.Stream(device=wl.q.device)  # D2H
+    copied = [torch.cuda.Event() for _ in range(2)]
+    used = [torch.cuda.Event() for _ in range(2)]
     decoded = [torch.cuda.Event() for _ in range(2)]
     read = [torch.cuda.Event() for _ in range(2)]
     count = [0]
 
-    def one():
+    def copy_in(i):
+        b = i & 1
+        if i >= 2:
+            up.wait_event(used[b])  # the kernels of two steps back have read this input buffer
+        with torch.cuda.stream(up):
+            dev_buf[b].copy_(host_buf, non_blocking=True)
+        copied[b].record(up)
+
+    def one(last):
         i = count[0]
         b = i & 1
-        dev_buf.copy_(host_buf, non_blocking=True)
+        cur.wait_event(copied[b])
         if i >= 2:
             cur.wait_event(read[b])  # the read of two steps back has left this output buffer
-        step.fused(dev["q"], dev["k_new"], dev["v_new"], dev["before"], dev["block_table"], out=out_dev[b])
+        step.fused(dev[b]["q"], dev[b]["k_new"], dev[b]["v_new"], dev[b]["before"], dev[b]["block_table"],
+                   out=out_dev[b])
+        used[b].record(cur)
         decoded[b].record(cur)
-        side.wait_event(decoded[b])
-        with torch.cuda.stream(side):
+        if not last:
+            copy_in(i + 1)
+        down.wait_event(decoded[b])
+        with torch.cuda.stream(down):
             out_host[b].copy_(out_dev[b], non_blocking=True)
-        read[b].record(side)
+        read[b].record(down)
         count[0] += 1
 
-    for _ in range(warmup):
-        one()
+    copy_in(count[0])
+    for w in range(warmup):
+        one(w == warmup - 1)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
-    for _ in range(steps):
-        one()
-    cur.wait_stream(side)  # every output read is inside the timed region
+    cur.wait_event(start)
+    up.wait_stream(cur)  # the first input copy starts inside the timed region
+    copy_in(count[0])
+    for k in range(steps):
+        one(k == steps - 1)
+    cur.wait_stream(down)  # every output read is inside the timed region
     end.record()
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps, h2d, d2h
