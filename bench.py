@@ -977,6 +977,20 @@ def ncu_case(args):
         torch.cuda.synchronize()
         log("ncu case done: multi_query")
         return
+    if args.ncu_case == "mixed":
+        # the mixed chunked batch itself (4 chunks over 0..8K prefixes + 60 decode rows, one varlen
+        # call after the write, chunks gathered): about 2.5 GB of K/V pool; launch lists only
+        wm = W.mixed_chunked(device="cuda")
+        sh = (wm.num_blocks, wm.block_size, wm.num_kv_heads, wm.head_dim)
+        gtok = W.gather_tokens(wm)
+        for _ in range(4):
+            pkv.kv_cache_write(wm.k_new, wm.v_new, wm.k_cache, wm.v_cache, wm.slot_mapping)
+            pkv.paged_attn_varlen(wm.q, wm.k_cache.view(sh), wm.v_cache.view(sh), wm.cu_seqlens_q,
+                                  wm.cu_seqlens_k, wm.max_len_q, wm.max_len_k, block_table=wm.block_table,
+                                  scale=wm.scale, gather_k_tokens=gtok)
+        torch.cuda.synchronize()
+        log("ncu case done: mixed")
+        return
     rng = np.random.default_rng(77)
     dt = {"decode_fp8": "fp8_e4m3", "decode_int8": "int8"}.get(args.ncu_case, "bf16")
     # 64 sequences of 1K..4K cached tokens: ~0.65 GB of bf16 K/V, larger than L2
@@ -1003,7 +1017,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", choices=["decode", "decode_fp8", "decode_int8", "prefill", "multi_query",
-                                           "prefill_fp8_direct"],
+                                           "prefill_fp8_direct", "mixed"],
                     default=None,
                     help="run a small case for an ncu capture and exit")
     args = ap.parse_args()

@@ -1115,6 +1115,38 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
 // Tile-count buckets of the unit order (counts past the last share it).
 constexpr int kOrderBuckets = 1024;
 
+// Exclusive prefix sum of v over the CTA's threads (in thread order) and the
+// CTA's total: a shuffle scan within each warp, then one warp scans the warp
+// totals.  ws: 33 shared slots; every thread of the CTA calls it.
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T* ws, T& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  T x = v;  // inclusive within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const T w = lane < nw ? ws[lane] : T(0);
+    T wx = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const T y = __shfl_up_sync(0xffffffffu, wx, o);
+      if (lane >= o) wx += y;
+    }
+    if (lane < nw) ws[lane] = wx - w;  // warps before this one
+    if (lane == 31) ws[32] = wx;
+  }
+  __syncthreads();
+  const T r = ws[warp] + x - v;
+  total = ws[32];
+  __syncthreads();  // (ws is free for the next call)
+  return r;
+}
+
 // SM split of a mixed batch.  The prefill CTAs hold one SM each for the whole
 // call, and the decode kernels that serve the routed rows start on the SMs the
 // prefill leaves free, then take the prefill's SMs as its CTAs finish.  The
@@ -1171,14 +1203,30 @@ struct PrepArgs {
 // a gathered batch, then the prefill unit list (with each unit's sequence
 // offsets, so that a claimed item needs one round of loads) and the SM split.
 __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
-  // the prefill kernel after this one (when no gather runs between them) may
-  // launch now: it waits for this grid's completion before it reads anything
+  // the kernel after this one (the gather, or the prefill when no gather runs)
+  // may launch now: it waits for this grid's completion before it reads anything
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int n;
   __shared__ int64_t carry;
   __shared__ unsigned long long routed_pos;  // positions the routed items read (decode load)
   __shared__ unsigned long long unit_tiles;  // K/V tile steps of all prefill units
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Every section below visits sequence b = threadIdx.x first: its offsets are
+  // loaded once, here (later sequences of a batch above blockDim load again).
+  int f_q0 = 0, f_q1 = 0, f_k0 = 0, f_k1 = 0;
+  if ((int)threadIdx.x < a.batch) {
+    f_q0 = __ldg(a.cu_q + threadIdx.x);
+    f_q1 = __ldg(a.cu_q + threadIdx.x + 1);
+    f_k0 = __ldg(a.cu_k + threadIdx.x);
+    f_k1 = __ldg(a.cu_k + threadIdx.x + 1);
+  }
+  auto offsets = [&](int b, int& q0, int& q1, int& k0, int& k1) {
+    if (b == (int)threadIdx.x) {
+      q0 = f_q0, q1 = f_q1, k0 = f_k0, k1 = f_k1;
+    } else {
+      q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1), k0 = __ldg(a.cu_k + b), k1 = __ldg(a.cu_k + b + 1);
+    }
+  };
   if (threadIdx.x == 0) {
     n = 0;
     carry = 0;
@@ -1191,19 +1239,32 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
     // every query row of a sequence with 1..route_max_q queries (item codes
     // b * kRouteCode + qi; the bound route_cap holds them all), or, with
     // per_sequence, one item per such sequence (code b * kRouteCode)
+    // (slots claimed once per warp: the lanes' counts scanned, one atomic)
     unsigned long long pos = 0;
-    for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
-      const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
-      if (lq >= 1 && lq <= a.route_max_q) {
-        const int nq = a.per_sequence ? 1 : lq;
-        const int base = atomicAdd(&n, nq);
-        for (int i = 0; i < nq; ++i)
-          if (base + i < a.route_cap) a.items[base + i] = b * kRouteCode + i;
-        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
-        if (lk > 0) pos += (unsigned long long)lk * nq;
+    for (int b0 = 0; b0 < a.batch; b0 += blockDim.x) {
+      const int b = b0 + threadIdx.x;
+      int nq = 0, lk = 0;
+      if (b < a.batch) {
+        int q0, q1, k0, k1;
+        offsets(b, q0, q1, k0, k1);
+        const int lq = q1 - q0;
+        if (lq >= 1 && lq <= a.route_max_q) nq = a.per_sequence ? 1 : lq;
+        lk = k1 - k0;
       }
+      int x = nq;  // inclusive warp scan of the counts
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      int wbase = 0;
+      if (lane == 31 && x > 0) wbase = atomicAdd(&n, x);
+      const int base = __shfl_sync(0xffffffffu, wbase, 31) + x - nq;
+      for (int i = 0; i < nq; ++i)
+        if (base + i < a.route_cap) a.items[base + i] = b * kRouteCode + i;
+      if (nq > 0 && lk > 0) pos += (unsigned long long)lk * nq;
     }
-    if (pos) atomicAdd(&routed_pos, pos);
+    for (int o = 16; o > 0; o >>= 1) pos += __shfl_xor_sync(0xffffffffu, pos, o);
+    if (lane == 0 && pos) atomicAdd(&routed_pos, pos);
     __syncthreads();
     if (threadIdx.x == 0) *a.count = n < a.route_cap ? n : a.route_cap;
   }
@@ -1212,31 +1273,22 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
     // serves: more than one query, or any query when nothing is routed):
     // cu_g[b] = sum of their key counts before b.  Exclusive scan, one
     // 32-sequence chunk per warp step, carried across passes.
-    const int nw = blockDim.x >> 5;
-    __shared__ int64_t warp_sum[32];
+    __shared__ int64_t scan_ws[33];
     for (int base = 0; base < a.batch; base += blockDim.x) {
       const int b = base + threadIdx.x;
       int64_t v = 0;
       if (b < a.batch) {
-        const int lq = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
-        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+        int q0, q1, k0, k1;
+        offsets(b, q0, q1, k0, k1);
+        const int lq = q1 - q0, lk = k1 - k0;
         const bool gathered = lq > a.route_max_q;
         v = gathered && lk > 0 ? lk : 0;
       }
-      int64_t x = v;  // inclusive warp scan
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (lane == 31) warp_sum[warp] = x;
-      __syncthreads();
-      int64_t before = carry;
-      for (int w = 0; w < warp; ++w) before += warp_sum[w];
-      if (b < a.batch) a.cu_g[b] = (int32_t)(before + x - v);
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        for (int w = 0; w < nw; ++w) carry += warp_sum[w];
-      }
+      int64_t chunk = 0;
+      const int64_t before = block_exclusive_scan(v, scan_ws, chunk);
+      if (b < a.batch) a.cu_g[b] = (int32_t)(carry + before);
+      __syncthreads();  // (every thread has read carry)
+      if (threadIdx.x == 0) carry += chunk;
       __syncthreads();
     }
     if (threadIdx.x == 0) {
@@ -1253,17 +1305,24 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
     // units with equal counts land in any order, which changes no result.
     // blockDim.x (1024) divides kOrderBuckets.
     __shared__ int hist[kOrderBuckets];
-    __shared__ int wtot[32];
-    __shared__ float wbest_t[32];
-    __shared__ int wbest_k[32];  // (the per-warp minima, then the picks)
+    __shared__ int wtot[33];
+    __shared__ float wbest_t[33];  // per-warp minima, then (slot 32) the CTA's
+    __shared__ int wbest_k[32];    // per-warp picks
     __shared__ int s_units;
     for (int i = threadIdx.x; i < kOrderBuckets; i += blockDim.x) hist[i] = 0;
     __syncthreads();
+    // a group of lps lanes per sequence (a power of two, up to a warp: more
+    // lanes for fewer sequences), the group's lanes taking the units in turn
+    int lps = 1;
+    while (lps < 32 && lps * 2 * a.batch <= (int)blockDim.x) lps *= 2;
+    const int grp = threadIdx.x / lps, sub = threadIdx.x % lps, ngrp = blockDim.x / lps;
     for (int pass = 0; pass < 2; ++pass) {
-      for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
-        const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
+      unsigned long long tiles = 0;
+      for (int b = grp; b < a.batch; b += ngrp) {
+        int q0, q1, ck0, ck1;
+        offsets(b, q0, q1, ck0, ck1);
         const int lq = q1 - q0;
-        const int lk = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+        const int lk = ck1 - ck0;
         if (lq < 0 || lk < 0) {
           if (pass == 0) flag_error(a.err, PKV_DEVERR_LENGTH);
           continue;
@@ -1275,10 +1334,9 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
         const int nu = min(all, a.n_pairs);
         // the offsets the prefill kernel reads K/V at: the packed copy's when gathered
         // (cu_g is written above by other threads of this CTA: plain loads)
-        const int k0 = pass == 1 ? (a.cu_g != nullptr ? a.cu_g[b] : __ldg(a.cu_k + b)) : 0;
-        const int k1 = pass == 1 ? (a.cu_g != nullptr ? a.cu_g[b + 1] : __ldg(a.cu_k + b + 1)) : 0;
-        unsigned long long tiles = 0;
-        for (int pe = 0; pe < nu; ++pe) {
+        const int k0 = pass == 1 ? (a.cu_g != nullptr ? a.cu_g[b] : ck0) : 0;
+        const int k1 = pass == 1 ? (a.cu_g != nullptr ? a.cu_g[b + 1] : ck1) : 0;
+        for (int pe = sub; pe < nu; pe += lps) {
           const int t = unit_kv_tiles(lq, lk, pe, a.head_pairs != 0);
           const int c = min(t, kOrderBuckets - 1);
           if (pass == 0) {
@@ -1293,8 +1351,9 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
               flag_error(a.err, PKV_DEVERR_LENGTH);  // more query rows than total_q
           }
         }
-        if (tiles) atomicAdd(&unit_tiles, tiles);
       }
+      for (int o = 16; o > 0; o >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+      if (lane == 0 && tiles) atomicAdd(&unit_tiles, tiles);
       __syncthreads();
       if (pass == 1) break;
       // bucket c -> first position of its units: the units with more tiles
@@ -1302,15 +1361,8 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
       const int per = kOrderBuckets / blockDim.x;
       int local = 0;
       for (int i = 0; i < per; ++i) local += hist[kOrderBuckets - 1 - threadIdx.x * per - i];
-      int x = local;  // inclusive warp scan
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (lane == 31) wtot[warp] = x;
-      __syncthreads();
-      int run = x - local;
-      for (int w = 0; w < warp; ++w) run += wtot[w];
+      int all_units = 0;
+      int run = block_exclusive_scan(local, wtot, all_units);
       for (int i = 0; i < per; ++i) {
         const int c = kOrderBuckets - 1 - threadIdx.x * per - i;
         const int h = hist[c];
@@ -1336,8 +1388,8 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
       if (K <= a.sms) {
         // time of the j-th longest item: its unit's bucket is the lowest one
         // whose first position is at most the unit's rank
-        auto item_t = [&](int64_t j) -> float {
-          const int64_t r = j / a.item_heads;
+        auto item_t = [&](int j) -> float {  // (item numbers fit int32: checked on the host)
+          const int r = j / a.item_heads;
           int lo = 0, hi = kOrderBuckets - 1;  // hist[kOrderBuckets - 1] == 0 <= r
           while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -1345,7 +1397,7 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
           }
           return kItemNs + a.step_ns * (float)lo;
         };
-        const int64_t n_items = (int64_t)units * a.item_heads;
+        const int n_items = units * a.item_heads;
         const float P = (float)a.item_heads * ((float)units * kItemNs + (float)unit_tiles * a.step_ns);
         const float D = (float)routed_pos * a.decode_pos_bytes;  // bytes
         float tp = fmaxf(P / (float)K, item_t(0));
@@ -1354,21 +1406,28 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
         const float all_rate = fminf((float)a.sms * kDecodeBytesPerNs, kDecodeChipBytesPerNs);
         t_mine = D <= free_rate * tp ? tp : tp + (D - free_rate * tp) / all_rate;
       }
+      // CTA-wide minimum of the modelled times, then the largest K within the slack
+      // (warp shuffles, then warp 0 over the warps' results)
+      const int nw = blockDim.x >> 5;
       float t_min = t_mine;
       for (int o = 16; o > 0; o >>= 1) t_min = fminf(t_min, __shfl_xor_sync(0xffffffffu, t_min, o));
       if (lane == 0) wbest_t[warp] = t_min;
       __syncthreads();
-      t_min = INFINITY;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t_min = fminf(t_min, wbest_t[w]);
+      if (warp == 0) {
+        float v = lane < nw ? wbest_t[lane] : INFINITY;
+        for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) wbest_t[32] = v;
+      }
+      __syncthreads();
+      t_min = wbest_t[32];
       int k_pick = t_min < INFINITY && t_mine <= t_min * (1.f + kSplitSlack) ? K : 0;
       for (int o = 16; o > 0; o >>= 1) k_pick = max(k_pick, __shfl_xor_sync(0xffffffffu, k_pick, o));
       if (lane == 0) wbest_k[warp] = k_pick;
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int kb = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) kb = max(kb, wbest_k[w]);
-        if (kb <= 0) kb = a.sms;
-        *a.active_ctas = kb;
+      if (warp == 0) {
+        int v = lane < nw ? wbest_k[lane] : 0;
+        for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) *a.active_ctas = v > 0 ? v : a.sms;
       }
       __syncthreads();
     }
@@ -1421,6 +1480,8 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restric
                                                         int route, int64_t cap, uint16_t* __restrict__ k_out,
                                                         uint16_t* __restrict__ v_out, int32_t* err) {
   constexpr int kPer = 4;  // 16-byte output vectors per lane and tensor in one round
+  // a programmatic dependent of the prep kernel: wait for its packed offsets
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.y;
   const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
   if (lq <= route) return;  // route: the routed query bound (0: none)
@@ -1771,8 +1832,21 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
     auto gk_kern = kv_dtype == PKV_FP8_E4M3 ? gather_kv_kernel<1>
                    : kv_dtype == PKV_INT8   ? gather_kv_kernel<2>
                                             : gather_kv_kernel<0>;
-    gk_kern<<<ggrid, 256, 0, st>>>(kc, vc, cu_seqlens_q, cu_seqlens_k, cu_g, block_table, max_blocks_per_seq,
-                                   block_size, num_blocks, row_elems, rmq, total_k, gk, gv, err_flag);
+    // a programmatic dependent of the prep (which triggers at its start): its
+    // launch and CTA start hide behind the prep
+    cudaLaunchConfig_t gcfg = {};
+    gcfg.gridDim = ggrid;
+    gcfg.blockDim = dim3(256);
+    gcfg.stream = st;
+    cudaLaunchAttribute gattr[1];
+    gattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    gattr[0].val.programmaticStreamSerializationAllowed = 1;
+    gcfg.attrs = gattr;
+    gcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&gcfg, gk_kern, kc, vc, cu_seqlens_q, cu_seqlens_k, (const int32_t*)cu_g, block_table,
+                           max_blocks_per_seq, block_size, num_blocks, row_elems, rmq, (int64_t)total_k, gk, gv,
+                           err_flag) != cudaSuccess)
+      return PKV_ERR_CUDA;
   }
   int rc = PKV_OK;
   if (all_routed)
