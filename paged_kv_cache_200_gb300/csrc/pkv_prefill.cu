@@ -1438,8 +1438,10 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
 // its cache slot to row cu_g[b] + j of a packed bf16 buffer, for K and V.  An
 // FP8 cache is widened exactly (every E4M3 value is a bf16 value; the scales
 // are applied by the attention).  Bad block ids are flagged and give zero rows;
-// rows at or past `cap` are not written.  CTA (t, b): positions
-// [kGatherPos t, kGatherPos (t + 1)), one warp per position at a time; a lane
+// rows at or past `cap` are not written.  CTA t: packed rows
+// [kGatherPos t, kGatherPos (t + 1)) (the grid covers the cap, so sequences
+// left to the decode kernels, which have no rows, cost nothing), one warp per
+// row at a time, which finds its sequence by a binary search over cu_g; a lane
 // issues all of its loads of a round (K and V) before its stores.
 constexpr int kGatherPos = 16;
 
@@ -1472,32 +1474,36 @@ __device__ __forceinline__ uint4 widen8_int8(uint2 codes) {
 template <int kMode>  // 0: bf16 rows, 1: E4M3 codes, 2: INT8 codes
 __global__ void __launch_bounds__(256) gather_kv_kernel(const uint8_t* __restrict__ k_cache,
                                                         const uint8_t* __restrict__ v_cache,
-                                                        const int32_t* __restrict__ cu_q,
-                                                        const int32_t* __restrict__ cu_k,
-                                                        const int32_t* __restrict__ cu_g,
+                                                        const int32_t* __restrict__ cu_g, int32_t batch,
                                                         const int32_t* __restrict__ block_table, int32_t max_blocks,
                                                         int32_t block_size, int32_t num_blocks, int32_t row_elems,
-                                                        int route, int64_t cap, uint16_t* __restrict__ k_out,
+                                                        int64_t cap, uint16_t* __restrict__ k_out,
                                                         uint16_t* __restrict__ v_out, int32_t* err) {
   constexpr int kPer = 4;  // 16-byte output vectors per lane and tensor in one round
   // a programmatic dependent of the prep kernel: wait for its packed offsets
+  // (cu_g: written by the prep; plain loads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.y;
-  const int lq = __ldg(cu_q + b + 1) - __ldg(cu_q + b);
-  if (lq <= route) return;  // route: the routed query bound (0: none)
-  int lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
-  if ((int64_t)lk > (int64_t)max_blocks * block_size) {  // more keys than the table holds
-    lk = max_blocks * block_size;
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, PKV_DEVERR_LENGTH);
-  }
-  const int j0 = blockIdx.x * kGatherPos;
-  if (j0 >= lk) return;
-  const int64_t g0 = __ldg(cu_g + b);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int64_t total = cu_g[batch];  // gathered rows; those at or past the buffer's cap are not
+  if (total > cap) total = cap;   // written (the prep flagged them)
   const int chunks = row_elems >> 3;  // 16-byte bf16 vectors per row
-  for (int j = j0 + warp; j < min(lk, j0 + kGatherPos); j += 8) {
-    const int64_t row = g0 + j;
-    if (row >= cap) break;
+  const int64_t cap_rows = (int64_t)max_blocks * block_size;
+  for (int64_t row = (int64_t)blockIdx.x * kGatherPos + warp; row < (int64_t)(blockIdx.x + 1) * kGatherPos;
+       row += 8) {
+    if (row >= total) break;
+    // the sequence of packed row `row`: the last b with cu_g[b] <= row (the
+    // sequences the prefill tiles do not serve have no rows)
+    int lo = 0, hi = batch;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)cu_g[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int64_t j = row - cu_g[b];  // key j of sequence b
+    if (j >= cap_rows) {  // more keys than the table holds: not gathered
+      if (lane == 0) flag_error(err, PKV_DEVERR_LENGTH);
+      continue;
+    }
     const int blk = __ldg(block_table + (int64_t)b * max_blocks + j / block_size);
     const bool bad = blk < 0 || blk >= num_blocks;
     if (bad && lane == 0) flag_error(err, PKV_DEVERR_BLOCK);
@@ -1822,8 +1828,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
   pa.err = err_flag;
   varlen_prep_kernel<<<1, 1024, 0, st>>>(pa);
   if (gather) {
-    const int gx = (max_len_k + kGatherPos - 1) / kGatherPos;
-    const dim3 ggrid((unsigned)(gx > 0 ? gx : 1), (unsigned)batch, 1);
+    const int64_t gx = ((int64_t)total_k + kGatherPos - 1) / kGatherPos;
+    const dim3 ggrid((unsigned)(gx > 0 ? gx : 1), 1, 1);
     const int row_elems = num_kv_heads * head_dim;
     uint16_t* gk = reinterpret_cast<uint16_t*>(wsb + wl.gk_off);
     uint16_t* gv = reinterpret_cast<uint16_t*>(wsb + wl.gv_off);
@@ -1843,8 +1849,8 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
     gattr[0].val.programmaticStreamSerializationAllowed = 1;
     gcfg.attrs = gattr;
     gcfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&gcfg, gk_kern, kc, vc, cu_seqlens_q, cu_seqlens_k, (const int32_t*)cu_g, block_table,
-                           max_blocks_per_seq, block_size, num_blocks, row_elems, rmq, (int64_t)total_k, gk, gv,
+    if (cudaLaunchKernelEx(&gcfg, gk_kern, kc, vc, (const int32_t*)cu_g, (int32_t)batch, block_table,
+                           max_blocks_per_seq, block_size, num_blocks, row_elems, (int64_t)total_k, gk, gv,
                            err_flag) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
