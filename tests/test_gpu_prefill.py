@@ -384,6 +384,28 @@ def test_gather_bound_too_small_is_flagged(pkv):
     assert int(err.item()) & 4  # PKV_DEVERR_LENGTH
 
 
+@pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
+def test_keys_past_the_block_table_are_flagged(pkv, gather):
+    """A sequence that claims more keys than its block-table row holds is flagged
+    (PKV_DEVERR_LENGTH); no key past the table is read, and the other sequence is exact."""
+    wl = W.make_varlen_paged([64, 40], [100, 30], 8, 2, 128, 16, seed=97, device="cuda")
+    kc, vc = _write_new_tokens(pkv, wl)
+    cap0 = wl.block_table.shape[1] * wl.block_size
+    cu_k = torch.tensor([0, cap0 + 14, cap0 + 14 + 70], dtype=torch.int32, device="cuda")
+    shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pkv.paged_attn_varlen(wl.q, kc.view(shape4), vc.view(shape4), wl.cu_seqlens_q, cu_k, wl.max_len_q,
+                                cap0 + 14, block_table=wl.block_table, scale=wl.scale, err_flag=err,
+                                gather_k_tokens=cap0 + 14 + 70 if gather else 0)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 4  # PKV_DEVERR_LENGTH
+    ref, _ = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                 wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                 block_table=wl.block_table.cpu().numpy(), block_size=16, seqs=[1])
+    rows = np.arange(64, 104)
+    assert_close(f64(out)[rows], ref[rows], BF16_ATOL, BF16_RTOL, "sequence 1")
+
+
 def test_more_queries_than_max_len_q_is_flagged(pkv):
     """A sequence with more queries than the caller's max_len_q is flagged (PKV_DEVERR_LENGTH); the tiles
     that the bound covers (those with the most keys, counted from the sequence's end) are still exact."""
