@@ -1271,8 +1271,8 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const PrepArgs a) {
   if (a.cu_g != nullptr) {
     // Packed offsets of the gathered sequences (those the prefill kernel
     // serves: more than one query, or any query when nothing is routed):
-    // cu_g[b] = sum of their key counts before b.  Exclusive scan, one
-    // 32-sequence chunk per warp step, carried across passes.
+    // cu_g[b] = sum of their key counts before b.  An exclusive scan over the
+    // CTA per chunk of blockDim sequences, carried across chunks.
     __shared__ int64_t scan_ws[33];
     for (int base = 0; base < a.batch; base += blockDim.x) {
       const int b = base + threadIdx.x;
