@@ -94,6 +94,18 @@ PKV_API const char* pkv_status_string(int status);
 PKV_API int pkv_abi_version(void);
 
 /*
+ * Tracing (no counterpart on the source pages; a profiling aid of this library).
+ * on != 0: the compute entry points below (write, decode, decode with append,
+ * varlen, block copy; not the decode without a workspace, which must allocate
+ * nothing, and an attached tool may) open an NVTX range named after themselves
+ * for the host-side span of the call, which holds its launches, so that a
+ * timeline tool shows the library's calls; on == 0 (the default): no range, one
+ * relaxed atomic load per call.  Without a tool attached, a range is a no-op.
+ * Process-wide; thread-safe.
+ */
+PKV_API void pkv_set_nvtx(int on);
+
+/*
  * KV-cache write ([KVM] "Triton カーネルによる KV キャッシュ書き込み"; checks from
  * "Python 層からのカーネル呼び出し").
  *

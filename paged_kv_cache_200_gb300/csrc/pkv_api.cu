@@ -1,12 +1,25 @@
-// libpkv: status strings, version, device queries shared by the entry points.
+// libpkv: status strings, version, device queries and tracing shared by the entry points.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pkv.h"
 #include "pkv_host.h"
 
 namespace pkv {
+
+namespace {
+std::atomic<int> g_nvtx{0};  // pkv_set_nvtx
+}  // namespace
+
+NvtxRange::NvtxRange(const char* name) : on(g_nvtx.load(std::memory_order_relaxed) != 0) {
+  if (on) nvtxRangePushA(name);
+}
+NvtxRange::~NvtxRange() {
+  if (on) nvtxRangePop();
+}
 
 int device_sm_count() {
   static std::mutex mu;
@@ -121,3 +134,5 @@ extern "C" const char* pkv_status_string(int status) {
 }
 
 extern "C" int pkv_abi_version(void) { return 2; }
+
+extern "C" void pkv_set_nvtx(int on) { pkv::g_nvtx.store(on != 0 ? 1 : 0, std::memory_order_relaxed); }

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint8_t* __re
 
 extern "C" int pkv_copy_blocks(void* k_cache, void* v_cache, int64_t block_bytes, int32_t num_blocks,
                                const int32_t* block_pairs, int32_t num_pairs, int32_t* err_flag, void* stream) {
+  const pkv::NvtxRange nvtx_range("pkv_copy_blocks");
   using namespace pkv;
   if (num_pairs < 0 || num_blocks <= 0 || block_bytes <= 0) return PKV_ERR_INVALID_ARG;
   if (block_bytes % 16 != 0) return PKV_ERR_INVALID_ARG;

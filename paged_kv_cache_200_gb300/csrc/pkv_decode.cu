@@ -1009,6 +1009,7 @@ extern "C" int pkv_paged_attn_decode(const void* q, const void* k_cache, const v
                                      int32_t num_blocks, int32_t max_seqlen_k, float scale, float k_scale,
                                      float v_scale, void* out, float* lse, void* workspace,
                                      size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  const pkv::NvtxRange nvtx_range("pkv_paged_attn_decode");
   return pkv::decode_impl(q, k_cache, v_cache, cache_dtype, cache_seqlens, block_table, max_blocks_per_seq, batch,
                           num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_seqlen_k, scale, k_scale,
                           v_scale, out, lse, workspace, workspace_bytes, err_flag, stream, nullptr);
@@ -1024,6 +1025,7 @@ extern "C" int pkv_paged_attn_decode_with_kvcache(const void* q, const void* k_n
                                                   float k_inv_scale, float v_inv_scale, void* out, float* lse,
                                                   void* workspace, size_t workspace_bytes, int32_t* err_flag,
                                                   void* stream) {
+  const pkv::NvtxRange nvtx_range("pkv_paged_attn_decode_with_kvcache");
   using namespace pkv;
   // a one-byte cache needs finite positive inverse scales, even when there is nothing to do
   if (cache_dtype != PKV_BF16 && (!(k_inv_scale > 0.f) || !(v_inv_scale > 0.f) || !std::isfinite(k_inv_scale) ||

@@ -20,6 +20,15 @@ inline int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? PKV_O
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// An NVTX range over an entry point's call when tracing is on (pkv_set_nvtx).
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char* name);
+  ~NvtxRange();
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // Tensor map over a [rows, heads, dim] array of `elt_bytes`-byte elements
 // (bf16 = 2, e4m3 = 1), boxes of box_inner elements x 1 head x box_rows rows,
 // swizzle of 128 or 64 bytes (or 0 for none).  False if the driver refuses it.

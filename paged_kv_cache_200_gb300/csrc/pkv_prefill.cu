@@ -1693,6 +1693,7 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
                                      float scale, int32_t causal, float k_scale, float v_scale, void* out,
                                      float* lse, void* workspace, size_t workspace_bytes, int32_t* err_flag,
                                      void* stream) {
+  const pkv::NvtxRange nvtx_range("pkv_paged_attn_varlen");
   using namespace pkv;
   if (batch < 0 || total_q < 0 || total_k < 0 || max_len_q < 0 || max_len_k < 0 || num_heads <= 0 ||
       num_kv_heads <= 0)

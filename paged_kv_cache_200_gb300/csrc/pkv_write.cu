@@ -76,6 +76,7 @@ extern "C" int pkv_kv_cache_write(const void* k, int64_t k_row_stride, const voi
                                   void* v_cache, int32_t cache_dtype, int64_t num_slots,
                                   const int32_t* slot_mapping, float k_inv_scale, float v_inv_scale,
                                   int32_t* err_flag, void* stream) {
+  const pkv::NvtxRange nvtx_range("pkv_kv_cache_write");
   using namespace pkv;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_slots <= 0) return PKV_ERR_INVALID_ARG;
   if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;

@@ -47,6 +47,7 @@ _SIGNATURES = {
         _c_void_p, _f32, _f32, _c_void_p, _c_void_p]),
     "pkv_copy_blocks": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i32, _c_void_p, _i32, _c_void_p, _c_void_p]),
     "pkv_paged_attn_decode_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "pkv_set_nvtx": (None, [_i32]),
     "pkv_paged_attn_decode": (ctypes.c_int, [
         _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _i32,
         _i32, _i32, _i32, _f32, _f32, _f32, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p, _c_void_p]),
@@ -98,6 +99,11 @@ def lib(path: str = LIB_PATH):
                 fn.argtypes = args
         _lib = handle
     return _lib
+
+
+def set_nvtx(on: bool = True):
+    """Turn the library's NVTX ranges (one per compute call, named after the C entry point) on or off."""
+    lib().pkv_set_nvtx(1 if on else 0)
 
 
 def _check(status: int):

@@ -235,3 +235,22 @@ def test_split_plan_ends_long_contexts_on_whole_waves():
     c = _split_plan(8, 8, 131073, 152, 2)
     assert c == 6912 and -(-131073 // c) == 19
     assert (8 * 8 * 19) % (152 * 2) == 0
+
+
+def test_nvtx_ranges_switch_on_and_off_around_calls():
+    """Tracing on, calls that return before any launch (nothing to do, or refused), tracing off:
+    the ranges open and close without a tool attached."""
+    pkv = built_library()
+    lib = pkv.lib()
+    nul = ctypes.c_void_p(0)
+    pkv.set_nvtx(True)
+    try:
+        assert lib.pkv_kv_cache_write(nul, 128, nul, 128, 0, 1, 128, nul, nul, 0, 16, nul, 1.0, 1.0, nul, nul) == 0
+        assert lib.pkv_kv_cache_write(nul, 128, nul, 128, -1, 1, 128, nul, nul, 0, 16, nul, 1.0, 1.0, nul, nul) == 1
+        assert lib.pkv_copy_blocks(nul, nul, 16, 1, nul, 0, nul, nul) == 0
+        assert lib.pkv_paged_attn_decode(nul, nul, nul, 0, nul, nul, 4, 1, 8, 3, 128, 16, 8, 64, 0.1, 1.0, 1.0,
+                                         nul, nul, nul, 0, nul, nul) == 1
+        assert lib.pkv_paged_attn_varlen(nul, nul, nul, 1, nul, nul, 4, 16, 0, 4, 64, nul, 8, 16, 64, 8, 2, 128,
+                                         0.1, 1, 1.0, 1.0, nul, nul, nul, 0, nul, nul) == 2
+    finally:
+        pkv.set_nvtx(False)
