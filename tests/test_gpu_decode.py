@@ -240,3 +240,30 @@ def test_decode_batch64_full_size_sampled(pkv):
 def test_long_decode_full_size_sampled(pkv, dt):
     wl = W.long_decode(device="cuda", cache_dtype=dt)
     _full_size(pkv, wl, [0, 5])
+
+
+def test_nvtx_tracing_changes_no_result(pkv):
+    """With NVTX ranges on, the write, decode and varlen calls give the same bits as with them off."""
+    wl = W.decode_example(device="cuda")
+    vw = W.make_varlen_packed([200, 1, 131], [200, 7, 300], 8, 2, 128, seed=77, device="cuda")
+
+    def run():
+        out, lse, kc, vc = _gpu_step(pkv, wl)
+        vo, vl = pkv.paged_attn_varlen(vw.q, vw.k, vw.v, vw.cu_seqlens_q, vw.cu_seqlens_k, vw.max_len_q,
+                                       vw.max_len_k, scale=vw.scale, return_lse=True)
+        torch.cuda.synchronize()
+        return out, lse, kc, vc, vo, vl
+
+    plain = run()
+    pkv.set_nvtx(True)
+    try:
+        traced = run()
+    finally:
+        pkv.set_nvtx(False)
+    for a, b in zip(plain, traced):  # byte for byte (lse is float32)
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+    rk, rv = O.kv_cache_write(bits(wl.k_new), bits(wl.v_new), bits(wl.k_cache), bits(wl.v_cache),
+                              wl.slot_mapping.cpu().numpy())
+    assert np.array_equal(bits(traced[2]), rk) and np.array_equal(bits(traced[3]), rv)
+    ref, ref_lse = _oracle(wl, rk, rv)
+    _check(wl, traced[0], traced[1], ref, ref_lse)
