@@ -32,7 +32,8 @@ def assert_close(got, ref, atol, rtol, what=""):
     assert got.shape == ref.shape, (got.shape, ref.shape)
     mask = ~np.isnan(ref)
     both_inf = np.isinf(ref) & (got == ref)
-    err = np.where(mask & ~both_inf, np.abs(got - ref), 0.0)
+    with np.errstate(invalid="ignore"):  # inf - inf where got and ref are opposite infinities: flagged below
+        err = np.where(mask & ~both_inf, np.abs(got - ref), 0.0)
     bound = atol + rtol * np.abs(np.where(np.isfinite(ref), ref, 0.0))
     bad = mask & ~both_inf & ~(err <= bound)
     if bad.any():
