@@ -384,26 +384,27 @@ def test_gather_bound_too_small_is_flagged(pkv):
     assert int(err.item()) & 4  # PKV_DEVERR_LENGTH
 
 
-def test_packed_batch_larger_than_the_prep_cta(pkv):
-    """1100 packed sequences of 1..40 queries (more than the prep kernel's 1024 threads: the
-    unit list over several sequences per thread): every row against the oracle."""
+@pytest.mark.parametrize("batch", [1100, 2300])
+def test_packed_batch_larger_than_the_prep_cta(pkv, batch):
+    """1100 or 2300 packed sequences of 1..40 queries (more than the prep kernel's 1024 threads:
+    the unit list over two or three sequences per thread): every row against the oracle."""
     rng = np.random.default_rng(31)
-    lq = rng.integers(1, 41, size=1100)
-    lk = lq + rng.integers(0, 30, size=1100)
+    lq = rng.integers(1, 41, size=batch)
+    lk = lq + rng.integers(0, 30, size=batch)
     wl = W.make_varlen_packed(list(lq), list(lk), 8, 2, 64, seed=32, device="cuda")
     out, lse = _packed(pkv, wl)
     ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(wl.k), bits(wl.v), wl.cu_seqlens_q.cpu().numpy(),
                                        wl.cu_seqlens_k.cpu().numpy(), wl.scale, True)
-    _check_rows(out, lse, ref, ref_lse, what="1100 packed sequences")
+    _check_rows(out, lse, ref, ref_lse, what=f"{batch} packed sequences")
 
 
+@pytest.mark.parametrize("n_dec", [1300, 2400])
 @pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
-def test_mixed_batch_larger_than_the_prep_cta(pkv, gather):
-    """Three chunks among 1300 decode rows (more than the prep kernel's 1024 threads: routing,
-    packed offsets carried across chunks of sequences, the unit list and the SM split over
-    them): every row against the oracle."""
+def test_mixed_batch_larger_than_the_prep_cta(pkv, gather, n_dec):
+    """Three chunks among 1300 or 2400 decode rows (more than the prep kernel's 1024 threads:
+    routing, packed offsets carried across two or three chunks of sequences, the unit list and
+    the SM split over them): every row against the oracle."""
     rng = np.random.default_rng(33)
-    n_dec = 1300
     q_lens = np.ones(n_dec + 3, dtype=np.int64)
     prefix = rng.integers(8, 96, size=n_dec + 3)
     pos = rng.choice(n_dec + 3, size=3, replace=False)  # the chunks sit among the decode rows
@@ -415,7 +416,7 @@ def test_mixed_batch_larger_than_the_prep_cta(pkv, gather):
     ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
                                        wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
                                        block_table=wl.block_table.cpu().numpy(), block_size=16)
-    _check_rows(out, lse, ref, ref_lse, what=f"1303-sequence mixed batch ({'gathered' if gather else 'direct'})")
+    _check_rows(out, lse, ref, ref_lse, what=f"{n_dec + 3}-sequence mixed batch ({'gathered' if gather else 'direct'})")
 
 
 @pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
