@@ -59,6 +59,8 @@ constexpr int kThreadsCoded = 384;  // one-byte caches: + a widening warp
 constexpr int kWidenWarp = 11;
 constexpr int kSoftmaxWarp0 = 3;  // first softmax warp (tile A: warps 3..6, tile B: 7..10)
 constexpr int kGroupThreads = 128;  // a softmax warp group: one thread per row of its tile
+constexpr int kSoftmaxThreads = 256;  // all softmax warps (one group per tile, or all on one tile)
+constexpr int kUnifiedKeys = 4096;    // key bound from which the one-tile-at-a-time softmax runs
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -174,7 +176,7 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // shared-memory plan
 // ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool kUnified = false>  // kUnified: the one-tile softmax's larger per-thread areas
 struct Smem {
   static constexpr int kAtoms = D / 64;                 // 64-element (128-byte) column groups
   static constexpr int kTileBytes = 128 * D * 2;        // a [128 x D] bf16 tile
@@ -186,11 +188,12 @@ struct Smem {
   static constexpr int kNumBars = 40;
   static constexpr int kMisc = kBar + kNumBars * 8;     // tmem holder, abort flag
   static constexpr int kRingData = kMisc + 16;          // 4 ring slots x 8 ints (item, q0, Lq, k0, Lk)
-  static constexpr int kEpi = kRingData + 4 * 32;       // per softmax thread: output and lse offsets, rows (32 B)
-  static constexpr int kTotal = kEpi + 2 * kGroupThreads * 32;
+  static constexpr int kEpi = kRingData + 4 * 32;       // per tile and softmax thread: output and lse offsets, rows (32 B)
+  static constexpr int kXch = kEpi + 2 * (kUnified ? kSoftmaxThreads : kGroupThreads) * 32;
+  static constexpr int kTotal = kXch + (kUnified ? 2 * kSoftmaxThreads * 4 : 0);  // 2 rounds x 256 floats swapped by row halves
   static constexpr int kAlloc = kTotal + 1024;          // slack to align the base to 1024
 };
-static_assert(Smem<128>::kAlloc <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
+static_assert(Smem<128, true>::kAlloc <= 227 * 1024, "shared memory plan exceeds a CTA's limit");
 
 constexpr int kRing = 4;  // work-item ring slots
 
@@ -216,14 +219,15 @@ enum Bar {
   kQReady0 = 32,     // +X: one-byte caches: Q converted to f16 in place (producer -> MMA)
   kKReady0 = 34,     // +stage: one-byte caches: K widened to f16 in place (producer -> MMA)
   kVReady0 = 36,     // +stage: one-byte caches: V widened to f16 in place (producer -> MMA)
-  kBarCount = 38
+  kXch0 = 38,        // row halves: a round of swapped values written (256 arrivals; one-tile softmax)
+  kBarCount = 39
 };
 static_assert(kQEmpty0 == kQFull0 + 2 && kKFull0 == kQEmpty0 + 2 && kKEmpty0 == kKFull0 + 2 &&
                   kVFull0 == kKEmpty0 + 2 && kVEmpty0 == kVFull0 + 2 && kSFull0 == kVEmpty0 + 2 &&
                   kPFull0 == kSFull0 + 2 && kODone0 == kPFull0 + 2 && kOFree0 == kODone0 + 2 &&
                   kRingFull0 == kOFree0 + 2 && kRingEmpty0 == kRingFull0 + kRing && kDrain0 == kRingEmpty0 + kRing &&
                   kTurn0 == kDrain0 + 2 && kQReady0 == kTurn0 + 2 && kKReady0 == kQReady0 + 2 &&
-                  kVReady0 == kKReady0 + 2 && kBarCount == kVReady0 + 2,
+                  kVReady0 == kKReady0 + 2 && kXch0 == kVReady0 + 2 && kBarCount == kXch0 + 1,
               "mbarrier index ranges must not overlap");
 static_assert(Smem<128>::kNumBars >= kBarCount && Smem<64>::kNumBars >= kBarCount, "too few mbarrier slots");
 
@@ -421,11 +425,11 @@ __device__ __forceinline__ void widen_kv_f16(uint8_t* stage, int lane) {
 // tiles) so the barriers' phases continue across items.
 // kCode: 0 bf16 K/V (packed or paged); 1 E4M3, 2 INT8 codes (paged, d128),
 // widened to f16 in shared memory by the producer warp.
-template <int D, bool kPaged, int kCode>
+template <int D, bool kPaged, int kCode, bool kUnified = false>
 __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
     varlen_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using L = Smem<D>;
+  using L = Smem<D, kUnified>;
   constexpr bool kCoded = kCode != 0;
   static_assert(!kCoded || (kPaged && D == 128), "one-byte K/V tiles: paged, head dim 128");
   // the MMA threads wait for a landed tile (bf16) or for its widening (one-byte codes)
@@ -462,10 +466,11 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
       mbar_init(bar(kVFull0 + x), 1);
       mbar_init(bar(kVEmpty0 + x), 2);
       mbar_init(bar(kSFull0 + x), 1);
-      mbar_init(bar(kPFull0 + x), kGroupThreads);
+      mbar_init(bar(kPFull0 + x), kUnified ? kSoftmaxThreads : kGroupThreads);
       mbar_init(bar(kODone0 + x), 1);
-      mbar_init(bar(kOFree0 + x), kGroupThreads);
+      mbar_init(bar(kOFree0 + x), kUnified ? kSoftmaxThreads : kGroupThreads);
     }
+    mbar_init(bar(kXch0), kSoftmaxThreads);
     mbar_init(bar(kDrain0), 1);
     mbar_init(bar(kDrain0 + 1), 1);
     mbar_init(bar(kTurn0), kGroupThreads / 32);
@@ -861,201 +866,396 @@ __global__ void __launch_bounds__(kCode ? kThreadsCoded : kThreads, 1)
     }
     __syncwarp();  // the warp reconverges before the CTA barrier below
   } else if (!kCoded || warp < kWidenWarp) {
-    // ------------------------------------------------------------------ softmax warps
-    const int xq = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warp group
-    const int quarter = warp & 3;       // TMEM lanes this warp may access
-    const int r = quarter * 32 + lane;  // TMEM lane == query row in the tile
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const float c = p.scale_log2;
-    bool ok = true;
-    int sc = 0, oc = 0;  // S tiles and items (with keys) processed
-    int tc = 0;          // tiles processed in turn with the other group
-    for (int u = 0; ok; ++u) {
-      SeqBase si;
-      Item x;
-      const int it = ring_get(u, si, x);
-      if (it < 0) break;
-      // Only a few values live across the tile loop (the 128 scores need the
-      // registers): the output offsets, the row limits and the loop counts.
-      int rows, nkv, vis0, jm;
-      int64_t obase, lse_idx;  // this tile's first output element; this row's lse index
-      int nturn;  // tiles taken in turn with the other group: the first n[0]
-      {
-        const Seq sq = seq_derive(p, si, x.pair);
-        // (selects, not an indexed load: xq differs between warps but the arrays stay in registers)
-        rows = xq ? sq.rows[1] : sq.rows[0];
-        const int row0 = xq ? sq.row0[1] : sq.row0[0];
-        nkv = xq ? sq.n[1] : sq.n[0];
-        const int head = xq ? x.head_b : x.head * (1 + p.head_pairs);  // tile_head(p, x.head, xq)
-        obase = ((int64_t)(sq.q0 + row0) * p.num_heads + head) * D;
-        lse_idx = (int64_t)head * p.total_q + sq.q0 + row0 + r;
-        // key limit of this row (bottom-right causal, inside the keys); tiles
-        // before jm need no mask for any row of the tile (its first row has
-        // the smallest limit)
-        vis0 = min(row0 + r + sq.diag, sq.Lk - 1);
-        const int first = row0 + sq.diag;  // limit of the tile's first row
-        jm = min(first < kBN - 1 ? 0 : (first + 1) / kBN, sq.Lk / kBN);
-        // While both tiles have K/V tiles left, the two groups take turns, tile
-        // by tile (A0, B0, A1, B1, ...): each softmax then has the SM's
-        // sub-partitions to itself, and while one group works the other tile's
-        // MMAs run.  Tile B's tiles past A's last one run without turns.
-        nturn = sq.n[0];
-      }
-      if (rows <= 0) continue;
-      // the offsets wait in shared memory while the tile loop runs (registers)
-      int64_t* epi = reinterpret_cast<int64_t*>(smem + L::kEpi) + 4 * (threadIdx.x - kSoftmaxWarp0 * 32);
-      epi[0] = obase;
-      epi[1] = lse_idx;
-      epi[2] = rows;
-      if (nkv == 0) {
-        const bool row_valid = r < rows;
-        // rows that see no key: zeros and lse = -inf
-        if (row_valid) {
-          uint16_t* orow = p.out + obase + (int64_t)r * p.num_heads * D;
-          for (int cc = 0; cc < D / 8; ++cc) reinterpret_cast<uint4*>(orow)[cc] = make_uint4(0, 0, 0, 0);
-          if (p.lse) p.lse[lse_idx] = -INFINITY;
+    if constexpr (!kUnified) {
+      // ------------------------------------------------------------------ softmax warps
+      const int xq = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warp group
+      const int quarter = warp & 3;       // TMEM lanes this warp may access
+      const int r = quarter * 32 + lane;  // TMEM lane == query row in the tile
+      const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+      const float c = p.scale_log2;
+      bool ok = true;
+      int sc = 0, oc = 0;  // S tiles and items (with keys) processed
+      int tc = 0;          // tiles processed in turn with the other group
+      for (int u = 0; ok; ++u) {
+        SeqBase si;
+        Item x;
+        const int it = ring_get(u, si, x);
+        if (it < 0) break;
+        // Only a few values live across the tile loop (the 128 scores need the
+        // registers): the output offsets, the row limits and the loop counts.
+        int rows, nkv, vis0, jm;
+        int64_t obase, lse_idx;  // this tile's first output element; this row's lse index
+        int nturn;  // tiles taken in turn with the other group: the first n[0]
+        {
+          const Seq sq = seq_derive(p, si, x.pair);
+          // (selects, not an indexed load: xq differs between warps but the arrays stay in registers)
+          rows = xq ? sq.rows[1] : sq.rows[0];
+          const int row0 = xq ? sq.row0[1] : sq.row0[0];
+          nkv = xq ? sq.n[1] : sq.n[0];
+          const int head = xq ? x.head_b : x.head * (1 + p.head_pairs);  // tile_head(p, x.head, xq)
+          obase = ((int64_t)(sq.q0 + row0) * p.num_heads + head) * D;
+          lse_idx = (int64_t)head * p.total_q + sq.q0 + row0 + r;
+          // key limit of this row (bottom-right causal, inside the keys); tiles
+          // before jm need no mask for any row of the tile (its first row has
+          // the smallest limit)
+          vis0 = min(row0 + r + sq.diag, sq.Lk - 1);
+          const int first = row0 + sq.diag;  // limit of the tile's first row
+          jm = min(first < kBN - 1 ? 0 : (first + 1) / kBN, sq.Lk / kBN);
+          // While both tiles have K/V tiles left, the two groups take turns, tile
+          // by tile (A0, B0, A1, B1, ...): each softmax then has the SM's
+          // sub-partitions to itself, and while one group works the other tile's
+          // MMAs run.  Tile B's tiles past A's last one run without turns.
+          nturn = sq.n[0];
         }
-        continue;
-      }
-      float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nkv; ++j) {
-        if (!mbar_wait(bar(kSFull0 + xq), sc & 1, abort_flag)) { ok = false; break; }
-        ++sc;
-        if (j < nturn) {  // tile A waits for B's previous tile, tile B for A's current one
-          const int need = xq == 0 ? tc - 1 : tc;
-          if (need >= 0 && !mbar_wait(bar(kTurn0 + xq), need & 1, abort_flag)) { ok = false; break; }
+        if (rows <= 0) continue;
+        // the offsets wait in shared memory while the tile loop runs (registers)
+        int64_t* epi = reinterpret_cast<int64_t*>(smem + L::kEpi) + 4 * (threadIdx.x - kSoftmaxWarp0 * 32);
+        epi[0] = obase;
+        epi[1] = lse_idx;
+        epi[2] = rows;
+        if (nkv == 0) {
+          const bool row_valid = r < rows;
+          // rows that see no key: zeros and lse = -inf
+          if (row_valid) {
+            uint16_t* orow = p.out + obase + (int64_t)r * p.num_heads * D;
+            for (int cc = 0; cc < D / 8; ++cc) reinterpret_cast<uint4*>(orow)[cc] = make_uint4(0, 0, 0, 0);
+            if (p.lse) p.lse[lse_idx] = -INFINITY;
+          }
+          continue;
         }
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < nkv; ++j) {
+          if (!mbar_wait(bar(kSFull0 + xq), sc & 1, abort_flag)) { ok = false; break; }
+          ++sc;
+          if (j < nturn) {  // tile A waits for B's previous tile, tile B for A's current one
+            const int need = xq == 0 ? tc - 1 : tc;
+            if (need >= 0 && !mbar_wait(bar(kTurn0 + xq), need & 1, abort_flag)) { ok = false; break; }
+          }
+          tc_fence_after();
+          // All 128 scores of the row in one TMEM round trip; P of keys 64..127
+          // goes to columns 64..95 and of keys 0..63 to columns 0..31 (each half
+          // over S columns already read; columns 32..63 and 96..127 are unused).
+          const int key0 = j * kBN;
+          uint32_t sr[kBN];
+          PKV_TMEM_LD32(tS(xq) + lane_off + 0, (sr + 0));
+          PKV_TMEM_LD32(tS(xq) + lane_off + 32, (sr + 32));
+          PKV_TMEM_LD32(tS(xq) + lane_off + 64, (sr + 64));
+          PKV_TMEM_LD32(tS(xq) + lane_off + 96, (sr + 96));
+          tmem_wait_ld();
+          if (j >= jm) {
+            const int vis = vis0 - key0;  // columns 0..vis are visible
+  #pragma unroll
+            for (int k = 0; k < kBN; ++k) sr[k] = (k <= vis) ? sr[k] : __float_as_uint(-INFINITY);
+          }
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+          for (int k = 0; k < kBN; k += 2)
+            mx4[(k >> 1) & 3] = fmax3(mx4[(k >> 1) & 3], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+          const float mt = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c;
+          float m_use = m;
+          if (mt > m + kRescaleThreshold || (m == -INFINITY && mt != -INFINITY)) m_use = mt;
+          const bool live = m_use != -INFINITY;
+          const bool moved = m_use != m;
+          const float alpha = (moved && m != -INFINITY) ? fast_exp2(m - m_use) : (moved ? 0.f : 1.f);
+          // p = 2^(s*c - m) on fp32 pairs; a row that saw no key yet (m = -inf) gives 0
+          const float nm = live ? -m_use : -INFINITY;
+          const uint64_t c2 = f32x2_pack(c, c), nm2 = f32x2_pack(nm, nm);
+          uint64_t sum2[2] = {0ull, 0ull};
+  #pragma unroll
+          for (int h = 1; h >= 0; --h) {
+            // P of keys 64h..64h+63 as bf16 pairs, packed in place over the scores just used
+            uint32_t* pk = sr + 64 * h;
+  #pragma unroll
+            for (int k = 0; k < 64; k += 2) {
+              float x0, x1;
+              f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(pk[k]), __uint_as_float(pk[k + 1])), c2, nm2), x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              sum2[(k >> 1) & 1] = fadd2(sum2[(k >> 1) & 1], f32x2_pack(p0, p1));
+              pk[k >> 1] = kCoded ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            }
+            PKV_TMEM_ST32(tS(xq) + lane_off + 64 * h, pk);
+          }
+          float s00, s01, s10, s11;
+          f32x2_unpack(sum2[0], s00, s01);
+          f32x2_unpack(sum2[1], s10, s11);
+          l = l * alpha + ((s00 + s01) + (s10 + s11));
+          m = m_use;
+          // rescale O_X when this row's reference max moved (warp-collective TMEM
+          // access).  PV_X of the previous tile is done: it was issued before this
+          // tile's S, whose completion was just waited for.
+          if (j > 0 && __any_sync(0xffffffffu, moved && alpha != 1.f)) {
+  #pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t o[32];
+              PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o);
+              tmem_wait_ld();
+  #pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              PKV_TMEM_ST32(tO(xq) + lane_off + ch * 32, o);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(kPFull0 + xq));
+          if (j < nturn) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kTurn0 + (xq ^ 1)));
+            ++tc;
+          }
+        }
+        if (!ok) break;
+        // ---- epilogue: O_X / l, released as soon as it is read, then stored ----
+        if (!mbar_wait(bar(kODone0 + xq), oc & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ++oc;
         tc_fence_after();
-        // All 128 scores of the row in one TMEM round trip; P of keys 64..127
-        // goes to columns 64..95 and of keys 0..63 to columns 0..31 (each half
-        // over S columns already read; columns 32..63 and 96..127 are unused).
-        const int key0 = j * kBN;
-        uint32_t sr[kBN];
-        PKV_TMEM_LD32(tS(xq) + lane_off + 0, (sr + 0));
-        PKV_TMEM_LD32(tS(xq) + lane_off + 32, (sr + 32));
-        PKV_TMEM_LD32(tS(xq) + lane_off + 64, (sr + 64));
-        PKV_TMEM_LD32(tS(xq) + lane_off + 96, (sr + 96));
-        tmem_wait_ld();
-        if (j >= jm) {
-          const int vis = vis0 - key0;  // columns 0..vis are visible
-#pragma unroll
-          for (int k = 0; k < kBN; ++k) sr[k] = (k <= vis) ? sr[k] : __float_as_uint(-INFINITY);
+        const float inv = l > 0.f ? p.v_mul / l : 0.f;
+        obase = epi[0];
+        lse_idx = epi[1];
+        const bool row_valid = r < (int)epi[2];
+        // O, normalised, packed to bf16 and stored 32 columns at a time; O is
+        // released once read.  Head dim 64: the whole row in one TMEM round trip
+        // (64 registers).  Head dim 128: chunk by chunk, so that no 128-register
+        // row is live (that spilled and cost 2-6 %).
+        uint4* orow = reinterpret_cast<uint4*>(p.out + obase + (int64_t)r * p.num_heads * D);
+        constexpr int kOneTrip = D <= 64;
+        uint32_t o_all[kOneTrip ? D : 32];
+        if constexpr (kOneTrip) {
+  #pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, (o_all + ch * 32));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(kOFree0 + xq));
         }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int k = 0; k < kBN; k += 2)
-          mx4[(k >> 1) & 3] = fmax3(mx4[(k >> 1) & 3], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
-        const float mt = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c;
-        float m_use = m;
-        if (mt > m + kRescaleThreshold || (m == -INFINITY && mt != -INFINITY)) m_use = mt;
-        const bool live = m_use != -INFINITY;
-        const bool moved = m_use != m;
-        const float alpha = (moved && m != -INFINITY) ? fast_exp2(m - m_use) : (moved ? 0.f : 1.f);
-        // p = 2^(s*c - m) on fp32 pairs; a row that saw no key yet (m = -inf) gives 0
-        const float nm = live ? -m_use : -INFINITY;
-        const uint64_t c2 = f32x2_pack(c, c), nm2 = f32x2_pack(nm, nm);
-        uint64_t sum2[2] = {0ull, 0ull};
-#pragma unroll
-        for (int h = 1; h >= 0; --h) {
-          // P of keys 64h..64h+63 as bf16 pairs, packed in place over the scores just used
-          uint32_t* pk = sr + 64 * h;
-#pragma unroll
+  #pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          const uint32_t* o = o_all + (kOneTrip ? ch * 32 : 0);
+          if constexpr (!kOneTrip) {
+            PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o_all);
+            tmem_wait_ld();
+            if (ch == D / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(bar(kOFree0 + xq));
+            }
+          }
+          if (row_valid) {
+            uint32_t w[16];
+  #pragma unroll
+            for (int k = 0; k < 16; ++k)
+              w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+            if (p.out_v8) {  // whole 32-byte sectors, half the store instructions
+  #pragma unroll
+              for (int h = 0; h < 2; ++h)
+                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + ch * 4 + 2 * h),
+                             "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
+                             "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                             : "memory");
+            } else {
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) orow[ch * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            }
+          }
+        }
+        if (row_valid && p.lse != nullptr) p.lse[lse_idx] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      }
+      if (!ok) fail();
+      tc_fence_before();
+    } else {
+      // ------------------------------------------------------------------ softmax warps
+      // All eight warps work on one tile at a time, A then B, K/V tile by K/V
+      // tile (A0, B0, A1, B1, ...): while they run one tile's softmax the other
+      // tile's MMAs run.  Warps 3..6 take keys 0..63 of their rows, warps 7..10
+      // keys 64..127 (TMEM lanes (warp % 4) * 32 + lane in both): two warps per
+      // sub-partition share each row, swapping the row maxima through shared
+      // memory; the row sums are combined once, at the epilogue.
+      const int tid = threadIdx.x - kSoftmaxWarp0 * 32;  // 0..255
+      const int hk = tid >> 7;                            // key half of this thread
+      const int quarter = warp & 3;       // TMEM lanes this warp may access
+      const int r = quarter * 32 + lane;  // TMEM lane == query row in the tile
+      const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+      const float c = p.scale_log2;
+      volatile float* xch = reinterpret_cast<volatile float*>(smem + L::kXch);  // [2][256]
+      bool ok = true;
+      int sc[2] = {0, 0}, oc[2] = {0, 0};  // S tiles and items (with keys) processed, per tile
+      int xc = 0;                          // exchanges with the other half
+      // this thread's value v for exchange round xc, plus the partner's
+      auto exchange = [&](float v) -> float {
+        xch[(xc & 1) * kSoftmaxThreads + tid] = v;
+        mbar_arrive(bar(kXch0));
+        if (!mbar_wait(bar(kXch0), xc & 1, abort_flag)) ok = false;
+        const float o = xch[(xc & 1) * kSoftmaxThreads + (tid ^ 128)];
+        ++xc;
+        return o;
+      };
+      for (int u = 0; ok; ++u) {
+        SeqBase si;
+        Item x;
+        const int it = ring_get(u, si, x);
+        if (it < 0) break;
+        int rows[2], nkv[2], vis0[2], jm[2];
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        {
+          const Seq sq = seq_derive(p, si, x.pair);
+  #pragma unroll
+          for (int xq = 0; xq < 2; ++xq) {
+            rows[xq] = sq.rows[xq];
+            nkv[xq] = sq.n[xq];
+            const int row0 = sq.row0[xq];
+            const int head = xq ? x.head_b : x.head * (1 + p.head_pairs);  // tile_head(p, x.head, xq)
+            // the offsets wait in shared memory while the tile loop runs (registers)
+            int64_t* epi = reinterpret_cast<int64_t*>(smem + L::kEpi) + 4 * (xq * kSoftmaxThreads + tid);
+            epi[0] = ((int64_t)(sq.q0 + row0) * p.num_heads + head) * D;  // the tile's first output element
+            epi[1] = (int64_t)head * p.total_q + sq.q0 + row0 + r;         // this row's lse index
+            // key limit of this row (bottom-right causal, inside the keys); tiles
+            // before jm need no mask for any row of the tile (its first row has
+            // the smallest limit)
+            vis0[xq] = min(row0 + r + sq.diag, sq.Lk - 1);
+            const int first = row0 + sq.diag;  // limit of the tile's first row
+            jm[xq] = min(first < kBN - 1 ? 0 : (first + 1) / kBN, sq.Lk / kBN);
+          }
+        }
+        // rows that see no key: zeros and lse = -inf (each half its 64 columns)
+  #pragma unroll
+        for (int xq = 0; xq < 2; ++xq) {
+          if (rows[xq] <= 0 || nkv[xq] != 0 || r >= rows[xq]) continue;
+          const int64_t* epi = reinterpret_cast<const int64_t*>(smem + L::kEpi) + 4 * (xq * kSoftmaxThreads + tid);
+          uint16_t* orow = p.out + epi[0] + (int64_t)r * p.num_heads * D;
+          for (int cc = hk * (D / 16); cc < (hk + 1) * (D / 16); ++cc)
+            reinterpret_cast<uint4*>(orow)[cc] = make_uint4(0, 0, 0, 0);
+          if (p.lse && hk == 0) p.lse[epi[1]] = -INFINITY;
+        }
+        const bool live_a = rows[0] > 0 && nkv[0] > 0, live_b = rows[1] > 0 && nkv[1] > 0;
+        const int nmax = max(live_a ? nkv[0] : 0, live_b ? nkv[1] : 0);
+        // one softmax step of tile xq over its K/V tile j
+        auto step = [&](const int xq, const int j) {
+          if (!mbar_wait(bar(kSFull0 + xq), sc[xq] & 1, abort_flag)) {
+            ok = false;
+            return;
+          }
+          ++sc[xq];
+          tc_fence_after();
+          // this half's 64 scores of the row in one TMEM round trip; P of its keys
+          // goes, as bf16 pairs, over the first 32 of its S columns (already read)
+          const int key0 = j * kBN + hk * 64;
+          uint32_t sr[64];
+          PKV_TMEM_LD32(tS(xq) + lane_off + hk * 64, (sr + 0));
+          PKV_TMEM_LD32(tS(xq) + lane_off + hk * 64 + 32, (sr + 32));
+          tmem_wait_ld();
+          if (j >= jm[xq]) {
+            const int vis = vis0[xq] - key0;  // columns 0..vis of this half are visible
+  #pragma unroll
+            for (int k = 0; k < 64; ++k) sr[k] = (k <= vis) ? sr[k] : __float_as_uint(-INFINITY);
+          }
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+          for (int k = 0; k < 64; k += 2)
+            mx4[(k >> 1) & 3] = fmax3(mx4[(k >> 1) & 3], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+          const float mine = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          const float mt = fmaxf(mine, exchange(mine)) * c;
+          if (!ok) return;
+          const float mo = m[xq];
+          float m_use = mo;
+          if (mt > mo + kRescaleThreshold || (mo == -INFINITY && mt != -INFINITY)) m_use = mt;
+          const bool live = m_use != -INFINITY;
+          const bool moved = m_use != mo;
+          const float alpha = (moved && mo != -INFINITY) ? fast_exp2(mo - m_use) : (moved ? 0.f : 1.f);
+          // p = 2^(s*c - m) on fp32 pairs; a row that saw no key yet (m = -inf) gives 0
+          const float nm = live ? -m_use : -INFINITY;
+          const uint64_t c2 = f32x2_pack(c, c), nm2 = f32x2_pack(nm, nm);
+          uint64_t sum2[2] = {0ull, 0ull};
+  #pragma unroll
           for (int k = 0; k < 64; k += 2) {
             float x0, x1;
-            f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(pk[k]), __uint_as_float(pk[k + 1])), c2, nm2), x0, x1);
+            f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nm2), x0, x1);
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             sum2[(k >> 1) & 1] = fadd2(sum2[(k >> 1) & 1], f32x2_pack(p0, p1));
-            pk[k >> 1] = kCoded ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            sr[k >> 1] = kCoded ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
-          PKV_TMEM_ST32(tS(xq) + lane_off + 64 * h, pk);
+          PKV_TMEM_ST32(tS(xq) + lane_off + hk * 64, sr);
+          float s00, s01, s10, s11;
+          f32x2_unpack(sum2[0], s00, s01);
+          f32x2_unpack(sum2[1], s10, s11);
+          l[xq] = l[xq] * alpha + ((s00 + s01) + (s10 + s11));
+          m[xq] = m_use;
+          // rescale this half's columns of O_X when the row's reference max moved
+          // (warp-collective TMEM access).  PV_X of the previous tile is done: it
+          // was issued before this tile's S, whose completion was just waited for.
+          if (j > 0 && __any_sync(0xffffffffu, moved && alpha != 1.f)) {
+  #pragma unroll
+            for (int ch = 0; ch < D / 64; ++ch) {
+              uint32_t o[32];
+              PKV_TMEM_LD32(tO(xq) + lane_off + hk * (D / 2) + ch * 32, o);
+              tmem_wait_ld();
+  #pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              PKV_TMEM_ST32(tO(xq) + lane_off + hk * (D / 2) + ch * 32, o);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(kPFull0 + xq));
+        };
+        for (int j = 0; j < nmax && ok; ++j) {
+          if (live_a && j < nkv[0]) step(0, j);
+          if (ok && live_b && j < nkv[1]) step(1, j);
         }
-        float s00, s01, s10, s11;
-        f32x2_unpack(sum2[0], s00, s01);
-        f32x2_unpack(sum2[1], s10, s11);
-        l = l * alpha + ((s00 + s01) + (s10 + s11));
-        m = m_use;
-        // rescale O_X when this row's reference max moved (warp-collective TMEM
-        // access).  PV_X of the previous tile is done: it was issued before this
-        // tile's S, whose completion was just waited for.
-        if (j > 0 && __any_sync(0xffffffffu, moved && alpha != 1.f)) {
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
+        if (!ok) break;
+        // ---- epilogue of each tile with keys: O_X / l, released once read, then stored ----
+  #pragma unroll
+        for (int xq = 0; xq < 2; ++xq) {
+          if (!(xq ? live_b : live_a)) continue;
+          const float lt = l[xq] + exchange(l[xq]);  // the whole row's sum
+          if (!ok) break;
+          if (!mbar_wait(bar(kODone0 + xq), oc[xq] & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++oc[xq];
+          tc_fence_after();
+          const float inv = lt > 0.f ? p.v_mul / lt : 0.f;
+          const int64_t* epi = reinterpret_cast<const int64_t*>(smem + L::kEpi) + 4 * (xq * kSoftmaxThreads + tid);
+          const bool row_valid = r < rows[xq];
+          uint4* orow = reinterpret_cast<uint4*>(p.out + epi[0] + (int64_t)r * p.num_heads * D);
+          // this half's D/2 columns of O, 32 at a time, normalised, packed to bf16
+          // and stored; O is released once every chunk is read
+  #pragma unroll
+          for (int cl = 0; cl < D / 64; ++cl) {
+            const int ch = hk * (D / 64) + cl;  // 32-column chunk of the row
             uint32_t o[32];
             PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o);
             tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            PKV_TMEM_ST32(tO(xq) + lane_off + ch * 32, o);
+            if (cl == D / 64 - 1) {
+              tc_fence_before();
+              mbar_arrive(bar(kOFree0 + xq));
+            }
+            if (row_valid) {
+              uint32_t w[16];
+  #pragma unroll
+              for (int k = 0; k < 16; ++k)
+                w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+              if (p.out_v8) {  // whole 32-byte sectors, half the store instructions
+  #pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + ch * 4 + 2 * h),
+                               "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]),
+                               "r"(w[8 * h + 4]), "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                               : "memory");
+              } else {
+  #pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  orow[ch * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+              }
+            }
           }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kPFull0 + xq));
-        if (j < nturn) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kTurn0 + (xq ^ 1)));
-          ++tc;
+          if (row_valid && hk == 0 && p.lse != nullptr)
+            p.lse[epi[1]] = lt > 0.f ? (m[xq] + log2f(lt)) * kLn2 : -INFINITY;
         }
       }
-      if (!ok) break;
-      // ---- epilogue: O_X / l, released as soon as it is read, then stored ----
-      if (!mbar_wait(bar(kODone0 + xq), oc & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      ++oc;
-      tc_fence_after();
-      const float inv = l > 0.f ? p.v_mul / l : 0.f;
-      obase = epi[0];
-      lse_idx = epi[1];
-      const bool row_valid = r < (int)epi[2];
-      // O, normalised, packed to bf16 and stored 32 columns at a time; O is
-      // released once read.  Head dim 64: the whole row in one TMEM round trip
-      // (64 registers).  Head dim 128: chunk by chunk, so that no 128-register
-      // row is live (that spilled and cost 2-6 %).
-      uint4* orow = reinterpret_cast<uint4*>(p.out + obase + (int64_t)r * p.num_heads * D);
-      constexpr int kOneTrip = D <= 64;
-      uint32_t o_all[kOneTrip ? D : 32];
-      if constexpr (kOneTrip) {
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, (o_all + ch * 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(kOFree0 + xq));
-      }
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        const uint32_t* o = o_all + (kOneTrip ? ch * 32 : 0);
-        if constexpr (!kOneTrip) {
-          PKV_TMEM_LD32(tO(xq) + lane_off + ch * 32, o_all);
-          tmem_wait_ld();
-          if (ch == D / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(bar(kOFree0 + xq));
-          }
-        }
-        if (row_valid) {
-          uint32_t w[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
-          if (p.out_v8) {  // whole 32-byte sectors, half the store instructions
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + ch * 4 + 2 * h),
-                           "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
-                           "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
-                           : "memory");
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) orow[ch * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-          }
-        }
-      }
-      if (row_valid && p.lse != nullptr) p.lse[lse_idx] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (!ok) fail();
+      tc_fence_before();
     }
-    if (!ok) fail();
-    tc_fence_before();
   } else {
     // ------------------------------------------------------------------ widening warp
     // One-byte caches: each landed Q, K and V tile of the published items, in
@@ -1627,17 +1827,22 @@ VarlenWs varlen_ws_layout(int batch, int route_items, int num_heads, int num_kv_
 
 template <int D, bool kPaged, int kCode = 0>
 int launch_prefill(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillParams& p,
-                   int batch, cudaStream_t st) {
-  auto kern = varlen_prefill_kernel<D, kPaged, kCode>;
-  const int smem = Smem<D>::kAlloc;
-  static bool attr_set[64] = {false};
+                   int batch, cudaStream_t st, bool unified = false) {
+  auto kern = varlen_prefill_kernel<D, kPaged, kCode, false>;
+  if constexpr (D == 128 && kCode == 0) {
+    if (unified) kern = varlen_prefill_kernel<D, kPaged, kCode, true>;
+  } else {
+    unified = false;
+  }
+  const int smem = unified ? Smem<D, true>::kAlloc : Smem<D>::kAlloc;
+  static bool attr_set[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 0 || dev >= 64) dev = 63;
-  if (!attr_set[dev]) {
+  if (!attr_set[unified][dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return PKV_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[unified][dev] = true;
   }
   const int64_t items = (int64_t)p.n_pairs * batch * p.item_heads;
   const int64_t sms = device_sm_count();
@@ -1855,12 +2060,15 @@ extern "C" int pkv_paged_attn_varlen(const void* q, const void* k, const void* v
                            err_flag) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
+  // Long keys (a bound of kUnifiedKeys or more): all softmax warps work on one
+  // tile at a time, two threads per row (faster K/V steps, costlier item ends)
+  const bool unified = max_len_k >= kUnifiedKeys;
   int rc = PKV_OK;
   if (all_routed)
     rc = launch_status();
   else if (head_dim == 128)
-    rc = packed_tiles                     ? launch_prefill<128, false>(mq, mk, mv, p, batch, st)
-         : !coded_tiles                   ? launch_prefill<128, true>(mq, mk, mv, p, batch, st)
+    rc = packed_tiles                     ? launch_prefill<128, false>(mq, mk, mv, p, batch, st, unified)
+         : !coded_tiles                   ? launch_prefill<128, true>(mq, mk, mv, p, batch, st, unified)
          : kv_dtype == PKV_FP8_E4M3       ? launch_prefill<128, true, 1>(mq, mk, mv, p, batch, st)
                                           : launch_prefill<128, true, 2>(mq, mk, mv, p, batch, st);
   else

@@ -21,10 +21,10 @@ def pkv():
     return built_library()
 
 
-def _packed(pkv, wl):
+def _packed(pkv, wl, max_len_k=None):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = pkv.paged_attn_varlen(wl.q, wl.k, wl.v, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.max_len_q,
-                                     wl.max_len_k, scale=wl.scale, return_lse=True, err_flag=err)
+                                     max_len_k or wl.max_len_k, scale=wl.scale, return_lse=True, err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
     return out, lse
@@ -73,12 +73,12 @@ def _write_new_tokens(pkv, wl):
     return kc, vc
 
 
-def _paged(pkv, wl, kc, vc, gather=False):
+def _paged(pkv, wl, kc, vc, gather=False, max_len_k=None):
     """Paged varlen; gather=True gives the library the bound that lets it gather K/V into a packed buffer."""
     shape4 = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = pkv.paged_attn_varlen(wl.q, kc.view(shape4), vc.view(shape4), wl.cu_seqlens_q, wl.cu_seqlens_k,
-                                     wl.max_len_q, wl.max_len_k, block_table=wl.block_table, scale=wl.scale,
+                                     wl.max_len_q, max_len_k or wl.max_len_k, block_table=wl.block_table, scale=wl.scale,
                                      return_lse=True, err_flag=err, gather_k_tokens=W.gather_tokens(wl) if gather else 0,
                                      k_scale=wl.extra.get("k_scale", 1.0), v_scale=wl.extra.get("v_scale", 1.0))
     torch.cuda.synchronize()
@@ -542,3 +542,39 @@ def test_multi_query_one_pass(pkv, case):
     atol, rtol = (BF16_ATOL, BF16_RTOL) if dt == "bf16" else (FP8_ATOL, FP8_RTOL)
     assert_close(f64(out), ref, atol, rtol, f"one-pass multi-query {case}")
     assert_close(f64(lse), ref_lse, 1e-3, 1e-3, f"one-pass multi-query lse {case}")
+
+
+# From this host key bound on, head dim 128 bf16 calls run the prefill kernel whose
+# softmax warps all work on one tile at a time (two threads per row).
+LONG_BOUND = 4096
+PACKED_128 = [c for c in PACKED if c[4] == 128] + [([256, 40], [5000, 40], 8, 2, 128)]
+
+
+@pytest.mark.parametrize("case", PACKED_128, ids=[f"{len(c[0])}seq_{c[2]}q{c[3]}kv_{i}" for i, c in
+                                                  enumerate(PACKED_128)])
+def test_varlen_packed_long_key_bound(pkv, case):
+    """The packed cases again with a key bound of LONG_BOUND (the one-tile softmax), against the oracle."""
+    q_lens, k_lens, Hq, Hkv, D = case
+    wl = W.make_varlen_packed(q_lens, k_lens, Hq, Hkv, D, seed=sum(q_lens) + 7 * Hq + D, device="cuda")
+    out, lse = _packed(pkv, wl, max_len_k=max(wl.max_len_k, LONG_BOUND))
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(wl.k), bits(wl.v), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True)
+    _check_rows(out, lse, ref, ref_lse, what=str(case))
+
+
+PAGED_128 = [c for c in PAGED if c[4] == 128]
+
+
+@pytest.mark.parametrize("gather", [False, True], ids=["direct", "gathered"])
+@pytest.mark.parametrize("case", PAGED_128, ids=[f"bs{c[5]}_{c[2]}q{c[3]}kv_{i}" for i, c in enumerate(PAGED_128)])
+def test_varlen_paged_long_key_bound(pkv, case, gather):
+    """The paged cases (routed single-query rows included) with a key bound of LONG_BOUND."""
+    q_lens, prefix, Hq, Hkv, D, bs = case
+    wl = W.make_varlen_paged(q_lens, prefix, Hq, Hkv, D, bs, seed=sum(q_lens) + sum(prefix) + bs, device="cuda",
+                             extra_blocks=3)
+    kc, vc = _write_new_tokens(pkv, wl)
+    out, lse = _paged(pkv, wl, kc, vc, gather=gather, max_len_k=max(wl.max_len_k, LONG_BOUND))
+    ref, ref_lse = O.paged_attn_varlen(bits(wl.q), bits(kc), bits(vc), wl.cu_seqlens_q.cpu().numpy(),
+                                       wl.cu_seqlens_k.cpu().numpy(), wl.scale, True,
+                                       block_table=wl.block_table.cpu().numpy(), block_size=bs)
+    _check_rows(out, lse, ref, ref_lse, what=str(case))
